@@ -1,0 +1,460 @@
+"""Benchmark of the FP8 paged-decode hot path on GB300.
+
+One step = the decode step of one attention layer of the Llama-3.1-8B-shaped
+workload under load: 8 sequences, contexts uniform in [18000, 22000], 32 query /
+8 KV heads, head_dim 128, page 16 with a shuffled page table, per-token-head
+e4m3 scales, 1% of (head, channel) pairs scaled x20.  Each step writes the 8 new
+tokens into the cache (kv_cache_write) and runs paged_decode_attn (+ split_merge)
+over all keys.  The same step on a bf16 cache is the in-run comparison.
+
+value = algorithmic HBM bytes of a step / step time (GB/s), with the cache
+resident in HBM; e2e = the same bytes over a step that also copies its inputs
+(q, new K/V, slots, lengths) from pinned host memory and reads the output back.
+Caches rotate over 4 copies (each > L2), so no step reads a previous step's data
+from L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank benchmarks its own GPU on its own batch (weak scaling,
+no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 paged-decode attn HBM GB/s (% of GB300 peak) & tokens/s vs bf16 KV"
+WORKLOAD = ("llama8b-decode: B=8, ctx~U[18000,22000], 32 Q / 8 KV heads, head_dim 128, page 16, "
+            "shuffled block_table, e4m3 per-token-head scales, 1% channels x20")
+ROTATIONS = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, group=None) -> float:
+    """Max over ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def reduce_sum(x: float, group=None) -> float:
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(bytes_per_step: float, tokens_per_step: float, seconds: float, steps: int):
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    t = reduce_max(seconds)
+    total_bytes = reduce_sum(bytes_per_step * steps)
+    total_tokens = reduce_sum(tokens_per_step * steps)
+    return total_bytes / t / 1e9, total_tokens / t, t
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "fp8_kv_cache_write_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_llama8b.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == kernel_source_hash():
+            return float(d["dram_bytes_per_launch_full_size"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workload
+def step_bytes(w, kv_elem_bytes: int, per_token_scales: bool):
+    """Algorithmic HBM bytes of one decode step: every visible key and value
+    byte once (+ per-token-head scales), q in, out (fp32) out, page-table
+    entries, and the cache write of the new tokens."""
+    ctx = w.context_lens.to(torch.int64)
+    n_tok = int(ctx.sum())
+    pages = int(((ctx + 15) // 16).sum())
+    kv = n_tok * w.Hkv * (2 * w.D * kv_elem_bytes + (8 if per_token_scales else 0))
+    q = w.B * w.Hq * w.D * 2
+    out = w.B * w.Hq * w.D * 4
+    bt = pages * 4
+    write = w.B * w.Hkv * (2 * w.D * 2 + 2 * w.D * kv_elem_bytes + (8 if per_token_scales else 0))
+    return kv + q + out + bt, write
+
+
+def build_caches(w, kv_dtype, dev, rotations):
+    import fp8_kv_cache_write_gb300 as fk
+    dt = torch.uint8 if kv_dtype == fk.KV_E4M3 else torch.bfloat16
+    k_hist, v_hist, hs = w.k_hist.to(dev), w.v_hist.to(dev), w.hist_slots.to(dev)
+    caches = []
+    for _ in range(rotations):
+        kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=dt, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.num_blocks, w.Hkv, 16, dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        fk.kv_cache_write(k_hist, v_hist, hs, kc, vc, kv_dtype=kv_dtype,
+                          scale_mode=w.scale_mode if kv_dtype == fk.KV_E4M3 else 0,
+                          k_scale_cache=ks, v_scale_cache=vs)
+        caches.append((kc, vc, ks, vs))
+    del k_hist, v_hist
+    torch.cuda.synchronize(dev)
+    return caches
+
+
+def run_ours(args, dev, w, world, rank):
+    import fp8_kv_cache_write_gb300 as fk
+
+    stream = torch.cuda.current_stream(dev)
+    q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
+    slots, bt, cl = w.new_slots.to(dev), w.block_table.to(dev), w.context_lens.to(dev)
+    mbs = bt.shape[1]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dec_bytes, write_bytes = {}, {}
+    results = {}
+    launches_per_step = {}
+
+    for kv_dtype, name in ((fk.KV_E4M3, "fp8"), (fk.KV_BF16, "bf16")):
+        mode = fk.SCALE_PER_TOKEN_HEAD if kv_dtype == fk.KV_E4M3 else 0
+        caches = build_caches(w, kv_dtype, dev, ROTATIONS)
+        splits, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0, 0)
+        ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+        out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
+        launches_per_step[name] = 1 + 1 + (1 if splits > 1 else 0)
+        d_b, w_b = step_bytes(w, 1 if kv_dtype == fk.KV_E4M3 else 2, kv_dtype == fk.KV_E4M3)
+        dec_bytes[name], write_bytes[name] = d_b, w_b
+
+        def step(i, k_in=kn, v_in=vn, s_in=slots, q_in=q, cl_in=cl, ev=None):
+            kc, vc, ks, vs = caches[i % ROTATIONS]
+            fk.kv_cache_write(k_in, v_in, s_in, kc, vc, kv_dtype=kv_dtype, scale_mode=mode,
+                              k_scale_cache=ks, v_scale_cache=vs, err_flag=err, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            fk.paged_decode_attn(q_in, kc, vc, bt, cl_in, kv_dtype=kv_dtype, scale_mode=mode,
+                                 k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=out,
+                                 err_flag=err, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        K = args.steps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(dev.index) if name == "fp8" else None
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for i in range(K):
+            step(i, ev=evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        clocks = sampler.stop() if sampler else None
+        secs = t0.elapsed_time(t1) / 1e3
+        dec_ms = [a.elapsed_time(b) for a, b in evs]
+        gbs, tok_s, tmax = aggregate(d_b + w_b, w.B, secs, K)
+        results[name] = {"gbs": gbs, "tokens_per_s": tok_s, "ms_per_step": tmax / K * 1e3,
+                         "decode_ms": statistics.mean(dec_ms), "num_splits": splits,
+                         "clocks": clocks, "secs": tmax}
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(err.item())} during the {name} run")
+
+        if name == "fp8":
+            # end to end: inputs from pinned host memory, output read back, each step
+            hq = w.q.pin_memory()
+            hk, hv = w.k_new.pin_memory(), w.v_new.pin_memory()
+            hs, hc = w.new_slots.pin_memory(), w.context_lens.pin_memory()
+            hout = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32).pin_memory()
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+            ds, dc = torch.empty_like(slots), torch.empty_like(cl)
+            h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hc))
+            d2h = hout.numel() * hout.element_size()
+
+            def e2e_step(i):
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                ds.copy_(hs, non_blocking=True)
+                dc.copy_(hc, non_blocking=True)
+                step(i, k_in=dk, v_in=dv, s_in=ds, q_in=dq, cl_in=dc)
+                hout.copy_(out, non_blocking=True)
+
+            for i in range(args.warmup):
+                e2e_step(i)
+            torch.cuda.synchronize(dev)
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(K):
+                e2e_step(i)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier()
+            e_secs = a.elapsed_time(b) / 1e3
+            e_gbs, e_tok, _ = aggregate(d_b + w_b, w.B, e_secs, K)
+            results["e2e"] = {"value": e_gbs, "unit": "GB/s", "tokens_per_s": e_tok,
+                              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del caches
+        torch.cuda.empty_cache()
+    return results, dec_bytes, launches_per_step
+
+
+class OracleBaseline:
+    """The oracle as it stands, timed on the host cores.  Its cache is written
+    once by the oracle's own cache write from the same bf16 inputs; each run
+    times decode attention for all query heads of the first `n_seq` sequences,
+    contexts optionally cut to the first n_tok tokens."""
+
+    def __init__(self, w, nthreads=None):
+        import numpy as np
+
+        import oracle
+        self.np, self.oracle, self.w = np, oracle, w
+        self.cores = nthreads or len(os.sched_getaffinity(0))
+        self.bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        nb, Hkv, D = w.num_blocks, w.Hkv, w.D
+        self.kc = np.zeros((nb, Hkv, 16, D), np.uint8)
+        self.vc = np.zeros_like(self.kc)
+        self.ks = np.zeros((nb, Hkv, 16), np.float32)
+        self.vs = np.zeros_like(self.ks)
+        for k, v, sl in ((w.k_hist, w.v_hist, w.hist_slots), (w.k_new, w.v_new, w.new_slots)):
+            st = oracle.kv_cache_write(self.bits(k), self.bits(v), sl.numpy(), self.kc, self.vc,
+                                       kv_dtype=0, scale_mode=2, k_scale_cache=self.ks,
+                                       v_scale_cache=self.vs)
+            assert st == 0
+        self.q = self.bits(w.q)
+        self.bt = w.block_table.numpy()
+
+    def run(self, n_seq=None, n_tok=None):
+        """Returns (GB/s, tokens/s, seconds, sample text)."""
+        np, w = self.np, self.w
+        seqs = list(range(w.B if n_seq is None else min(w.B, n_seq)))
+        units = [(sq, h) for sq in seqs for h in range(w.Hq)]
+        ctx = w.context_lens.numpy().copy()
+        if n_tok is not None:
+            ctx = np.minimum(ctx, n_tok)
+        t = time.perf_counter()
+        st, _ = self.oracle.decode_attn(self.q, self.kc, self.vc, self.bt, ctx, kv_dtype=0,
+                                        scale_mode=2, k_scale_cache=self.ks,
+                                        v_scale_cache=self.vs, units=units, nthreads=self.cores)
+        secs = time.perf_counter() - t
+        assert st == 0
+        n = int(ctx[seqs].sum())
+        bytes_ = n * w.Hkv * (2 * w.D + 8)
+        sample = (f"{len(seqs)} of {w.B} sequences x all {w.Hq} query heads, {n} context "
+                  f"tokens" + (f" (contexts cut to {n_tok})" if n_tok else ""))
+        return bytes_ / secs / 1e9, len(seqs) / secs, secs, sample
+
+
+def run_reference(args, w, world, rank):
+    """The oracle timed on the host cores, K steps of a bounded sample each."""
+    if rank != 0:
+        return None
+    ob = OracleBaseline(w)
+    budget = 120.0                                  # seconds for warmup + steps
+    per_step = budget / max(1, args.steps + args.warmup)
+    _, _, s_cal, _ = ob.run(n_seq=1, n_tok=512)     # calibration: 1 sequence, 512 tokens
+    n_tok = int(max(16, min(int(w.context_lens.min()), per_step / (s_cal / 512))))
+    for _ in range(args.warmup):
+        ob.run(n_seq=1, n_tok=n_tok)
+    tot_s, tot_b = 0.0, 0.0
+    sample = ""
+    for _ in range(args.steps):
+        gbs, tps, secs, sample = ob.run(n_seq=1, n_tok=n_tok)
+        tot_s += secs
+        tot_b += gbs * secs * 1e9
+    value = tot_b / tot_s / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_s / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": "host cores"},
+            "cpu_baseline": {"kind": "oracle", "cores": ob.cores, "value": value, "unit": "GB/s",
+                             "sample": sample + " per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from fp8_kv_cache_write_gb300 import synth
+    w = synth.llama8b(seed=1002 + rank)
+    if args.impl == "reference":
+        line = run_reference(args, w, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import fp8_kv_cache_write_gb300 as fk
+    fk.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    res, dec_bytes, lps = run_ours(args, dev, w, world, rank)
+    peak, peak_kind = measured_peaks()
+    fp8, bf16 = res["fp8"], res["bf16"]
+    achieved = dec_bytes["fp8"] / (fp8["decode_ms"] / 1e3) / 1e9
+    line = None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ob = OracleBaseline(w)
+        gbs, tps, secs, sample = ob.run()
+        cpu = {"value": gbs, "unit": "GB/s", "tokens_per_s": tps, "cores": ob.cores,
+               "kind": "oracle", "sample": sample + f"; {secs:.2f} s wall"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": fp8["gbs"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": fp8["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 8 * world,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"{ROTATIONS} rotating cache copies, each larger than L2",
+                       "num_splits": fp8["num_splits"]},
+            "pct_of_peak": fp8["gbs"] / peak,
+            "tokens_per_s": fp8["tokens_per_s"],
+            "bf16_twin": {"value": bf16["gbs"], "unit": "GB/s",
+                          "tokens_per_s": bf16["tokens_per_s"],
+                          "ms_per_step": bf16["ms_per_step"], "decode_ms": bf16["decode_ms"]},
+            "fp8_vs_bf16_tokens_per_s": fp8["tokens_per_s"] / bf16["tokens_per_s"],
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + split_merge)",
+                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profiled_traffic(),
+                         "algorithmic_bytes_per_launch": dec_bytes["fp8"],
+                         "decode_ms": fp8["decode_ms"]},
+            "cpu_baseline": cpu,
+            "e2e": res["e2e"],
+            "gpu_launches": lps["fp8"] * args.steps,
+            "clocks": fp8["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

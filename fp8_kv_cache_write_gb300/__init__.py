@@ -1,0 +1,191 @@
+"""fp8_kv_cache_write_gb300 -- Python binding of libfp8kv (FP8 paged KV cache and
+attention over it, hand-written CUDA for GB300 / sm_103a).
+
+This module only marshals arguments: it checks dtypes/devices, allocates outputs
+and workspaces with torch when the caller does not pass them, and calls the C
+ABI declared in include/fp8kv.h with raw device pointers and the current CUDA
+stream.  Every step of the computation runs in the library's kernels; there is
+no CPU fallback, and every call raises if libfp8kv.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8kv.so")
+
+PAGE_SIZE = 16
+KV_E4M3, KV_BF16 = 0, 1
+SCALE_PER_TENSOR, SCALE_PER_HEAD, SCALE_PER_TOKEN_HEAD = 0, 1, 2
+OUT_F32, OUT_BF16 = 0, 1
+
+STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
+          -3: "FP8KV_ERR_WORKSPACE", -4: "FP8KV_ERR_CUDA", -5: "FP8KV_ERR_TIMEOUT",
+          -6: "FP8KV_ERR_BAD_INDEX"}
+
+EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
+           "fp8kv_quantize_e4m3", "fp8kv_status_string", "fp8kv_last_warning")
+
+_lib = None
+
+
+class Fp8kvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def build(force: bool = False) -> str:
+    """Compile libfp8kv.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libfp8kv.so not found at {LIB_PATH}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        L.fp8kv_kv_cache_write.argtypes = [P, P, P, i64, i32, i32, P, P, i64, i32, i32, P, P, P,
+                                           P, P, P]
+        L.fp8kv_kv_cache_write.restype = i32
+        L.fp8kv_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32,
+                                        ctypes.POINTER(i32), ctypes.POINTER(sz)]
+        L.fp8kv_decode_plan.restype = i32
+        L.fp8kv_paged_decode_attn.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
+                                              i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
+        L.fp8kv_paged_decode_attn.restype = i32
+        L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
+        L.fp8kv_quantize_e4m3.restype = i32
+        L.fp8kv_status_string.argtypes = [i32]
+        L.fp8kv_status_string.restype = ctypes.c_char_p
+        L.fp8kv_last_warning.argtypes = []
+        L.fp8kv_last_warning.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fp8kv_status_string(int(status)).decode()
+
+
+def last_warning() -> str:
+    return lib().fp8kv_last_warning().decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype=None, device=True, contiguous=True):
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+def _raise(st, what):
+    if st != 0:
+        raise Fp8kvError(st, what)
+
+
+def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, *, kv_dtype, scale_mode=SCALE_PER_TENSOR,
+                   k_scale=None, v_scale=None, k_scale_cache=None, v_scale_cache=None,
+                   err_flag=None, stream=None) -> None:
+    """Store bf16 K/V rows [T][Hkv][D] at slot_mapping into the paged cache
+    (uint8 e4m3 or bf16 [num_blocks][Hkv][16][D]); see fp8kv_kv_cache_write."""
+    _check(k, "k", torch.bfloat16)
+    _check(v, "v", torch.bfloat16)
+    _check(slot_mapping, "slot_mapping", torch.int64)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
+                 ("v_scale_cache", v_scale_cache)):
+        _check(t, n, torch.float32)
+    _check(err_flag, "err_flag", torch.int32)
+    T, Hkv, D = k.shape
+    st = lib().fp8kv_kv_cache_write(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], kv_dtype, scale_mode, _ptr(k_scale), _ptr(v_scale),
+        _ptr(k_scale_cache), _ptr(v_scale_cache), _ptr(err_flag), _stream(stream))
+    _raise(st, "kv_cache_write")
+
+
+def decode_plan(B, Hq, Hkv, D, max_blocks_per_seq, window=0, num_splits=0):
+    """(num_splits, workspace_bytes) that paged_decode_attn will use."""
+    s = ctypes.c_int(0)
+    w = ctypes.c_size_t(0)
+    st = lib().fp8kv_decode_plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits,
+                                 ctypes.byref(s), ctypes.byref(w))
+    _raise(st, "decode_plan")
+    return s.value, w.value
+
+
+def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtype,
+                      scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
+                      k_scale_cache=None, v_scale_cache=None, softmax_scale=None, window=0,
+                      num_splits=0, workspace=None, out=None, out_dtype=OUT_F32, err_flag=None,
+                      stream=None):
+    """Decode attention of q [B][Hq][D] (bf16) over the paged cache; returns out
+    [B][Hq][D] (fp32 or bf16).  See fp8kv_paged_decode_attn."""
+    _check(q, "q", torch.bfloat16)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
+    _check(block_table, "block_table", torch.int32)
+    _check(context_lens, "context_lens", torch.int32)
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
+                 ("v_scale_cache", v_scale_cache)):
+        _check(t, n, torch.float32)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    mbs = block_table.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    splits, ws_bytes = decode_plan(B, Hq, Hkv, D, mbs, window, num_splits)
+    if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size()
+                         < ws_bytes):
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty(B, Hq, D, device=q.device,
+                          dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    st = lib().fp8kv_paged_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), kv_dtype, scale_mode, _ptr(k_scale),
+        _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache), _ptr(block_table), mbs,
+        _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), int(window),
+        int(num_splits), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
+        out_dtype, _ptr(err_flag), _stream(stream))
+    _raise(st, "paged_decode_attn")
+    return out
+
+
+def quantize_e4m3(x, scale=1.0, out=None, stream=None):
+    """e4m3 codes (uint8) of fp32 x / scale, computed on the GPU."""
+    _check(x, "x", torch.float32)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(out, "out", torch.uint8)
+    st = lib().fp8kv_quantize_e4m3(_ptr(x), float(scale), _ptr(out), x.numel(), _stream(stream))
+    _raise(st, "quantize_e4m3")
+    return out

@@ -1,0 +1,326 @@
+// api.cu -- the extern "C" boundary of libfp8kv: host-side validation, the
+// decode split planner, TMA tensor-map encoding and kernel launches.  Every
+// check runs before the first launch, so an invalid call launches nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fp8kv.h"
+#include "internal.h"
+
+namespace {
+
+using namespace fp8kv;
+
+thread_local std::string g_warning;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// SM count of the current device (cached per device; 152 if none is visible).
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map over a paged cache [num_blocks * Hkv][16][row_bytes] (bytes):
+// boxes of 16 rows x 128 bytes with 128-byte swizzle (64-byte rows are viewed
+// as 8 rows of 128 bytes, two tokens each).  Encodings are cached per thread.
+struct MapKey {
+    const void* base;
+    int row_bytes;
+    int64_t nbh;
+};
+
+bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out) {
+    struct Entry {
+        MapKey key;
+        CUtensorMap map;
+        bool used;
+    };
+    thread_local Entry cache[8] = {};
+    thread_local int next = 0;
+    for (auto& e : cache)
+        if (e.used && e.key.base == base && e.key.row_bytes == row_bytes && e.key.nbh == nbh) {
+            *out = e.map;
+            return true;
+        }
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (row_bytes == 64) {
+        dims[0] = 128; dims[1] = 8; dims[2] = static_cast<cuuint64_t>(nbh);
+        strides[0] = 128; strides[1] = 1024;
+        box[0] = 128; box[1] = 8; box[2] = 1;
+    } else {
+        dims[0] = static_cast<cuuint64_t>(row_bytes); dims[1] = 16;
+        dims[2] = static_cast<cuuint64_t>(nbh);
+        strides[0] = static_cast<cuuint64_t>(row_bytes);
+        strides[1] = static_cast<cuuint64_t>(row_bytes) * 16;
+        box[0] = 128; box[1] = 16; box[2] = 1;
+    }
+    CUtensorMap m;
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    cache[next] = Entry{MapKey{base, row_bytes, nbh}, m, true};
+    next = (next + 1) % 8;
+    *out = m;
+    return true;
+}
+
+struct Plan {
+    int num_splits;
+    int pages_per_split;
+    size_t workspace_bytes;
+};
+
+// Split planner.  The visible pages of a sequence are at most max_blocks (or,
+// with a window w, ceil(w/16)+1).  Automatic: about 4 CTAs per SM of page
+// work in total, 16..128 pages per split; the split count is then rebalanced
+// so every split but the last has the same number of pages.
+int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out) {
+    int maxvis = max_blocks;
+    if (window > 0) {
+        const int wp = (window + FP8KV_PAGE_SIZE - 1) / FP8KV_PAGE_SIZE + 1;
+        if (wp < maxvis) maxvis = wp;
+    }
+    if (maxvis < 1) maxvis = 1;
+    int S;
+    if (req > 0) {
+        S = req < maxvis ? req : maxvis;
+    } else {
+        const int64_t work = static_cast<int64_t>(B) * Hkv * maxvis;
+        const int64_t target = static_cast<int64_t>(sm_count()) * 4;
+        int64_t pps = (work + target - 1) / target;
+        if (pps < 16) pps = 16;
+        if (pps > 128) pps = 128;
+        S = static_cast<int>((maxvis + pps - 1) / pps);
+    }
+    if (S > 1024) S = 1024;
+    if (S < 1) S = 1;
+    int pps = (maxvis + S - 1) / S;
+    S = (maxvis + pps - 1) / pps;
+    out->num_splits = S;
+    out->pages_per_split = pps;
+    out->workspace_bytes =
+        S > 1 ? static_cast<size_t>(B) * Hq * S * (static_cast<size_t>(D) + 2) * sizeof(float) : 0;
+    return FP8KV_OK;
+}
+
+bool valid_d(int D) { return D == 64 || D == 128 || D == 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8kv_status_string(int status) {
+    switch (status) {
+        case FP8KV_OK: return "ok";
+        case FP8KV_ERR_INVALID: return "invalid argument";
+        case FP8KV_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case FP8KV_ERR_WORKSPACE: return "workspace too small";
+        case FP8KV_ERR_CUDA: return "CUDA error";
+        case FP8KV_ERR_TIMEOUT: return "device wait timed out";
+        case FP8KV_ERR_BAD_INDEX: return "block id or slot outside the cache";
+        default: return "unknown status";
+    }
+}
+
+const char* fp8kv_last_warning(void) { return g_warning.c_str(); }
+
+int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T,
+                         int Hkv, int D, void* k_cache, void* v_cache, int64_t num_blocks,
+                         int kv_dtype, int scale_mode, const float* k_scale, const float* v_scale,
+                         float* k_scale_cache, float* v_scale_cache, int32_t* err_flag,
+                         void* cuda_stream) {
+    g_warning.clear();
+    if (T < 0 || Hkv <= 0 || num_blocks < 0) return FP8KV_ERR_INVALID;
+    if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
+    if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
+    if (kv_dtype == FP8KV_KV_E4M3 && (scale_mode < FP8KV_SCALE_PER_TENSOR ||
+                                      scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD))
+        return FP8KV_ERR_INVALID;
+    if (T == 0) return FP8KV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return FP8KV_ERR_INVALID;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8) ||
+        !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return FP8KV_ERR_INVALID;
+    if (kv_dtype == FP8KV_KV_E4M3) {
+        if (scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) {
+            if (!k_scale_cache || !v_scale_cache || !aligned(k_scale_cache, 4) ||
+                !aligned(v_scale_cache, 4))
+                return FP8KV_ERR_INVALID;
+        } else if (!k_scale || !v_scale) {
+            return FP8KV_ERR_INVALID;
+        }
+    }
+    WriteParams p{};
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.slot_mapping = slot_mapping;
+    p.T = T;
+    p.Hkv = Hkv;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.num_blocks = num_blocks;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.k_scale_cache = k_scale_cache;
+    p.v_scale_cache = v_scale_cache;
+    p.err = err_flag;
+    cudaError_t e = launch_kv_cache_write(p, D, kv_dtype, scale_mode,
+                                          static_cast<cudaStream_t>(cuda_stream), sm_count());
+    return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int window,
+                      int num_splits, int* num_splits_out, size_t* workspace_bytes_out) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq < 0 || window < 0 ||
+        num_splits < 0)
+        return FP8KV_ERR_INVALID;
+    if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
+    Plan pl;
+    plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &pl);
+    if (num_splits_out) *num_splits_out = pl.num_splits;
+    if (workspace_bytes_out) *workspace_bytes_out = pl.workspace_bytes;
+    return FP8KV_OK;
+}
+
+int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                            int kv_dtype, int scale_mode, const float* k_scale,
+                            const float* v_scale, const float* k_scale_cache,
+                            const float* v_scale_cache, const int32_t* block_table,
+                            int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
+                            int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
+                            int num_splits, void* workspace, size_t workspace_bytes, void* out,
+                            int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    g_warning.clear();
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || window < 0 || num_splits < 0 ||
+        max_blocks_per_seq < 0 || num_blocks < 0)
+        return FP8KV_ERR_INVALID;
+    if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 8) return FP8KV_ERR_UNSUPPORTED;
+    if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
+    if (kv_dtype == FP8KV_KV_E4M3 && (scale_mode < FP8KV_SCALE_PER_TENSOR ||
+                                      scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD))
+        return FP8KV_ERR_INVALID;
+    if (out_dtype != FP8KV_OUT_F32 && out_dtype != FP8KV_OUT_BF16) return FP8KV_ERR_INVALID;
+    if (!(softmax_scale == softmax_scale)) return FP8KV_ERR_INVALID;   // NaN
+    if (B == 0) return FP8KV_OK;
+    if (B > 65535 || Hkv > 65535 || max_blocks_per_seq < 1 || num_blocks < 1)
+        return FP8KV_ERR_INVALID;
+    if (num_blocks * static_cast<int64_t>(Hkv) >= (int64_t{1} << 31))
+        return FP8KV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_blocks_per_seq) * FP8KV_PAGE_SIZE >= (int64_t{1} << 31))
+        return FP8KV_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+        return FP8KV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+        return FP8KV_ERR_INVALID;
+    if (kv_dtype == FP8KV_KV_E4M3) {
+        if (scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) {
+            if (!k_scale_cache || !v_scale_cache || !aligned(k_scale_cache, 16) ||
+                !aligned(v_scale_cache, 16))
+                return FP8KV_ERR_INVALID;
+        } else if (!k_scale || !v_scale) {
+            return FP8KV_ERR_INVALID;
+        }
+    }
+    Plan pl;
+    plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &pl);
+    if (pl.num_splits > 1) {
+        if (!workspace || workspace_bytes < pl.workspace_bytes) return FP8KV_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
+    }
+    const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
+    const int64_t nbh = num_blocks * Hkv;
+    CUtensorMap kmap, vmap;
+    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap) || !make_kv_map(v_cache, row_bytes, nbh, &vmap))
+        return FP8KV_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.k_scale_cache = k_scale_cache;
+    p.v_scale_cache = v_scale_cache;
+    p.block_table = block_table;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.window = window;
+    p.num_splits = pl.num_splits;
+    p.pages_per_split = pl.pages_per_split;
+    if (pl.num_splits > 1) {
+        float* ws = static_cast<float*>(workspace);
+        const size_t rows = static_cast<size_t>(B) * Hq * pl.num_splits;
+        p.ws_o = ws;
+        p.ws_m = ws + rows * D;
+        p.ws_l = p.ws_m + rows;
+    }
+    p.out = out;
+    p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
+    p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
+    p.err = err_flag;
+    cudaError_t e =
+        launch_paged_decode(p, kmap, vmap, D, kv_dtype, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
+                        void* cuda_stream) {
+    g_warning.clear();
+    if (n < 0) return FP8KV_ERR_INVALID;
+    if (n == 0) return FP8KV_OK;
+    if (!x || !out) return FP8KV_ERR_INVALID;
+    cudaError_t e =
+        launch_quantize_e4m3(x, scale, out, n, static_cast<cudaStream_t>(cuda_stream), sm_count());
+    return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+}  // extern "C"

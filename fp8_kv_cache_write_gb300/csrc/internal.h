@@ -1,0 +1,69 @@
+// internal.h -- kernel parameter blocks and launchers shared between the
+// kernels' translation units and the C-ABI layer (api.cu).  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8kv {
+
+struct WriteParams {
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const int64_t* slot_mapping;
+    int64_t T;
+    int Hkv;
+    void* k_cache;
+    void* v_cache;
+    int64_t num_blocks;
+    const float* k_scale;
+    const float* v_scale;
+    float* k_scale_cache;
+    float* v_scale_cache;
+    int32_t* err;
+};
+
+cudaError_t launch_kv_cache_write(const WriteParams& p, int D, int kv_dtype, int mode,
+                                  cudaStream_t stream, int num_sms);
+cudaError_t launch_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
+                                 cudaStream_t stream, int num_sms);
+
+// Split-K decode.  Split s of (seq b, KV head h) covers visible pages
+// [p_lo + s*pages_per_split, min(p_lo + (s+1)*pages_per_split, p_hi)) where
+// p_lo/p_hi bound the pages holding positions [lo, ctx).
+struct DecodeParams {
+    const __nv_bfloat16* q;
+    const float* k_scale;        // per tensor / per head (fp8 only)
+    const float* v_scale;
+    const float* k_scale_cache;  // per token-head (fp8 only)
+    const float* v_scale_cache;
+    const int32_t* block_table;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;
+    int B, Hq, Hkv, G;
+    int64_t num_blocks;
+    float scale_log2;            // softmax_scale * log2(e)
+    int window;
+    int num_splits;
+    int pages_per_split;
+    float* ws_m;                 // [B*Hq][num_splits] running max (log2 units)
+    float* ws_l;                 // [B*Hq][num_splits] softmax denominator
+    float* ws_o;                 // [B*Hq][num_splits][D] unnormalised output
+    void* out;                   // [B][Hq][D]
+    int out_bf16;
+    int scale_mode;
+    int32_t* err;
+};
+
+// Launches the split kernel and (when num_splits > 1) the merge kernel.
+cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, int D, int kv_dtype,
+                                cudaStream_t stream);
+
+// Decode kernel geometry used by the planner and the tensor maps.
+constexpr int kDecodeWarps = 4;
+int decode_ctas_per_sm(int D, int kv_dtype);
+
+}  // namespace fp8kv

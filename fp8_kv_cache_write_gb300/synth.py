@@ -64,7 +64,7 @@ def slots_for(block_table, seq_positions):
     """Slot (block * 16 + offset) of each (seq, position) pair, int64."""
     out = torch.empty(len(seq_positions), dtype=torch.int64)
     for i, (s, p) in enumerate(seq_positions):
-        out[i] = int(block_table[s, p // PAGE]) * PAGE + p % PAGE
+        out[i] = int(block_table[s, p // PAGE]) * PAGE + p % PAGE if p >= 0 else -1
     return out
 
 
@@ -255,3 +255,16 @@ def prefill(seed=1005, device="cpu", ctx=(32768,), chunk=(4096,), Hq=8, Hkv=1,
     one = torch.ones(1, dtype=torch.float32)
     return PrefillWorkload("prefill", Hq, Hkv, D, ctx, cu, bt, nb, k_all, v_all, slots, q,
                            one, one.clone())
+
+
+def decode_workload(seed, context_lens, Hq, Hkv, D, scale_mode, outlier_frac=0.0,
+                    spare_blocks=0, window=0, name="custom") -> DecodeWorkload:
+    """A decode step with explicit context lengths (parity tests' ragged cases).
+    Per-tensor / per-head scales default to 1.0 / a per-head calibration."""
+    w = _decode_common(name, seed, context_lens, Hq, Hkv, D, scale_mode,
+                       outlier_frac=outlier_frac, spare_blocks=spare_blocks)
+    w.window = window
+    if scale_mode == 1:
+        w.k_scale = per_head_calibration(torch.cat([w.k_hist, w.k_new]))
+        w.v_scale = per_head_calibration(torch.cat([w.v_hist, w.v_new]))
+    return w

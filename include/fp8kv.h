@@ -1,0 +1,170 @@
+/*
+ * fp8kv.h -- C ABI of libfp8kv: an FP8 (e4m3) paged KV cache and attention
+ * directly over it, hand-written for GB300 (sm_103a).
+ *
+ * What the library computes follows these pages (cited by title and section):
+ *   [KO]  "vLLM FP8 KV-Cache 및 Attention 양자화 업데이트" (agentlenshq.com):
+ *         storing K/V as FP8 e4m3 halves the KV cache and attention then runs
+ *         over FP8 data (opening paragraph); per-KV-head scale arrays
+ *         ("커널 및 퓨전 최적화"); uncalibrated scale 1.0 ("정확도 및 검증");
+ *         sliding-window layers kept in BF16 ("하이브리드 Attention 및 레이어
+ *         스킵"); two-level FP32 accumulation for long contractions
+ *         ("정확도를 위한 2단계 누적"), not needed on Blackwell ("아키텍처별 결과").
+ *   [KVQ] "[vLLM] KV Cache Quantization: KV 캐시 FP8/INT8 양자화"
+ *         (blog.secrett2633.cloud): per-tensor K/V scale from a checkpoint or
+ *         1.0, or per-token-head scales that the kernel computes when it stores
+ *         the cache ("Per-Token-Head vs Per-Tensor 양자화"); q and prob scales
+ *         for FP8 attention and the uncalibrated-scale warning ("Q/Prob 스케일과
+ *         FP8 Attention").
+ *   [PR]  "vLLM Qwen3.8-Flash-Next: QSA Indexer 캐시를 위한 FP8 지원" (same blog):
+ *         torch.float8_e4m3fn storage and paged caches with a shuffled page
+ *         table ("코드 분석").
+ *
+ * Conventions for every entry point
+ *   - Ownership: the caller owns every buffer.  Array arguments are DEVICE
+ *     pointers on the current CUDA device (from cudaMalloc or a framework's
+ *     allocator); the library allocates nothing and keeps no pointer after the
+ *     call returns.  Scalars are host values.
+ *   - Streams: work is enqueued on `cuda_stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and nothing synchronizes.
+ *   - Errors: a negative fp8kv_status is returned, never an exception.  Host
+ *     checks run before any launch, so an invalid call launches nothing.  Errors
+ *     found by a kernel (a block id or slot outside the cache, a timed-out wait)
+ *     are written to `*err_flag` (device int32, first error wins; NULL = do not
+ *     report) and the offending page/row is skipped; read it after a sync.
+ *   - Cache layout (page size 16): k_cache / v_cache are
+ *     [num_blocks][Hkv][16][D] of e4m3 bytes (kv_dtype E4M3) or bf16
+ *     (kv_dtype BF16); one (block, head) tile is 16*D contiguous elements.
+ *     Per-token-head scales live beside the pages in fp32
+ *     k_scale_cache / v_scale_cache [num_blocks][Hkv][16], indexed by the same
+ *     block id and in-page offset.
+ *   - Supported shapes: D in {64, 128, 256}; Hq % Hkv == 0; Hq / Hkv <= 8 for
+ *     attention; base addresses 16-byte aligned.
+ */
+#ifndef FP8KV_H
+#define FP8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8KV_PAGE_SIZE 16
+
+typedef enum {
+    FP8KV_OK = 0,
+    FP8KV_ERR_INVALID = -1,     /* a pointer, size or enum value is invalid */
+    FP8KV_ERR_UNSUPPORTED = -2, /* valid but not implemented (shape, mode) */
+    FP8KV_ERR_WORKSPACE = -3,   /* workspace too small */
+    FP8KV_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    FP8KV_ERR_TIMEOUT = -5,     /* device: a bounded wait expired (err_flag) */
+    FP8KV_ERR_BAD_INDEX = -6    /* device: block id / slot outside the cache (err_flag) */
+} fp8kv_status;
+
+typedef enum { FP8KV_KV_E4M3 = 0, FP8KV_KV_BF16 = 1 } fp8kv_kv_dtype;
+
+typedef enum {
+    FP8KV_SCALE_PER_TENSOR = 0,     /* k_scale[0], v_scale[0] ([KVQ] per-tensor; 1.0 uncalibrated) */
+    FP8KV_SCALE_PER_HEAD = 1,       /* k_scale[h], v_scale[h] ([KO] per-KV-head scale arrays) */
+    FP8KV_SCALE_PER_TOKEN_HEAD = 2  /* computed at write time ([KVQ] per-token-head) */
+} fp8kv_scale_mode;
+
+typedef enum { FP8KV_OUT_F32 = 0, FP8KV_OUT_BF16 = 1 } fp8kv_out_dtype;
+
+/*
+ * fp8kv_kv_cache_write -- store T new tokens of K and V into the paged cache.
+ * [KO] opening paragraph (e4m3 storage), [KVQ] "Per-Token-Head vs Per-Tensor
+ * 양자화" (scale modes).
+ *
+ *   k, v          bf16 [T][Hkv][D], row-major.
+ *   slot_mapping  int64 [T]: slot = block * 16 + offset; a negative slot skips
+ *                 the token (padding).  A slot at or past num_blocks * 16 sets
+ *                 FP8KV_ERR_BAD_INDEX in err_flag and is skipped.
+ *   kv_dtype      E4M3: codes e4m3_rn_satfinite(fp32(x / scale)); BF16: a copy.
+ *   scale_mode    (E4M3 only) PER_TENSOR: scale = k_scale[0] / v_scale[0];
+ *                 PER_HEAD: k_scale[h] / v_scale[h]; PER_TOKEN_HEAD: scale =
+ *                 fp32(max_d |x_d| / 448) per (token, head), written to
+ *                 k_scale_cache / v_scale_cache.  A zero scale writes code 0.
+ *   k_scale, v_scale  fp32 device arrays of 1 or Hkv entries (ignored for
+ *                 PER_TOKEN_HEAD and BF16).
+ * The division is an IEEE fp32 divide and the encoding rounds to nearest even,
+ * so codes and scales are bit-identical to a plain CPU restatement.
+ */
+int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T,
+                         int Hkv, int D, void* k_cache, void* v_cache, int64_t num_blocks,
+                         int kv_dtype, int scale_mode, const float* k_scale, const float* v_scale,
+                         float* k_scale_cache, float* v_scale_cache, int32_t* err_flag,
+                         void* cuda_stream);
+
+/*
+ * fp8kv_decode_plan -- how fp8kv_paged_decode_attn splits the context and the
+ * workspace it needs (pure host function, no CUDA call besides reading the
+ * current device's SM count).
+ *
+ *   max_blocks_per_seq  columns of block_table (upper bound on pages per sequence)
+ *   window              0 = full attention, else the last `window` keys
+ *   num_splits          0 = choose automatically, else the requested split count
+ *   *num_splits_out     the split count the kernel will use
+ *   *workspace_bytes_out  bytes of fp32 workspace needed (0 when one split)
+ */
+int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int window,
+                      int num_splits, int* num_splits_out, size_t* workspace_bytes_out);
+
+/*
+ * fp8kv_paged_decode_attn -- one query token per sequence attends to its paged
+ * FP8 (or bf16) cache: split-K flash decoding plus a split-merge kernel.
+ * [KO] opening paragraph (attention over the FP8 cache), "커널 및 퓨전 최적화"
+ * (per-KV-head scales), "하이브리드 Attention 및 레이어 스킵" (window on a bf16
+ * cache); [KVQ] "Per-Token-Head vs Per-Tensor 양자화" (per-token-head scales).
+ *
+ *   q              bf16 [B][Hq][D]; query head hq reads KV head hq / (Hq / Hkv).
+ *   k_cache, v_cache, kv_dtype, scale_mode  as written by fp8kv_kv_cache_write;
+ *                  the bf16 cache ignores scales.
+ *   k_scale, v_scale              fp32 [1] or [Hkv] (PER_TENSOR / PER_HEAD).
+ *   k_scale_cache, v_scale_cache  fp32 [num_blocks][Hkv][16] (PER_TOKEN_HEAD).
+ *   block_table    int32 [B][max_blocks_per_seq]: page p of sequence b is block
+ *                  block_table[b][p]; entries past the sequence are not read.
+ *   context_lens   int32 [B]: keys of sequence b are positions 0 .. ctx-1
+ *                  (the new token already written); ctx 0 gives a zero row.
+ *   softmax_scale  logits are softmax_scale * q . k (usually 1/sqrt(D)).
+ *   window         0 = all keys; w > 0 = keys at positions >= ctx - w.
+ *   num_splits     0 = automatic (see fp8kv_decode_plan).
+ *   workspace      fp32 scratch of at least the planned bytes (may be NULL when
+ *                  the plan needs none); its contents need no initialisation.
+ *   out            [B][Hq][D] fp32 or bf16 (out_dtype).
+ * Output: softmax(z) V over the visible keys, accumulated in fp32.
+ */
+int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                            int kv_dtype, int scale_mode, const float* k_scale,
+                            const float* v_scale, const float* k_scale_cache,
+                            const float* v_scale_cache, const int32_t* block_table,
+                            int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
+                            int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
+                            int num_splits, void* workspace, size_t workspace_bytes, void* out,
+                            int out_dtype, int32_t* err_flag, void* cuda_stream);
+
+/*
+ * fp8kv_quantize_e4m3 -- the cache writer's encoder on its own: out[i] =
+ * e4m3_rn_satfinite(fp32(x[i] / scale)) for n fp32 values (device arrays).
+ * [PR] "코드 분석" (torch.float8_e4m3fn storage).  A zero scale writes code 0.
+ */
+int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
+                        void* cuda_stream);
+
+/* Human-readable name of a status code (static string). */
+const char* fp8kv_status_string(int status);
+
+/*
+ * Last warning raised by a call on this thread, or "" if none: FP8 attention
+ * with uncalibrated q/prob scales of 1.0 warns as [KVQ] "Q/Prob 스케일과 FP8
+ * Attention" describes.  The string stays valid until the next call.
+ */
+const char* fp8kv_last_warning(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H */

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every symbol include/fp8kv.h declares, and
+rejects invalid host arguments before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_kv_cache_write_gb300 as fk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fk.build()
+    return fk.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8kv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_exports():
+    assert _declared_functions() == sorted(fk.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert fk.status_string(code) not in ("", "unknown status")
+    assert fk.status_string(17) == "unknown status"
+    assert fk.last_warning() == ""
+
+
+def test_decode_plan_is_consistent(lib):
+    for B, Hq, Hkv, D, mbs, win in [(8, 32, 8, 128, 1375, 0), (1, 64, 8, 128, 8192, 0),
+                                    (32, 64, 8, 64, 2048, 128), (1, 32, 8, 128, 64, 0)]:
+        s, ws = fk.decode_plan(B, Hq, Hkv, D, mbs, win)
+        assert 1 <= s <= 1024
+        assert ws == (0 if s == 1 else B * Hq * s * (D + 2) * 4)
+        for req in (1, 2, 7):
+            s2, _ = fk.decode_plan(B, Hq, Hkv, D, mbs, win, req)
+            assert 1 <= s2 <= req
+    # a window bounds the visible pages: 128 keys touch at most 9 pages
+    s, _ = fk.decode_plan(1, 8, 8, 64, 4096, 128, 1000)
+    assert s <= 9
+
+
+def _null():
+    return ctypes.c_void_p(0)
+
+
+def test_write_rejects_bad_arguments_without_a_gpu(lib):
+    N = _null()
+    call = lambda **kw: lib.fp8kv_kv_cache_write(
+        kw.get("k", N), kw.get("v", N), kw.get("slots", N), kw.get("T", 4), kw.get("Hkv", 2),
+        kw.get("D", 128), kw.get("kc", N), kw.get("vc", N), 10, kw.get("dtype", 0),
+        kw.get("mode", 0), N, N, N, N, N, N)
+    assert call() == -1            # null pointers
+    assert call(D=96) == -2
+    assert call(dtype=5) == -1
+    assert call(mode=3) == -1
+    assert call(T=-1) == -1
+    assert call(T=0) == 0          # nothing to do, nothing launched
+
+
+def test_decode_rejects_bad_arguments_without_a_gpu(lib):
+    N = _null()
+
+    def call(B=2, Hq=8, Hkv=2, D=128, dtype=0, mode=0, out_dtype=0, window=0, splits=0):
+        return lib.fp8kv_paged_decode_attn(N, N, N, dtype, mode, N, N, N, N, N, 4, N, B, Hq, Hkv,
+                                           D, 10, 0.1, window, splits, N, 0, N, out_dtype, N, N)
+
+    assert call() == -1            # null pointers
+    assert call(Hq=9) == -1        # Hq % Hkv
+    assert call(Hq=32, Hkv=2) == -2   # group of 16 query heads
+    assert call(D=80) == -2
+    assert call(dtype=2) == -1
+    assert call(mode=7) == -1
+    assert call(out_dtype=3) == -1
+    assert call(window=-1) == -1
+    assert call(B=0) == 0
+
+
+def test_quantize_rejects_bad_arguments_without_a_gpu(lib):
+    assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), 5, _null()) == -1
+    assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), 0, _null()) == 0
+    assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), -1, _null()) == -1

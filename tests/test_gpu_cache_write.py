@@ -1,0 +1,123 @@
+"""GPU parity of kv_cache_write and the e4m3 encoder: bit-exact against the oracle.
+
+Cache codes and stored per-token-head scales must equal the oracle's byte for
+byte (scale = fp32(amax / 448), code = e4m3_rn_satfinite(fp32(x / scale)); "[vLLM]
+KV Cache Quantization: KV 캐시 FP8/INT8 양자화", section "Per-Token-Head vs Per-Tensor
+양자화").  The encoder is also swept over every fp32 bit pattern.
+"""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_kv_cache_write_gb300 as fk
+from fp8_kv_cache_write_gb300 import synth
+from tests._helpers import bits16
+from tests._parity import assert_same_cache, gpu_fill, oracle_cache
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
+def test_cache_write_bit_exact(D, kv_dtype, mode):
+    w = synth.decode_workload(11 + D, [1, 15, 16, 17, 300, 1000], 8, 4, D, mode,
+                              outlier_frac=0.01, spare_blocks=5)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gc = gpu_fill(w, kv_dtype, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_same_cache(gc, oracle_cache(w, kv_dtype))
+
+
+def test_llama_shaped_bulk_fill_bit_exact():
+    # Llama-3.1-8B-shaped cache fill: 8 KV heads, D 128, outlier channels x20.
+    w = synth.llama8b(seed=21, B=2, ctx_lo=3000, ctx_hi=5000)
+    assert_same_cache(gpu_fill(w, 0), oracle_cache(w, 0))
+
+
+def test_zero_rows_negative_slots_and_untouched_bytes():
+    T, Hkv, D, nb = 40, 2, 128, 6
+    g = torch.Generator().manual_seed(3)
+    k = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    k[5] = 0                                              # all-zero rows: scale 0, codes 0
+    v = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int64)
+    slots[::7] = -1                                       # padding tokens are skipped
+    kc = torch.full((nb, Hkv, 16, D), 0x5A, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    ks = torch.full((nb, Hkv, 16), -3.0, device="cuda")
+    vs = ks.clone()
+    fk.kv_cache_write(k.cuda(), v.cuda(), slots.cuda(), kc, vc, kv_dtype=0, scale_mode=2,
+                      k_scale_cache=ks, v_scale_cache=vs)
+    okc = np.full((nb, Hkv, 16, D), 0x5A, np.uint8)
+    ovc = okc.copy()
+    oks = np.full((nb, Hkv, 16), -3.0, np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_cache_write(bits16(k), bits16(v), slots.numpy(), okc, ovc, kv_dtype=0,
+                                 scale_mode=2, k_scale_cache=oks, v_scale_cache=ovs) == 0
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(ks.cpu().numpy(), oks) and np.array_equal(vs.cpu().numpy(), ovs)
+    blk, off = divmod(int(slots[5]), 16)
+    if int(slots[5]) >= 0:
+        assert np.all(okc[blk, :, off] == 0) and np.all(oks[blk, :, off] == 0)
+
+
+def test_slot_outside_cache_sets_error_and_skips():
+    T, Hkv, D, nb = 4, 1, 64, 2
+    k = torch.randn(T, Hkv, D).to(torch.bfloat16).cuda()
+    slots = torch.tensor([0, 32, 5, 1 << 40], dtype=torch.int64, device="cuda")
+    kc = torch.zeros(nb, Hkv, 16, D, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    one = torch.ones(1, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fk.kv_cache_write(k, k, slots, kc, vc, kv_dtype=0, scale_mode=0, k_scale=one, v_scale=one,
+                      err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -6
+    want = oracle.e4m3_encode(k.float().cpu().numpy())
+    assert np.array_equal(kc[0, 0, 0].cpu().numpy(), want[0, 0])
+    assert np.array_equal(kc[0, 0, 5].cpu().numpy(), want[2, 0])
+
+
+def _oracle_encode_parallel(x: np.ndarray, workers=16) -> np.ndarray:
+    out = np.empty(x.shape, np.uint8)
+    n = x.size
+    step = (n + workers - 1) // workers
+
+    def run(i):
+        lo, hi = i * step, min(n, (i + 1) * step)
+        out[lo:hi] = oracle.e4m3_encode(x[lo:hi])
+
+    with cf.ThreadPoolExecutor(workers) as ex:
+        list(ex.map(run, range(workers)))
+    return out
+
+
+def test_encoder_matches_oracle_on_every_fp32_pattern():
+    # All 2^32 fp32 bit patterns through the device encoder (scale 1), against
+    # the oracle's integer-arithmetic encoder.  NaN inputs stay NaN codes on both
+    # sides (the sign of a NaN code is not compared).
+    chunk = 1 << 28
+    for start in range(0, 1 << 32, chunk):
+        bits = torch.arange(start, start + chunk, dtype=torch.int64, device="cuda")
+        bits = torch.where(bits >= 1 << 31, bits - (1 << 32), bits).to(torch.int32)
+        x = bits.view(torch.float32)
+        got = fk.quantize_e4m3(x, 1.0).cpu().numpy()
+        xh = x.cpu().numpy()
+        want = _oracle_encode_parallel(xh)
+        nan = np.isnan(xh)
+        assert np.array_equal(got[~nan], want[~nan]), f"chunk at {start:#x}"
+        assert np.all((got[nan] & 0x7F) == 0x7F)
+        del bits, x
+
+
+@pytest.mark.parametrize("scale", [0.37, 1.0 / 448, 3.0e-3, 17.5])
+def test_encoder_with_scales_matches_oracle(scale):
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(1 << 20, generator=g) * 10
+    got = fk.quantize_e4m3(x.cuda(), scale).cpu().numpy()
+    q = (x.numpy().astype(np.float32) / np.float32(scale)).astype(np.float32)
+    assert np.array_equal(got, oracle.e4m3_encode(q))

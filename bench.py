@@ -204,68 +204,114 @@ def build_caches(w, kv_dtype, dev, rotations):
     return caches
 
 
+def _graph(fn, n, stream):
+    """Capture n calls fn(i) into one CUDA graph on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def _replay_steps(graphs, K, stream):
+    """Replay graphs covering exactly K steps: (full graph of n, remainder graph)."""
+    full, n, rem = graphs
+    for _ in range(K // n):
+        full.replay()
+    if rem is not None:
+        rem.replay()
+
+
+def _capture_steps(fn, K, n, stream):
+    full = _graph(fn, n, stream)
+    rem = _graph(fn, K % n, stream) if K % n else None
+    return full, n, rem
+
+
 def run_ours(args, dev, w, world, rank):
+    """Times K steps of the fp8 path and of the bf16 twin (CUDA graphs of
+    `per_graph` steps replayed back to back), the decode call alone, and the
+    end-to-end step with host copies."""
     import fp8_kv_cache_write_gb300 as fk
 
-    stream = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)
     q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
     slots, bt, cl = w.new_slots.to(dev), w.block_table.to(dev), w.context_lens.to(dev)
     mbs = bt.shape[1]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    dec_bytes, write_bytes = {}, {}
-    results = {}
-    launches_per_step = {}
+    dec_bytes, results, launches_per_step = {}, {}, {}
+    K = args.steps
+    per_graph = args.rotations * 8
+    dtypes = [(fk.KV_E4M3, "fp8"), (fk.KV_BF16, "bf16")]
+    if args.only:
+        dtypes = [d for d in dtypes if d[1] == args.only]
 
-    for kv_dtype, name in ((fk.KV_E4M3, "fp8"), (fk.KV_BF16, "bf16")):
+    for kv_dtype, name in dtypes:
         mode = fk.SCALE_PER_TOKEN_HEAD if kv_dtype == fk.KV_E4M3 else 0
-        caches = build_caches(w, kv_dtype, dev, ROTATIONS)
-        splits, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0, 0)
+        caches = build_caches(w, kv_dtype, dev, args.rotations)
+        splits, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0, args.splits)
         ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-        launches_per_step[name] = 1 + 1 + (1 if splits > 1 else 0)
+        launches_per_step[name] = 2 + (1 if splits > 1 else 0)
         d_b, w_b = step_bytes(w, 1 if kv_dtype == fk.KV_E4M3 else 2, kv_dtype == fk.KV_E4M3)
-        dec_bytes[name], write_bytes[name] = d_b, w_b
+        dec_bytes[name] = d_b
 
-        def step(i, k_in=kn, v_in=vn, s_in=slots, q_in=q, cl_in=cl, ev=None):
-            kc, vc, ks, vs = caches[i % ROTATIONS]
+        def write(i, k_in=kn, v_in=vn, s_in=slots):
+            kc, vc, ks, vs = caches[i % args.rotations]
             fk.kv_cache_write(k_in, v_in, s_in, kc, vc, kv_dtype=kv_dtype, scale_mode=mode,
-                              k_scale_cache=ks, v_scale_cache=vs, err_flag=err, stream=stream)
-            if ev is not None:
-                ev[0].record(stream)
+                              k_scale_cache=ks, v_scale_cache=vs, err_flag=err)
+
+        def decode(i, q_in=q, cl_in=cl):
+            kc, vc, ks, vs = caches[i % args.rotations]
             fk.paged_decode_attn(q_in, kc, vc, bt, cl_in, kv_dtype=kv_dtype, scale_mode=mode,
                                  k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=out,
-                                 err_flag=err, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
+                                 num_splits=args.splits, err_flag=err)
 
-        for i in range(args.warmup):
-            step(i)
+        def step(i):
+            write(i)
+            decode(i)
+
+        with torch.cuda.stream(cap):
+            for i in range(args.warmup):             # eager warm-up (also first-call setup)
+                step(i)
         torch.cuda.synchronize(dev)
-        K = args.steps
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
+        graphs = _capture_steps(step, K, per_graph, cap)
+        dgraph = _capture_steps(decode, K, per_graph, cap)
+        for _ in range(max(1, args.warmup // per_graph)):
+            graphs[0].replay()
+            dgraph[0].replay()
+        torch.cuda.synchronize(dev)
+
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         sampler = ClockSampler(dev.index) if name == "fp8" else None
         barrier()
         torch.cuda.synchronize(dev)
-        t0.record(stream)
-        for i in range(K):
-            step(i, ev=evs[i])
-        t1.record(stream)
+        with torch.cuda.stream(cap):
+            t0.record(cap)
+            _replay_steps(graphs, K, cap)
+            t1.record(cap)
         torch.cuda.synchronize(dev)
         barrier()
         clocks = sampler.stop() if sampler else None
         secs = t0.elapsed_time(t1) / 1e3
-        dec_ms = [a.elapsed_time(b) for a, b in evs]
+
+        # the decode call alone (split kernel + split_merge), same caches
+        with torch.cuda.stream(cap):
+            t0.record(cap)
+            _replay_steps(dgraph, K, cap)
+            t1.record(cap)
+        torch.cuda.synchronize(dev)
+        dec_ms = t0.elapsed_time(t1) / K
         gbs, tok_s, tmax = aggregate(d_b + w_b, w.B, secs, K)
         results[name] = {"gbs": gbs, "tokens_per_s": tok_s, "ms_per_step": tmax / K * 1e3,
-                         "decode_ms": statistics.mean(dec_ms), "num_splits": splits,
-                         "clocks": clocks, "secs": tmax}
+                         "decode_ms": dec_ms, "num_splits": splits, "clocks": clocks,
+                         "secs": tmax}
         if int(err.item()) != 0:
             raise RuntimeError(f"device error flag {int(err.item())} during the {name} run")
 
-        if name == "fp8":
-            # end to end: inputs from pinned host memory, output read back, each step
+        if name == "fp8" and not args.no_e2e:
+            # end to end through the public API: every step copies its inputs from
+            # pinned host memory and reads the output back (captured as graph nodes)
             hq = w.q.pin_memory()
             hk, hv = w.k_new.pin_memory(), w.v_new.pin_memory()
             hs, hc = w.new_slots.pin_memory(), w.context_lens.pin_memory()
@@ -281,25 +327,33 @@ def run_ours(args, dev, w, world, rank):
                 dv.copy_(hv, non_blocking=True)
                 ds.copy_(hs, non_blocking=True)
                 dc.copy_(hc, non_blocking=True)
-                step(i, k_in=dk, v_in=dv, s_in=ds, q_in=dq, cl_in=dc)
+                write(i, k_in=dk, v_in=dv, s_in=ds)
+                decode(i, q_in=dq, cl_in=dc)
                 hout.copy_(out, non_blocking=True)
 
-            for i in range(args.warmup):
-                e2e_step(i)
+            with torch.cuda.stream(cap):
+                for i in range(3):
+                    e2e_step(i)
+            torch.cuda.synchronize(dev)
+            egraphs = _capture_steps(e2e_step, K, per_graph, cap)
+            egraphs[0].replay()
             torch.cuda.synchronize(dev)
             barrier()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for i in range(K):
-                e2e_step(i)
-            b.record(stream)
+            with torch.cuda.stream(cap):
+                t0.record(cap)
+                _replay_steps(egraphs, K, cap)
+                t1.record(cap)
             torch.cuda.synchronize(dev)
             barrier()
-            e_secs = a.elapsed_time(b) / 1e3
+            e_secs = t0.elapsed_time(t1) / 1e3
             e_gbs, e_tok, _ = aggregate(d_b + w_b, w.B, e_secs, K)
             results["e2e"] = {"value": e_gbs, "unit": "GB/s", "tokens_per_s": e_tok,
-                              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        del caches
+                              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                              "how": "each step: 5 H2D copies from pinned memory, cache write, "
+                                     "decode, 1 D2H copy; steps replayed as CUDA graphs"}
+            del egraphs
+        del graphs, dgraph, caches
+        torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
     return results, dec_bytes, launches_per_step
 
@@ -384,9 +438,15 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["fp8", "bf16"], default=None,
+                    help="time one cache dtype only (profiling runs)")
+    ap.add_argument("--rotations", type=int, default=ROTATIONS,
+                    help="cache copies rotated between steps (each larger than L2)")
+    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planner)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -414,43 +474,55 @@ def main():
     torch.cuda.set_device(dev)
     res, dec_bytes, lps = run_ours(args, dev, w, world, rank)
     peak, peak_kind = measured_peaks()
-    fp8, bf16 = res["fp8"], res["bf16"]
-    achieved = dec_bytes["fp8"] / (fp8["decode_ms"] / 1e3) / 1e9
-    line = None
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ob = OracleBaseline(w)
-        gbs, tps, secs, sample = ob.run()
-        cpu = {"value": gbs, "unit": "GB/s", "tokens_per_s": tps, "cores": ob.cores,
-               "kind": "oracle", "sample": sample + f"; {secs:.2f} s wall"}
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": fp8["gbs"], "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": fp8["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 8 * world,
-                       "parallelism": f"replicas x{world}",
-                       "l2": f"{ROTATIONS} rotating cache copies, each larger than L2",
-                       "num_splits": fp8["num_splits"]},
-            "pct_of_peak": fp8["gbs"] / peak,
-            "tokens_per_s": fp8["tokens_per_s"],
-            "bf16_twin": {"value": bf16["gbs"], "unit": "GB/s",
-                          "tokens_per_s": bf16["tokens_per_s"],
-                          "ms_per_step": bf16["ms_per_step"], "decode_ms": bf16["decode_ms"]},
-            "fp8_vs_bf16_tokens_per_s": fp8["tokens_per_s"] / bf16["tokens_per_s"],
-            "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + split_merge)",
-                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": profiled_traffic(),
-                         "algorithmic_bytes_per_launch": dec_bytes["fp8"],
-                         "decode_ms": fp8["decode_ms"]},
-            "cpu_baseline": cpu,
-            "e2e": res["e2e"],
-            "gpu_launches": lps["fp8"] * args.steps,
-            "clocks": fp8["clocks"],
-        }
-        print(json.dumps(line), flush=True)
+    if args.only:                       # profiling / sweep runs: a short line
+        r = res[args.only]
+        if rank == 0:
+            print(json.dumps({"only": args.only, "splits": r["num_splits"],
+                              "step_gbs": r["gbs"], "ms_per_step": r["ms_per_step"],
+                              "decode_ms": r["decode_ms"],
+                              "decode_gbs": dec_bytes[args.only] / r["decode_ms"] / 1e6,
+                              "tokens_per_s": r["tokens_per_s"], "clocks": r["clocks"]}),
+                  flush=True)
+    else:
+        fp8, bf16 = res["fp8"], res["bf16"]
+        achieved = dec_bytes["fp8"] / (fp8["decode_ms"] / 1e3) / 1e9
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            ob = OracleBaseline(w)
+            gbs, tps, secs, sample = ob.run()
+            cpu = {"value": gbs, "unit": "GB/s", "tokens_per_s": tps, "cores": ob.cores,
+                   "kind": "oracle", "sample": sample + f"; {secs:.2f} s wall"}
+        if rank == 0:
+            line = {
+                "metric": METRIC, "value": fp8["gbs"], "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": fp8["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "e4m3", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "global_batch": 8 * world,
+                           "parallelism": f"replicas x{world}",
+                           "l2": f"{args.rotations} rotating cache copies, each larger than L2",
+                           "num_splits": fp8["num_splits"],
+                           "timing": "CUDA graphs of whole steps replayed back to back"},
+                "pct_of_peak": fp8["gbs"] / peak,
+                "tokens_per_s": fp8["tokens_per_s"],
+                "bf16_twin": {"value": bf16["gbs"], "unit": "GB/s",
+                              "tokens_per_s": bf16["tokens_per_s"],
+                              "ms_per_step": bf16["ms_per_step"],
+                              "decode_ms": bf16["decode_ms"],
+                              "decode_gbs": dec_bytes["bf16"] / bf16["decode_ms"] / 1e6},
+                "fp8_vs_bf16_tokens_per_s": fp8["tokens_per_s"] / bf16["tokens_per_s"],
+                "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (split + split_merge)",
+                             "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                             "unit": "GB/s", "frac": achieved / peak,
+                             "traffic": profiled_traffic(),
+                             "algorithmic_bytes_per_launch": dec_bytes["fp8"],
+                             "decode_ms": fp8["decode_ms"]},
+                "cpu_baseline": cpu,
+                "e2e": res.get("e2e"),
+                "gpu_launches": lps["fp8"] * args.steps,
+                "clocks": fp8["clocks"],
+            }
+            print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

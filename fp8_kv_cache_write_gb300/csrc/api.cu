@@ -128,12 +128,14 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     if (req > 0) {
         S = req < maxvis ? req : maxvis;
     } else {
-        const int64_t work = static_cast<int64_t>(B) * Hkv * maxvis;
-        const int64_t target = static_cast<int64_t>(sm_count()) * 4;
-        int64_t pps = (work + target - 1) / target;
-        if (pps < 16) pps = 16;
-        if (pps > 128) pps = 128;
-        S = static_cast<int>((maxvis + pps - 1) / pps);
+        // fill one wave of resident CTAs (3 per SM for the shipped tile sizes),
+        // keeping at least 16 pages (4 per warp) in a split
+        const int64_t units = static_cast<int64_t>(B) * Hkv;
+        const int64_t slots = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0);
+        int64_t s_wave = slots / (units > 0 ? units : 1);
+        if (s_wave < 1) s_wave = 1;
+        const int64_t s_min_pages = (maxvis + 15) / 16;
+        S = static_cast<int>(s_wave < s_min_pages ? s_wave : s_min_pages);
     }
     if (S > 1024) S = 1024;
     if (S < 1) S = 1;

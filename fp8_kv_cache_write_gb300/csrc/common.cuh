@@ -114,6 +114,18 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_bytes) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Four e4m3fn bytes -> two f16x2 words (bytes 0,1 -> lo; bytes 2,3 -> hi), exact.
+// The halves are taken as 16-bit register views so no extraction is needed.
+__device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t four_bytes, uint32_t& lo,
+                                                    uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_bytes));
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);

@@ -285,9 +285,16 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
     };
 
+    // fp8 path: P = hi + lo with lo scaled by 2^11 into f16's normal range and
+    // accumulated separately (O = o + 2^-11 olo); bf16 P has no subnormal issue
+    constexpr int kLoTiles = BF16 ? 1 : C::kMTiles;
+    constexpr float kLoScale = 2048.f;
     float o[C::kMTiles][4];
+    float olo[kLoTiles][4];
 #pragma unroll
     for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLoTiles; ++i) olo[i][0] = olo[i][1] = olo[i][2] = olo[i][3] = 0.f;
     float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
     bool timed_out = false;
     int drain_from = 0;
@@ -325,17 +332,19 @@ __global__ void __launch_bounds__(kWarps * 32)
                     mma_bf16(acc, wx[2 * jj], wy[2 * jj], wx[2 * jj + 1], wy[2 * jj + 1], qb[ks][0],
                              qb[ks][1]);
                 } else {
-                    mma_f16(acc, f16x2_from_e4m3x2(wx[jj] & 0xffffu),
-                            f16x2_from_e4m3x2(wy[jj] & 0xffffu), f16x2_from_e4m3x2(wx[jj] >> 16),
-                            f16x2_from_e4m3x2(wy[jj] >> 16), qb[ks][0], qb[ks][1]);
+                    uint32_t xl, xh, yl, yh;
+                    f16x2x2_from_e4m3x4(wx[jj], xl, xh);
+                    f16x2x2_from_e4m3x4(wy[jj], yl, yh);
+                    mma_f16(acc, xl, yl, xh, yh, qb[ks][0], qb[ks][1]);
                 }
             }
         }
 
-        // ---- logits (base 2), masked outside [lo, ctx)
+        // ---- logits (base 2), masked outside [lo, ctx) (only boundary pages)
+        const bool interior = !bad && pos0 >= lo && pos0 + kPage <= ctx;
         const int posA = pos0 + tA, posB = pos0 + tB;
-        const bool vA = !bad && posA >= lo && posA < ctx;
-        const bool vB = !bad && posB >= lo && posB < ctx;
+        const bool vA = interior || (!bad && posA >= lo && posA < ctx);
+        const bool vB = interior || (!bad && posB >= lo && posB < ctx);
         float ksA = 1.f, ksB = 1.f, vsA = 1.f, vsB = 1.f;
         if constexpr (PER_TOKEN) {
             const float* sk = reinterpret_cast<const float*>(scl + st * C::kScaleB);
@@ -363,6 +372,13 @@ __global__ void __launch_bounds__(kWarps * 32)
                 o[i][0] *= a;
                 o[i][2] *= a;
             }
+            if constexpr (!BF16) {
+#pragma unroll
+                for (int i = 0; i < kLoTiles; ++i) {
+                    olo[i][0] *= a;
+                    olo[i][2] *= a;
+                }
+            }
             m0 = mx0;
         }
         if (mx1 > m1 + 8.f) {
@@ -372,6 +388,13 @@ __global__ void __launch_bounds__(kWarps * 32)
             for (int i = 0; i < C::kMTiles; ++i) {
                 o[i][1] *= a;
                 o[i][3] *= a;
+            }
+            if constexpr (!BF16) {
+#pragma unroll
+                for (int i = 0; i < kLoTiles; ++i) {
+                    olo[i][1] *= a;
+                    olo[i][3] *= a;
+                }
             }
             m1 = mx1;
         }
@@ -397,8 +420,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         } else {
             const uint32_t hA = pack_f16x2(w0, w1), hB = pack_f16x2(w2, w3);
             const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
-            const uint32_t lA = pack_f16x2(w0 - fA.x, w1 - fA.y);
-            const uint32_t lB = pack_f16x2(w2 - fB.x, w3 - fB.y);
+            const uint32_t lA = pack_f16x2((w0 - fA.x) * kLoScale, (w1 - fA.y) * kLoScale);
+            const uint32_t lB = pack_f16x2((w2 - fB.x) * kLoScale, (w3 - fB.y) * kLoScale);
             bh0 = movmatrix_trans(hA);
             bh1 = movmatrix_trans(hB);
             bl0 = movmatrix_trans(lA);
@@ -428,10 +451,12 @@ __global__ void __launch_bounds__(kWarps * 32)
                 }
             }
             // rows outside [lo, ctx) may hold any bytes (even NaN codes): zero them
-            const int pos = pos0 + t;
-            if (bad || pos < lo || pos >= ctx) {
+            if (!interior) {
+                const int pos = pos0 + t;
+                if (bad || pos < lo || pos >= ctx) {
 #pragma unroll
-                for (int w = 0; w < C::kVWords; ++w) vr[r][w] = 0u;
+                    for (int w = 0; w < C::kVWords; ++w) vr[r][w] = 0u;
+                }
             }
         }
 
@@ -451,12 +476,10 @@ __global__ void __launch_bounds__(kWarps * 32)
                 const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
                 const uint32_t x01 = __byte_perm(vr[0][w], vr[1][w], sel);
                 const uint32_t x23 = __byte_perm(vr[2][w], vr[3][w], sel);
-                a0 = f16x2_from_e4m3x2(x01 & 0xffffu);
-                a1 = f16x2_from_e4m3x2(x01 >> 16);
-                a2 = f16x2_from_e4m3x2(x23 & 0xffffu);
-                a3 = f16x2_from_e4m3x2(x23 >> 16);
+                f16x2x2_from_e4m3x4(x01, a0, a1);
+                f16x2x2_from_e4m3x4(x23, a2, a3);
                 mma_f16(o[i], a0, a1, a2, a3, bh0, bh1);
-                mma_f16(o[i], a0, a1, a2, a3, bl0, bl1);
+                mma_f16(olo[i < kLoTiles ? i : 0], a0, a1, a2, a3, bl0, bl1);
             }
         }
 
@@ -498,6 +521,12 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int dbase = perm8(g) * (D / 8);
         float* o0 = ow + (warp * 8 + 2 * c) * D;
         float* o1 = ow + (warp * 8 + 2 * c + 1) * D;
+        if constexpr (!BF16) {
+#pragma unroll
+            for (int i = 0; i < C::kMTiles; ++i)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) o[i][r] += olo[i < kLoTiles ? i : 0][r] * (1.f / kLoScale);
+        }
 #pragma unroll
         for (int i = 0; i < C::kMTiles; ++i) {
             const int d = dbase + 2 * i;
@@ -585,9 +614,16 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
                          cudaStream_t stream) {
     using C = Cfg<D, BF16>;
     auto kern = paged_decode_kernel<D, BF16, PER_TOKEN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    // opt in to the large dynamic shared-memory size once per device
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
     dim3 grid(p.num_splits, p.Hkv, p.B);
     kern<<<grid, kWarps * 32, C::kSmem, stream>>>(kmap, vmap, p);
     e = cudaGetLastError();

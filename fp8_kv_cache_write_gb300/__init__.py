@@ -28,7 +28,9 @@ STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -6: "FP8KV_ERR_BAD_INDEX"}
 
 EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
-           "fp8kv_quantize_e4m3", "fp8kv_status_string", "fp8kv_last_warning")
+           "fp8kv_paged_decode_attn_noalloc", "fp8kv_quantize_e4m3", "fp8kv_status_string",
+           "fp8kv_last_warning")
+NOALLOC_DECODE_SCRATCH_BYTES = 8 << 20
 
 _lib = None
 
@@ -65,6 +67,10 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_paged_decode_attn.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
                                               i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
         L.fp8kv_paged_decode_attn.restype = i32
+        L.fp8kv_paged_decode_attn_noalloc.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P,
+                                                      i32, i32, i32, i32, i64, f32, i32, i32, P,
+                                                      i32, P, P]
+        L.fp8kv_paged_decode_attn_noalloc.restype = i32
         L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
         L.fp8kv_quantize_e4m3.restype = i32
         L.fp8kv_status_string.argtypes = [i32]
@@ -177,6 +183,41 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
         out_dtype, _ptr(err_flag), _stream(stream))
     _raise(st, "paged_decode_attn")
+    return out
+
+
+def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *, kv_dtype,
+                              scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
+                              k_scale_cache=None, v_scale_cache=None, softmax_scale=None,
+                              window=0, num_splits=0, out, out_dtype=OUT_F32, err_flag=None,
+                              stream=None):
+    """paged_decode_attn without a workspace, for callers that cannot allocate
+    device memory: the split partials live in the library's static device array
+    (NOALLOC_DECODE_SCRATCH_BYTES per GPU).  `out` must be passed.  Calls that
+    overlap on the GPU race on that array; the first call on a device should
+    come before any stream capture."""
+    _check(q, "q", torch.bfloat16)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
+    _check(block_table, "block_table", torch.int32)
+    _check(context_lens, "context_lens", torch.int32)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    mbs = block_table.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    st = lib().fp8kv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), kv_dtype, scale_mode, _ptr(k_scale),
+        _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache), _ptr(block_table), mbs,
+        _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), int(window),
+        int(num_splits), _ptr(out), out_dtype, _ptr(err_flag), _stream(stream))
+    if st == -3:
+        _, need = decode_plan(B, Hq, Hkv, D, mbs, window, num_splits)
+        raise Fp8kvError(st, f"paged_decode_attn_noalloc: the split plan needs {need} bytes of "
+                             f"scratch but the static array holds "
+                             f"{NOALLOC_DECODE_SCRATCH_BYTES}; pass fewer num_splits")
+    _raise(st, "paged_decode_attn_noalloc")
     return out
 
 

@@ -153,6 +153,40 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
 int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
                         void* cuda_stream);
 
+/*
+ * fp8kv_paged_decode_attn_noalloc -- fp8kv_paged_decode_attn for callers that
+ * cannot allocate device memory.  The pages have no counterpart of it: it is a
+ * deployment variant of the same computation, not part of the method.
+ *
+ * Who needs it: a C host program or plugin that only receives the tensors it
+ * reads and writes from the framework owning the GPU's memory pool (it has no
+ * allocator to get a workspace from), and serving loops that cannot call
+ * cudaMalloc / cudaFree because those synchronize the device.
+ *
+ * Arguments are those of fp8kv_paged_decode_attn without workspace: the split
+ * partials live in a static device array of FP8KV_NOALLOC_DECODE_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The caller still passes q, the caches, the tables and `out`.
+ *   - A call whose plan (fp8kv_decode_plan) needs more scratch than the array
+ *     holds returns FP8KV_ERR_WORKSPACE and launches nothing; request fewer
+ *     splits or use fp8kv_paged_decode_attn.
+ *   - All calls on a device share the array: calls whose kernels overlap on the
+ *     GPU (other streams, other host threads) race.  Serialize them.
+ *   - The first call on each device looks the array's address up with that
+ *     device current; make that first call before any stream capture.
+ *   - The array needs no initialisation and keeps the last call's partials.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define FP8KV_NOALLOC_DECODE_SCRATCH_BYTES (8u << 20)
+int fp8kv_paged_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                    int kv_dtype, int scale_mode, const float* k_scale,
+                                    const float* v_scale, const float* k_scale_cache,
+                                    const float* v_scale_cache, const int32_t* block_table,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                    int Hq, int Hkv, int D, int64_t num_blocks,
+                                    float softmax_scale, int window, int num_splits, void* out,
+                                    int out_dtype, int32_t* err_flag, void* cuda_stream);
+
 /* Human-readable name of a status code (static string). */
 const char* fp8kv_status_string(int status);
 

@@ -42,13 +42,17 @@ namespace {
 
 constexpr int kWarps = kDecodeWarps;
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+constexpr float kMaxInit = -1.0e30f;   // running-max start: finite, below any real logit
 
 template <int D, bool BF16>
 struct Cfg {
     static constexpr int kElem = BF16 ? 2 : 1;
     static constexpr int kRowB = D * kElem;           // bytes of one token row
     static constexpr int kTileB = kPage * kRowB;      // bytes of one (page, head) tile
-    static constexpr int kStageB = 2 * kTileB;        // K tile + V tile
+    // pages per iteration: two when a page tile is small, so each warp works on
+    // two independent pages between waits
+    static constexpr int kPPI = kRowB <= 128 ? 2 : 1;
+    static constexpr int kStageB = 2 * kPPI * kTileB; // K tiles, then V tiles
     static constexpr int kStagesRaw = 16384 / kStageB;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kSegs = kRowB / 64;          // 64-byte segments of a row
@@ -59,8 +63,8 @@ struct Cfg {
     static constexpr int kVWords = kVBytes / 4;
     static constexpr int kBoxes = kRowB >= 128 ? kRowB / 128 : 1;
     static constexpr int kWarpSmem = kStages * kStageB;
-    static constexpr int kScaleB = 128;               // k scales + v scales of a page
-    static constexpr int kSmem = 1024 + kWarps * kWarpSmem + kWarps * kStages * kScaleB +
+    static constexpr int kScaleB = 128;               // k scales + v scales of one page
+    static constexpr int kSmem = 1024 + kWarps * kWarpSmem + kWarps * kStages * kPPI * kScaleB +
                                  kWarps * kStages * 8 + 16;
     static_assert(kSegs * kKPerSeg == kKSteps, "k-step split");
     static_assert(kWarps * 8 * (D + 2) * 4 <= kWarps * kWarpSmem, "merge area fits the rings");
@@ -168,13 +172,14 @@ __global__ void __launch_bounds__(kWarps * 32)
         return;
     }
 
+    constexpr int PPI = C::kPPI;
     uint8_t* ring = smem + warp * C::kWarpSmem;
-    uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * C::kScaleB;
+    uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * C::kWarpSmem +
-                                                 kWarps * C::kStages * C::kScaleB) +
+                                                 kWarps * C::kStages * PPI * C::kScaleB) +
                      warp * C::kStages;
     int* abort_flag = reinterpret_cast<int*>(smem + kWarps * C::kWarpSmem +
-                                             kWarps * C::kStages * C::kScaleB +
+                                             kWarps * C::kStages * PPI * C::kScaleB +
                                              kWarps * C::kStages * 8);
     if (threadIdx.x == 0) *abort_flag = 0;
     if (lane == 0) {
@@ -241,46 +246,64 @@ __global__ void __launch_bounds__(kWarps * 32)
     const float hs0 = __shfl_sync(0xffffffffu, qscale, (2 * c) * 4);
     const float hs1 = __shfl_sync(0xffffffffu, qscale, (2 * c + 1) * 4);
 
-    // ---- pages of this warp: pb + warp + j * kWarps
-    const int n_my = (pe - pb > warp) ? (pe - pb - warp + kWarps - 1) / kWarps : 0;
+    // ---- work: groups of PPI consecutive pages; this warp takes groups
+    //      warp, warp + 4, ...; its j-th group starts at page pb + PPI*(warp + 4j)
+    const int n_groups = (pe - pb + PPI - 1) / PPI;
+    const int n_my = n_groups > warp ? (n_groups - warp + kWarps - 1) / kWarps : 0;
     const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    auto bt_load = [&](int batch) -> int {
-        const int pg = pb + warp + (batch * 32 + lane) * kWarps;
-        return pg < pe ? bt_row[pg] : 0;
+    constexpr int kGroupsPerBatch = 32 / PPI;
+    auto bt_load = [&](int batch) -> int {   // lane L: page L%PPI of group batch*GPB + L/PPI
+        const int grp = warp + (batch * kGroupsPerBatch + lane / PPI) * kWarps;
+        const int pg = pb + PPI * grp + lane % PPI;
+        return pg < pe ? bt_row[pg] : -1;
     };
     int bt_cur = 0, bt_next = 0;
-    uint32_t bad_mask = 0u;                 // stage bit set: block id was outside the cache
-    const uint32_t tx_bytes = C::kStageB + (PER_TOKEN ? C::kScaleB : 0);
+    uint32_t bad_mask = 0u;                 // bit st*PPI+k: page k of stage st is absent/invalid
 
     auto issue = [&](int j) {               // called by all lanes of the warp
-        if ((j & 31) == 0) {
+        if ((j % kGroupsPerBatch) == 0) {
             bt_cur = (j == 0) ? bt_load(0) : bt_next;
-            bt_next = bt_load((j >> 5) + 1);
+            bt_next = bt_load(j / kGroupsPerBatch + 1);
         }
-        int blk = __shfl_sync(0xffffffffu, bt_cur, j & 31);
         const int st = j % C::kStages;
-        const bool ok = blk >= 0 && static_cast<int64_t>(blk) < p.num_blocks;
-        bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
-        if (lane == 0) {
-            if (!ok) {
-                report(p.err, FP8KV_ERR_BAD_INDEX);
-                blk = 0;
-            }
-            const uint32_t bar = smem_addr(&bars[st]);
-            const uint32_t kdst = smem_addr(ring + st * C::kStageB);
-            const uint32_t vdst = kdst + C::kTileB;
-            const int z = blk * p.Hkv + h;
-            fence_proxy_async();
-            mbar_arrive_expect_tx(bar, tx_bytes);
+        const int pg0 = pb + PPI * (warp + j * kWarps);
+        int blk[PPI];
+        bool here[PPI];
+        uint32_t tx = 0;
 #pragma unroll
-            for (int box = 0; box < C::kBoxes; ++box) {
-                tma_load_3d(kdst + box * 2048, &kmap, box * 128, 0, z, bar);
-                tma_load_3d(vdst + box * 2048, &vmap, box * 128, 0, z, bar);
+        for (int k = 0; k < PPI; ++k) {
+            blk[k] = __shfl_sync(0xffffffffu, bt_cur, (j % kGroupsPerBatch) * PPI + k);
+            here[k] = pg0 + k < pe;
+            const bool ok = here[k] && blk[k] >= 0 && static_cast<int64_t>(blk[k]) < p.num_blocks;
+            const uint32_t bit = 1u << (st * PPI + k);
+            bad_mask = ok ? (bad_mask & ~bit) : (bad_mask | bit);
+            if (here[k] && !ok) {
+                if (lane == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+                blk[k] = 0;                  // load an in-range page, masked later
             }
-            if constexpr (PER_TOKEN) {
-                const uint32_t sdst = smem_addr(scl + st * C::kScaleB);
-                bulk_load(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
-                bulk_load(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
+            if (here[k]) tx += 2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0);
+        }
+        if (lane == 0) {
+            const uint32_t bar = smem_addr(&bars[st]);
+            const uint32_t base = smem_addr(ring + st * C::kStageB);
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+            for (int k = 0; k < PPI; ++k) {
+                if (!here[k]) continue;
+                const int z = blk[k] * p.Hkv + h;
+#pragma unroll
+                for (int box = 0; box < C::kBoxes; ++box) {
+                    tma_load_3d(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0, z, bar);
+                    tma_load_3d(base + (PPI + k) * C::kTileB + box * 2048, &vmap, box * 128, 0, z,
+                                bar);
+                }
+                if constexpr (PER_TOKEN) {
+                    const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
+                    bulk_load(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
+                    bulk_load(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                              bar);
+                }
             }
         }
     };
@@ -295,14 +318,35 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 #pragma unroll
     for (int i = 0; i < kLoTiles; ++i) olo[i][0] = olo[i][1] = olo[i][2] = olo[i][3] = 0.f;
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    // running max starts finite so that a fully masked group gives ex2(-inf) = 0
+    float m0 = kMaxInit, m1 = kMaxInit, l0 = 0.f, l1 = 0.f;
     bool timed_out = false;
     int drain_from = 0;
 
     const int pre = n_my < C::kStages ? n_my : C::kStages;
     for (int j = 0; j < pre; ++j) issue(j);
 
+    // per-thread shared-memory offsets inside a page tile (fixed for the kernel)
     const int tA = perm8(g), tB = tA + 8;
+    int koffA[C::kSegs], koffB[C::kSegs];
+#pragma unroll
+    for (int s = 0; s < C::kSegs; ++s) {
+        koffA[s] = chunk_off<C::kRowB>(tA, 4 * s + c);
+        koffB[s] = chunk_off<C::kRowB>(tB, 4 * s + c);
+    }
+    int voff[4][C::kVBytes >= 16 ? C::kVBytes / 16 : 1];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = c + 4 * r;
+        if constexpr (C::kVBytes == 8) {
+            voff[r][0] = chunk_off<C::kRowB>(t, perm8(g) >> 1) + (perm8(g) & 1) * 8;
+        } else {
+#pragma unroll
+            for (int q4 = 0; q4 < C::kVBytes / 16; ++q4)
+                voff[r][q4] = chunk_off<C::kRowB>(t, perm8(g) * (C::kVBytes / 16) + q4);
+        }
+    }
+
     for (int j = 0; j < n_my; ++j) {
         const int st = j % C::kStages;
         const bool arrived =
@@ -312,58 +356,80 @@ __global__ void __launch_bounds__(kWarps * 32)
             drain_from = j;
             break;
         }
-        const uint8_t* kt = ring + st * C::kStageB;
-        const uint8_t* vt = kt + C::kTileB;
-        const int pos0 = (pb + warp + j * kWarps) * kPage;
-        const bool bad = (bad_mask >> st) & 1u;
+        const uint8_t* stage = ring + st * C::kStageB;
+        const int pos0 = (pb + PPI * (warp + j * kWarps)) * kPage;
 
-        // ---- S^T = K_page Q^T  (rows: tokens tA, tB; cols: heads 2c, 2c+1)
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        bool bad[PPI], interior[PPI];
+#pragma unroll
+        for (int k = 0; k < PPI; ++k) {
+            bad[k] = (bad_mask >> (st * PPI + k)) & 1u;
+            interior[k] = !bad[k] && pos0 + k * kPage >= lo && pos0 + (k + 1) * kPage <= ctx;
+        }
+
+        // ---- S^T = K_page Q^T for each page (rows: tokens tA, tB; cols: heads 2c, 2c+1)
+        float acc[PPI][4];
+#pragma unroll
+        for (int k = 0; k < PPI; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
 #pragma unroll
         for (int s = 0; s < C::kSegs; ++s) {
-            const uint4 kx = *reinterpret_cast<const uint4*>(kt + chunk_off<C::kRowB>(tA, 4 * s + c));
-            const uint4 ky = *reinterpret_cast<const uint4*>(kt + chunk_off<C::kRowB>(tB, 4 * s + c));
-            const uint32_t wx[4] = {kx.x, kx.y, kx.z, kx.w};
-            const uint32_t wy[4] = {ky.x, ky.y, ky.z, ky.w};
+            uint4 kx[PPI], ky[PPI];
+#pragma unroll
+            for (int k = 0; k < PPI; ++k) {
+                kx[k] = *reinterpret_cast<const uint4*>(stage + k * C::kTileB + koffA[s]);
+                ky[k] = *reinterpret_cast<const uint4*>(stage + k * C::kTileB + koffB[s]);
+            }
 #pragma unroll
             for (int jj = 0; jj < C::kKPerSeg; ++jj) {
                 const int ks = s * C::kKPerSeg + jj;
-                if constexpr (BF16) {
-                    mma_bf16(acc, wx[2 * jj], wy[2 * jj], wx[2 * jj + 1], wy[2 * jj + 1], qb[ks][0],
-                             qb[ks][1]);
-                } else {
-                    uint32_t xl, xh, yl, yh;
-                    f16x2x2_from_e4m3x4(wx[jj], xl, xh);
-                    f16x2x2_from_e4m3x4(wy[jj], yl, yh);
-                    mma_f16(acc, xl, yl, xh, yh, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                for (int k = 0; k < PPI; ++k) {
+                    const uint32_t wx[4] = {kx[k].x, kx[k].y, kx[k].z, kx[k].w};
+                    const uint32_t wy[4] = {ky[k].x, ky[k].y, ky[k].z, ky[k].w};
+                    if constexpr (BF16) {
+                        mma_bf16(acc[k], wx[2 * jj], wy[2 * jj], wx[2 * jj + 1], wy[2 * jj + 1],
+                                 qb[ks][0], qb[ks][1]);
+                    } else {
+                        uint32_t xl, xh, yl, yh;
+                        f16x2x2_from_e4m3x4(wx[jj], xl, xh);
+                        f16x2x2_from_e4m3x4(wy[jj], yl, yh);
+                        mma_f16(acc[k], xl, yl, xh, yh, qb[ks][0], qb[ks][1]);
+                    }
                 }
             }
         }
 
-        // ---- logits (base 2), masked outside [lo, ctx) (only boundary pages)
-        const bool interior = !bad && pos0 >= lo && pos0 + kPage <= ctx;
-        const int posA = pos0 + tA, posB = pos0 + tB;
-        const bool vA = interior || (!bad && posA >= lo && posA < ctx);
-        const bool vB = interior || (!bad && posB >= lo && posB < ctx);
-        float ksA = 1.f, ksB = 1.f, vsA = 1.f, vsB = 1.f;
-        if constexpr (PER_TOKEN) {
-            const float* sk = reinterpret_cast<const float*>(scl + st * C::kScaleB);
-            ksA = sk[tA];
-            ksB = sk[tB];
-            vsA = sk[16 + tA];
-            vsB = sk[16 + tB];
+        // ---- logits (base 2), masked outside [lo, ctx) on boundary pages
+        float z[PPI][4], vs[PPI][2];
+        float mx0 = neg_inf(), mx1 = neg_inf();
+#pragma unroll
+        for (int k = 0; k < PPI; ++k) {
+            const int posA = pos0 + k * kPage + tA, posB = pos0 + k * kPage + tB;
+            const bool vA = interior[k] || (!bad[k] && posA >= lo && posA < ctx);
+            const bool vB = interior[k] || (!bad[k] && posB >= lo && posB < ctx);
+            float ksA = 1.f, ksB = 1.f;
+            vs[k][0] = vs[k][1] = 1.f;
+            if constexpr (PER_TOKEN) {
+                const float* sk = reinterpret_cast<const float*>(scl + (st * PPI + k) * C::kScaleB);
+                ksA = sk[tA];
+                ksB = sk[tB];
+                // scales of masked tokens may be any bits (slots never written,
+                // pages not fetched): zero them so that 0 * scale stays 0
+                vs[k][0] = vA ? sk[16 + tA] : 0.f;
+                vs[k][1] = vB ? sk[16 + tB] : 0.f;
+            }
+            z[k][0] = vA ? acc[k][0] * hs0 * ksA : neg_inf();
+            z[k][1] = vA ? acc[k][1] * hs1 * ksA : neg_inf();
+            z[k][2] = vB ? acc[k][2] * hs0 * ksB : neg_inf();
+            z[k][3] = vB ? acc[k][3] * hs1 * ksB : neg_inf();
+            mx0 = fmaxf(mx0, fmaxf(z[k][0], z[k][2]));
+            mx1 = fmaxf(mx1, fmaxf(z[k][1], z[k][3]));
         }
-        const float z0 = vA ? acc[0] * hs0 * ksA : neg_inf();
-        const float z1 = vA ? acc[1] * hs1 * ksA : neg_inf();
-        const float z2 = vB ? acc[2] * hs0 * ksB : neg_inf();
-        const float z3 = vB ? acc[3] * hs1 * ksB : neg_inf();
-        float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        // lazy running max: move it only when a page exceeds it by 2^8
+        // lazy running max: move it only when the group exceeds it by 2^8
         if (mx0 > m0 + 8.f) {
             const float a = ex2(m0 - mx0);
             l0 *= a;
@@ -398,88 +464,88 @@ __global__ void __launch_bounds__(kWarps * 32)
             }
             m1 = mx1;
         }
-        const float p0 = vA ? ex2(z0 - m0) : 0.f;
-        const float p1 = vA ? ex2(z1 - m1) : 0.f;
-        const float p2 = vB ? ex2(z2 - m0) : 0.f;
-        const float p3 = vB ? ex2(z3 - m1) : 0.f;
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        const float w0 = p0 * vsA, w1 = p1 * vsA, w2 = p2 * vsB, w3 = p3 * vsB;
 
-        // ---- P^T as the B operand: hi + lo halves, transposed by movmatrix
-        uint32_t bh0, bh1, bl0, bl1;
-        if constexpr (BF16) {
-            const uint32_t hA = pack_bf16x2(w0, w1), hB = pack_bf16x2(w2, w3);
-            const float2 fA = unpack_bf16x2(hA), fB = unpack_bf16x2(hB);
-            const uint32_t lA = pack_bf16x2(w0 - fA.x, w1 - fA.y);
-            const uint32_t lB = pack_bf16x2(w2 - fB.x, w3 - fB.y);
-            bh0 = movmatrix_trans(hA);
-            bh1 = movmatrix_trans(hB);
-            bl0 = movmatrix_trans(lA);
-            bl1 = movmatrix_trans(lB);
-        } else {
-            const uint32_t hA = pack_f16x2(w0, w1), hB = pack_f16x2(w2, w3);
-            const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
-            const uint32_t lA = pack_f16x2((w0 - fA.x) * kLoScale, (w1 - fA.y) * kLoScale);
-            const uint32_t lB = pack_f16x2((w2 - fB.x) * kLoScale, (w3 - fB.y) * kLoScale);
-            bh0 = movmatrix_trans(hA);
-            bh1 = movmatrix_trans(hB);
-            bl0 = movmatrix_trans(lA);
-            bl1 = movmatrix_trans(lB);
-        }
+#pragma unroll
+        for (int k = 0; k < PPI; ++k) {
+            // masked logits are -inf and give weight 0 (the running max is finite)
+            const float p0 = ex2(z[k][0] - m0), p1 = ex2(z[k][1] - m1);
+            const float p2 = ex2(z[k][2] - m0), p3 = ex2(z[k][3] - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            const float w0 = p0 * vs[k][0], w1 = p1 * vs[k][0];
+            const float w2 = p2 * vs[k][1], w3 = p3 * vs[k][1];
 
-        // ---- V rows of tokens c, c+4, c+8, c+12 (k-slots 2c, 2c+1, 2c+8, 2c+9)
-        uint32_t vr[4][C::kVWords];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int t = c + 4 * r;
-            if constexpr (C::kVBytes == 8) {
-                const int ch = perm8(g) >> 1;
-                const uint2 v2 = *reinterpret_cast<const uint2*>(
-                    vt + chunk_off<C::kRowB>(t, ch) + (perm8(g) & 1) * 8);
-                vr[r][0] = v2.x;
-                vr[r][1] = v2.y;
-            } else {
-#pragma unroll
-                for (int q4 = 0; q4 < C::kVBytes / 16; ++q4) {
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(
-                        vt + chunk_off<C::kRowB>(t, perm8(g) * (C::kVBytes / 16) + q4));
-                    vr[r][4 * q4 + 0] = v4.x;
-                    vr[r][4 * q4 + 1] = v4.y;
-                    vr[r][4 * q4 + 2] = v4.z;
-                    vr[r][4 * q4 + 3] = v4.w;
-                }
-            }
-            // rows outside [lo, ctx) may hold any bytes (even NaN codes): zero them
-            if (!interior) {
-                const int pos = pos0 + t;
-                if (bad || pos < lo || pos >= ctx) {
-#pragma unroll
-                    for (int w = 0; w < C::kVWords; ++w) vr[r][w] = 0u;
-                }
-            }
-        }
-
-        // ---- O^T += V^T P^T  (row g <-> d = perm8(g)*D/8 + 2i, row g+8 <-> d+1)
-#pragma unroll
-        for (int i = 0; i < C::kMTiles; ++i) {
-            uint32_t a0, a1, a2, a3;
+            // ---- P^T as the B operand: hi + lo halves, transposed by movmatrix
+            uint32_t bh0, bh1, bl0, bl1;
             if constexpr (BF16) {
-                a0 = __byte_perm(vr[0][i], vr[1][i], 0x5410);
-                a1 = __byte_perm(vr[0][i], vr[1][i], 0x7632);
-                a2 = __byte_perm(vr[2][i], vr[3][i], 0x5410);
-                a3 = __byte_perm(vr[2][i], vr[3][i], 0x7632);
-                mma_bf16(o[i], a0, a1, a2, a3, bh0, bh1);
-                mma_bf16(o[i], a0, a1, a2, a3, bl0, bl1);
+                const uint32_t hA = pack_bf16x2(w0, w1), hB = pack_bf16x2(w2, w3);
+                const float2 fA = unpack_bf16x2(hA), fB = unpack_bf16x2(hB);
+                bh0 = movmatrix_trans(hA);
+                bh1 = movmatrix_trans(hB);
+                bl0 = movmatrix_trans(pack_bf16x2(w0 - fA.x, w1 - fA.y));
+                bl1 = movmatrix_trans(pack_bf16x2(w2 - fB.x, w3 - fB.y));
             } else {
-                const int w = i >> 1;
-                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-                const uint32_t x01 = __byte_perm(vr[0][w], vr[1][w], sel);
-                const uint32_t x23 = __byte_perm(vr[2][w], vr[3][w], sel);
-                f16x2x2_from_e4m3x4(x01, a0, a1);
-                f16x2x2_from_e4m3x4(x23, a2, a3);
-                mma_f16(o[i], a0, a1, a2, a3, bh0, bh1);
-                mma_f16(olo[i < kLoTiles ? i : 0], a0, a1, a2, a3, bl0, bl1);
+                const uint32_t hA = pack_f16x2(w0, w1), hB = pack_f16x2(w2, w3);
+                const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
+                bh0 = movmatrix_trans(hA);
+                bh1 = movmatrix_trans(hB);
+                bl0 = movmatrix_trans(pack_f16x2((w0 - fA.x) * kLoScale, (w1 - fA.y) * kLoScale));
+                bl1 = movmatrix_trans(pack_f16x2((w2 - fB.x) * kLoScale, (w3 - fB.y) * kLoScale));
+            }
+
+            // ---- V rows of tokens c, c+4, c+8, c+12 (k-slots 2c, 2c+1, 2c+8, 2c+9)
+            const uint8_t* vt = stage + (PPI + k) * C::kTileB;
+            uint32_t vr[4][C::kVWords];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if constexpr (C::kVBytes == 8) {
+                    const uint2 v2 = *reinterpret_cast<const uint2*>(vt + voff[r][0]);
+                    vr[r][0] = v2.x;
+                    vr[r][1] = v2.y;
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < C::kVBytes / 16; ++q4) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(vt + voff[r][q4]);
+                        vr[r][4 * q4 + 0] = v4.x;
+                        vr[r][4 * q4 + 1] = v4.y;
+                        vr[r][4 * q4 + 2] = v4.z;
+                        vr[r][4 * q4 + 3] = v4.w;
+                    }
+                }
+            }
+            if (!interior[k]) {
+                // rows outside [lo, ctx) may hold any bytes (even NaN codes): zero them
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int pos = pos0 + k * kPage + c + 4 * r;
+                    if (bad[k] || pos < lo || pos >= ctx) {
+#pragma unroll
+                        for (int w = 0; w < C::kVWords; ++w) vr[r][w] = 0u;
+                    }
+                }
+            }
+
+            // ---- O^T += V^T P^T  (row g <-> d = perm8(g)*D/8 + 2i, row g+8 <-> d+1)
+#pragma unroll
+            for (int i = 0; i < C::kMTiles; ++i) {
+                uint32_t a0, a1, a2, a3;
+                if constexpr (BF16) {
+                    a0 = __byte_perm(vr[0][i], vr[1][i], 0x5410);
+                    a1 = __byte_perm(vr[0][i], vr[1][i], 0x7632);
+                    a2 = __byte_perm(vr[2][i], vr[3][i], 0x5410);
+                    a3 = __byte_perm(vr[2][i], vr[3][i], 0x7632);
+                    mma_bf16(o[i], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16(o[i], a0, a1, a2, a3, bl0, bl1);
+                } else {
+                    const int w = i >> 1;
+                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t x01 = __byte_perm(vr[0][w], vr[1][w], sel);
+                    const uint32_t x23 = __byte_perm(vr[2][w], vr[3][w], sel);
+                    f16x2x2_from_e4m3x4(x01, a0, a1);
+                    f16x2x2_from_e4m3x4(x23, a2, a3);
+                    mma_f16(o[i], a0, a1, a2, a3, bh0, bh1);
+                    mma_f16(olo[i < kLoTiles ? i : 0], a0, a1, a2, a3, bl0, bl1);
+                }
             }
         }
 

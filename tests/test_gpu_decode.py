@@ -176,3 +176,28 @@ def test_workspace_too_small_is_rejected():
                                      8, 2, 128, w.num_blocks, 0.08, 0, 4, P(ws),
                                      ws.numel() * 4, P(out), 0, None, None)
     assert st == -3
+
+
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 2), (0, 0), (1, 0)])
+def test_unwritten_slots_holding_nan_do_not_leak(kv_dtype, mode):
+    # Cache bytes and scales of slots no token was written to may hold anything,
+    # NaN included; masked positions must contribute exactly nothing.
+    w = synth.decode_workload(14, [1, 17, 33, 250], 16, 2, 64, mode)
+    clean = gpu_fill(w, kv_dtype)
+    dirty = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in clean.items()}
+    # e4m3 code 0x7F is NaN; the bf16 cache gets a bf16 NaN
+    nan_k = torch.full_like(dirty["k"], 0x7F) if kv_dtype == 0 else \
+        torch.full_like(dirty["k"], float("nan"))
+    written = torch.zeros(w.num_blocks * 16, dtype=torch.bool)
+    written[torch.cat([w.hist_slots, w.new_slots])] = True
+    mask = (~written).view(w.num_blocks, 16).cuda()
+    for key in ("k", "v"):
+        t = dirty[key].permute(0, 2, 1, 3)          # [blk][16][Hkv][D] view
+        t[mask] = nan_k.permute(0, 2, 1, 3)[mask]
+    for key in ("ks", "vs"):
+        t = dirty[key].permute(0, 2, 1)
+        t[mask] = float("nan")
+    a = gpu_decode(w, clean).cpu()
+    b = gpu_decode(w, dirty).cpu()
+    assert torch.isfinite(b).all()
+    assert torch.equal(a, b)

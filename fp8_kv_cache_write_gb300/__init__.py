@@ -28,8 +28,8 @@ STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -6: "FP8KV_ERR_BAD_INDEX"}
 
 EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
-           "fp8kv_paged_decode_attn_noalloc", "fp8kv_quantize_e4m3", "fp8kv_status_string",
-           "fp8kv_last_warning")
+           "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn", "fp8kv_quantize_e4m3",
+           "fp8kv_status_string", "fp8kv_last_warning")
 NOALLOC_DECODE_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
                                                       i32, i32, i32, i32, i64, f32, i32, i32, P,
                                                       i32, P, P]
         L.fp8kv_paged_decode_attn_noalloc.restype = i32
+        L.fp8kv_prefill_attn.argtypes = [P, P, i32, P, P, i32, i32, P, P, f32, f32, P, i32, P,
+                                         i32, i32, i32, i32, i64, f32, i32, P, i32, P, P]
+        L.fp8kv_prefill_attn.restype = i32
         L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
         L.fp8kv_quantize_e4m3.restype = i32
         L.fp8kv_status_string.argtypes = [i32]
@@ -218,6 +221,38 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
                              f"scratch but the static array holds "
                              f"{NOALLOC_DECODE_SCRATCH_BYTES}; pass fewer num_splits")
     _raise(st, "paged_decode_attn_noalloc")
+    return out
+
+
+def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, context_lens,
+                 *, kv_dtype=KV_E4M3, scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
+                 q_scale=1.0, prob_scale=1.0, softmax_scale=None, two_level=False, out=None,
+                 out_dtype=OUT_F32, err_flag=None, stream=None):
+    """Chunked causal FP8 prefill of q [Tq][Hq][D] (bf16) over the paged cache;
+    returns out [Tq][Hq][D].  See fp8kv_prefill_attn."""
+    _check(q, "q", torch.bfloat16)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
+    _check(block_table, "block_table", torch.int32)
+    _check(context_lens, "context_lens", torch.int32)
+    _check(k_scale, "k_scale", torch.float32)
+    _check(v_scale, "v_scale", torch.float32)
+    Tq, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(Tq, Hq, D, device=q.device,
+                          dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    st = lib().fp8kv_prefill_attn(
+        _ptr(q), _ptr(cu_seqlens_q), int(max_seqlen_q), _ptr(k_cache), _ptr(v_cache), kv_dtype,
+        scale_mode, _ptr(k_scale), _ptr(v_scale), float(q_scale), float(prob_scale),
+        _ptr(block_table), block_table.shape[1], _ptr(context_lens), cu_seqlens_q.numel() - 1,
+        Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), 1 if two_level else 0, _ptr(out),
+        out_dtype, _ptr(err_flag), _stream(stream))
+    _raise(st, "prefill_attn")
     return out
 
 

@@ -314,6 +314,73 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
     return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
 }
 
+int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
+                       const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
+                       const float* k_scale, const float* v_scale, float q_scale,
+                       float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
+                       const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                       int64_t num_blocks, float softmax_scale, int two_level, void* out,
+                       int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    g_warning.clear();
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen_q < 0 ||
+        max_blocks_per_seq < 0 || num_blocks < 0 || (two_level != 0 && two_level != 1))
+        return FP8KV_ERR_INVALID;
+    if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
+    if (scale_mode < FP8KV_SCALE_PER_TENSOR || scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD)
+        return FP8KV_ERR_INVALID;
+    if (out_dtype != FP8KV_OUT_F32 && out_dtype != FP8KV_OUT_BF16) return FP8KV_ERR_INVALID;
+    if (!(q_scale > 0.f) || !(prob_scale > 0.f) || !(q_scale < 3.0e38f) ||
+        !(prob_scale < 3.0e38f) || !(softmax_scale == softmax_scale))
+        return FP8KV_ERR_INVALID;
+    const int G = Hq / Hkv;
+    if (kv_dtype != FP8KV_KV_E4M3 || scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD ||
+        (D != 128 && D != 256) || G > 128 || (128 % G) != 0)
+        return FP8KV_ERR_UNSUPPORTED;
+    if (B == 0 || max_seqlen_q == 0) return FP8KV_OK;
+    if (B > 65535 || Hkv > 65535 || max_blocks_per_seq < 1 || num_blocks < 1)
+        return FP8KV_ERR_INVALID;
+    if (num_blocks * static_cast<int64_t>(Hkv) >= (int64_t{1} << 31) ||
+        static_cast<int64_t>(max_blocks_per_seq) * FP8KV_PAGE_SIZE >= (int64_t{1} << 31))
+        return FP8KV_ERR_UNSUPPORTED;
+    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_table || !context_lens || !out ||
+        !k_scale || !v_scale)
+        return FP8KV_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return FP8KV_ERR_INVALID;
+    CUtensorMap kmap, vmap;
+    const int64_t nbh = num_blocks * Hkv;
+    if (!make_kv_map(k_cache, D, nbh, &kmap) || !make_kv_map(v_cache, D, nbh, &vmap))
+        return FP8KV_ERR_CUDA;
+    PrefillParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.block_table = block_table;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.q_scale = q_scale;
+    p.prob_scale = prob_scale;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.scale_mode = scale_mode;
+    p.out = out;
+    p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
+    p.err = err_flag;
+    const int tpt = 128 / G;
+    const int grid_x = (max_seqlen_q + tpt - 1) / tpt;
+    cudaError_t e = launch_prefill(p, kmap, vmap, D, two_level, grid_x,
+                                   static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return FP8KV_ERR_CUDA;
+    if (q_scale == 1.0f || prob_scale == 1.0f)
+        g_warning = "fp8 attention with uncalibrated q_scale and/or prob_scale of 1.0";
+    return FP8KV_OK;
+}
+
 int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
                         void* cuda_stream) {
     g_warning.clear();

@@ -62,6 +62,31 @@ cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, int D, int kv_dtype,
                                 cudaStream_t stream);
 
+// Chunked causal prefill on the tcgen05 FP8 tensor cores.  CTA (x, h, b) takes
+// query tokens [x*128/G, (x+1)*128/G) of sequence b with the G query heads of
+// KV head h (128 MMA rows).
+struct PrefillParams {
+    const __nv_bfloat16* q;        // [Tq][Hq][D]
+    const int32_t* cu_seqlens_q;   // [B+1]
+    const int32_t* block_table;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;   // keys of each sequence, the chunk included
+    int B, Hq, Hkv, G;
+    int64_t num_blocks;
+    float scale_log2;              // softmax_scale * log2(e)
+    float q_scale, prob_scale;
+    const float* k_scale;          // [1] or [Hkv]
+    const float* v_scale;
+    int scale_mode;
+    void* out;                     // [Tq][Hq][D]
+    int out_bf16;
+    int32_t* err;
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int D, int two_level, int grid_x,
+                           cudaStream_t stream);
+
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;
 int decode_ctas_per_sm(int D, int kv_dtype);

@@ -1,0 +1,497 @@
+// prefill.cu -- fp8_prefill_attn: chunked causal prefill over the paged e4m3
+// cache on the 5th-generation tensor cores (tcgen05, FP8 MMA, TMEM accumulators).
+//
+// What it computes ("vLLM FP8 KV-Cache 및 Attention 양자화 업데이트": attention in
+// FP8 e4m3 over the FP8 cache (opening paragraph), query quantization fused into
+// the kernel ("커널 및 퓨전 최적화"), two-level FP32 accumulation for long
+// contractions ("정확도를 위한 2단계 누적") that Blackwell does not need ("아키텍처별
+// 결과"); "[vLLM] KV Cache Quantization": q_scale / prob_scale of FP8 attention
+// ("Q/Prob 스케일과 FP8 Attention")): for query i of sequence b at position
+// pos_i = ctx_b - n_b + i and every query head of a KV head,
+//     q8 = e4m3(q / q_scale),  s_t = q8 . code_k(t) * q_scale * s_k * softmax_scale,
+//     p8_t = e4m3(exp(s_t - m) / prob_scale),  o = sum_t p8_t code_v(t) / sum_t p8_t
+// over keys t = 0 .. pos_i (times s_v * prob_scale), fp32 accumulation.
+//
+// Design (GB300):
+//   * one CTA per (tile of 128 / G query tokens x the G query heads of a KV
+//     head) = 128 MMA rows; 6 warps: warps 0-3 own one row each per thread
+//     (softmax, P quantization, rescale, epilogue), warp 4 issues TMA, warp 5
+//     allocates tensor memory and issues the MMAs from one thread.
+//   * per KV tile of 128 keys (8 pages): S = Q8 K^T (kind::f8f6f4, M 128, N 128,
+//     K = D in steps of 32) into TMEM; softmax reads S with tcgen05.ld, writes
+//     P8 (e4m3) to shared memory; O += P8 V (M 128, N = D, K = 128 keys) with V
+//     read MN-major straight from the cache tile.  Q8, K and P8 are K-major.
+//     All tiles use the 128-byte swizzle that TMA writes.
+//   * two-level off: O accumulates in TMEM across tiles; the lazy running max
+//     rescales a row of O in TMEM only when the row max grows by more than 2^8.
+//     two-level on: every tile's P V lands in a fresh TMEM tile and the softmax
+//     threads add it into an fp32 accumulator on the CUDA cores.
+//   * every mbarrier wait is bounded and watches a shared abort flag, so a stuck
+//     stage ends the kernel with FP8KV_ERR_TIMEOUT instead of hanging.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace fp8kv {
+
+namespace {
+
+constexpr int kRows = 128;          // MMA M: query rows of a CTA
+constexpr int kKeys = 128;          // keys per KV tile (8 pages)
+constexpr int kThreads = 192;
+constexpr float kMaxInitP = -1.0e30f;
+
+template <int D>
+struct PCfg {
+    // tensor memory: S (or the two-level P V tile) from column 0, O from kOCol;
+    // D 128 takes 256 columns so two co-resident CTAs never wait on each other
+    static constexpr uint32_t kTmemCols = D <= 128 ? 256u : 512u;
+    static constexpr uint32_t kOCol = D <= 128 ? 128u : 256u;
+    static constexpr int kPanels = D / 128;                 // 128-byte K panels of a row
+    static constexpr int kQBytes = kRows * D;               // Q8 tile
+    static constexpr int kKVBytes = kKeys * D;              // one K (or V) tile
+    static constexpr int kPBytes = kRows * kKeys;           // one P8 tile
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQBytes;          // [stage][K | V]
+    static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes; // [2] P8 tiles
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kNumBars = 12;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8; // tmem slot, abort flag
+    static constexpr int kSmem = 1024 + kOffMisc + 16;
+};
+
+// barrier indices
+enum { kKvFull0 = 0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull, kSEmpty, kPFull0, kPFull1,
+       kPvDone0, kPvDone1, kPvtFree, kMmaIdle };
+
+__device__ __forceinline__ float ex2p(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait that also gives up as soon as another thread raised `abort`.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, int32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitBudgetNs) {
+                *abort_flag = 1;
+                report(err, FP8KV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+template <int D, bool TWO_LEVEL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using C = PCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.G, TPT = kRows / G;                 // query tokens per tile
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int q0 = p.cu_seqlens_q[b], nq = p.cu_seqlens_q[b + 1] - q0;
+    const int tok0 = blockIdx.x * TPT;
+    if (tok0 >= nq) return;
+    int ctx = p.context_lens[b];
+    if (ctx > p.max_blocks_per_seq * kPage) {
+        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+        ctx = p.max_blocks_per_seq * kPage;
+    }
+    const int pos_base = ctx - nq;                      // position of the chunk's first query
+    const int n_tok = min(TPT, nq - tok0);
+    const int pos_max = pos_base + tok0 + n_tok - 1;
+    const int pos_min = pos_base + tok0;
+    if (pos_min < 0) {                                  // chunk longer than the context
+        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+        return;
+    }
+    const int n_tiles = pos_max / kKeys + 1;
+    const int ctx_pages = (ctx + kPage - 1) / kPage;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+    if (tid == 0) {
+        mbar_init(bar(kKvFull0), 1);
+        mbar_init(bar(kKvFull1), 1);
+        mbar_init(bar(kKvEmpty0), 1);
+        mbar_init(bar(kKvEmpty1), 1);
+        mbar_init(bar(kSFull), 1);
+        mbar_init(bar(kSEmpty), kRows);
+        mbar_init(bar(kPFull0), kRows);
+        mbar_init(bar(kPFull1), kRows);
+        mbar_init(bar(kPvDone0), 1);
+        mbar_init(bar(kPvDone1), 1);
+        mbar_init(bar(kPvtFree), kRows);
+        mbar_init(bar(kMmaIdle), 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 5) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+
+    // ---- Q8 = e4m3(q / q_scale) into the K-major, 128-byte-swizzled A tile
+    if (warp < 4) {
+        const int r = tid;
+        const int tk = tok0 + r / G, head = r % G;
+        uint8_t* qrow_s = smem + C::kOffQ;
+#pragma unroll 4
+        for (int c = 0; c < D / 16; ++c) {              // 16 e4m3 bytes per chunk
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (tk < nq) {
+                const __nv_bfloat16* src =
+                    p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D + c * 16;
+                const uint4 a = *reinterpret_cast<const uint4*>(src);
+                const uint4 bq = *reinterpret_cast<const uint4*>(src + 8);
+                const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float lo = __fdiv_rn(bf16_bits_to_float(in[i] & 0xffffu), p.q_scale);
+                    const float hi = __fdiv_rn(bf16_bits_to_float(in[i] >> 16), p.q_scale);
+                    w[i >> 1] |= static_cast<uint32_t>(e4m3x2_from_f32(lo, hi)) << (16 * (i & 1));
+                }
+            }
+            const int panel = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4*>(qrow_s + panel * (kRows * 128) + r * 128 +
+                                      ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async();                            // generic writes -> tensor core reads
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // =============================== TMA producer
+        const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            bool go = true;
+            if (j >= 2 && lane == 0)
+                go = wait_or_abort(bar(kKvEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            const int page0 = j * (kKeys / kPage);
+            int n_pages = ctx_pages - page0;
+            n_pages = n_pages > kKeys / kPage ? kKeys / kPage : n_pages;
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar(kKvFull0 + st),
+                                      static_cast<uint32_t>(n_pages) * 2u * kPage * D);
+            __syncwarp();
+            if (lane < n_pages) {
+                int blk = bt_row[page0 + lane];
+                if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+                    report(p.err, FP8KV_ERR_BAD_INDEX);
+                    blk = 0;
+                }
+                const int z = blk * p.Hkv + h;
+                const uint32_t kdst = sbase + C::kOffKV + st * 2 * C::kKVBytes;
+                const uint32_t vdst = kdst + C::kKVBytes;
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn) {
+                    tma_load_3d(kdst + pn * (kKeys * 128) + lane * 2048, &kmap, pn * 128, 0, z,
+                                bar(kKvFull0 + st));
+                    tma_load_3d(vdst + pn * (kKeys * 128) + lane * 2048, &vmap, pn * 128, 0, z,
+                                bar(kKvFull0 + st));
+                }
+            }
+            __syncwarp();
+            issued = j + 1;
+        }
+        // copies still in flight land before the CTA can leave (each wait bounded)
+        if (lane == 0 && *abort_flag) {
+            for (int j = issued - 2 > 0 ? issued - 2 : 0; j < issued; ++j)
+                (void)mbar_wait_bounded(bar(kKvFull0 + (j & 1)), (j >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // =============================== MMA issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, kKeys, kRows);
+            constexpr uint32_t idesc_pv = instr_desc(0, 0, 0, 1, D, kRows);
+            const uint32_t tS = tmem;                           // S: columns [0, 128)
+            const uint32_t tO = tmem + (TWO_LEVEL ? 0u : C::kOCol); // PV target
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (!wait_or_abort(bar(kKvFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
+                if (j > 0) {
+                    if (!wait_or_abort(bar(kSEmpty), (j - 1) & 1, abort_flag, p.err)) break;
+                    if (TWO_LEVEL &&
+                        !wait_or_abort(bar(kPvtFree), (j - 1) & 1, abort_flag, p.err))
+                        break;
+                }
+                tc_fence_after();
+                const uint32_t kbase = sbase + C::kOffKV + st * 2 * C::kKVBytes;
+                const uint32_t vbase = kbase + C::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
+                    const uint64_t ad = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * (kKeys * 128) +
+                                                            (kk & 3) * 32, 16, 1024);
+                    mma_f8f6f4(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(kSFull));
+                if (!wait_or_abort(bar(kPFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t pbase = sbase + C::kOffP + st * C::kPBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 32; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
+                    // V: MN-major; 8-key groups 1024 B apart, 128-byte D panels
+                    // kKeys * 128 B apart; 32 keys further = 4 groups
+                    const uint64_t bd = smem_desc_sw128(vbase + kk * 4096, kKeys * 128, 1024);
+                    const uint32_t acc = TWO_LEVEL ? (kk > 0 ? 1u : 0u)
+                                                   : ((j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f8f6f4(tO, ad, bd, idesc_pv, acc);
+                }
+                mma_commit(bar(kPvDone0 + st));
+                mma_commit(bar(kKvEmpty0 + st));
+            }
+            // every issued MMA finishes before tensor memory is released (bounded
+            // wait that does not stop early on an abort)
+            mma_commit(bar(kMmaIdle));
+            (void)mbar_wait_bounded(bar(kMmaIdle), 0);
+        }
+        __syncwarp();
+    } else {
+        // =============================== softmax / correction / epilogue (row = tid)
+        const int r = tid;
+        const int tk = tok0 + r / G;
+        const bool row_ok = tk < nq;
+        const int pos_r = row_ok ? pos_base + tk : -1;
+        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        const float kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
+        const float vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
+        const float sc = p.q_scale * kconst * p.scale_log2;
+        const float inv_ps = 1.0f / p.prob_scale;
+        float m = kMaxInitP, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            const int st = j & 1;
+            if (!__all_sync(0xffffffffu, wait_or_abort(bar(kSFull), j & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[kKeys];
+#pragma unroll
+            for (int cch = 0; cch < kKeys / 32; ++cch) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + cch * 32, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[cch * 32 + i] = __uint_as_float(rr[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kSEmpty));
+
+            // logits (base 2) with the causal mask; keys past ctx are always masked
+            const int key0 = j * kKeys;
+            float mx = -__int_as_float(0x7f800000);
+            const bool full = key0 + kKeys - 1 <= pos_r;
+#pragma unroll
+            for (int i = 0; i < kKeys; ++i) {
+                const float x = (full || key0 + i <= pos_r) ? s[i] * sc
+                                                            : -__int_as_float(0x7f800000);
+                s[i] = x;
+                mx = fmaxf(mx, x);
+            }
+            float alpha = 1.f;
+            if (mx > m + 8.f) {                 // lazy running max
+                alpha = ex2p(m - mx);
+                m = mx;
+                l *= alpha;
+            }
+            // a row whose max moved rescales its O row in TMEM (two-level off); the
+            // tcgen05 loads are warp-wide, so the warp does it when any row needs it
+            if (!TWO_LEVEL && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                {
+                    // O (TMEM) must hold PV of tile j-1 before it is rescaled
+                    if (!__all_sync(0xffffffffu,
+                                    wait_or_abort(bar(kPvDone0 + ((j - 1) & 1)),
+                                                  ((j - 1) >> 1) & 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cch = 0; cch < D / 32; ++cch) {
+                        uint32_t rr[32];
+                        const uint32_t ta = tmem + lane_addr + C::kOCol + cch * 32;
+                        tmem_ld32(ta, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        tmem_st32(ta, rr);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P8 tile j&1 was read by PV of tile j-2
+            if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(kPvDone0 + st),
+                                                                 ((j - 2) >> 1) & 1, abort_flag,
+                                                                 p.err))) {
+                ok = false;
+                break;
+            }
+            uint8_t* prow = smem + C::kOffP + st * C::kPBytes + r * 128;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {            // 16 keys per chunk
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float pa = ex2p(s[cc * 16 + 2 * i] - m) * inv_ps;
+                    const float pb = ex2p(s[cc * 16 + 2 * i + 1] - m) * inv_ps;
+                    const uint32_t code = e4m3x2_from_f32(pa, pb);
+                    if (i & 1)
+                        w[i >> 1] |= code << 16;
+                    else
+                        w[i >> 1] = code;
+                    // the denominator sums the same quantized weights
+                    const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
+                    l += q2.x + q2.y;
+                }
+                *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            // value rows past ctx in the last tile hold unwritten cache slots (any
+            // bytes, NaN codes included): zero them so 0 * v stays 0
+            if (key0 + kKeys > ctx) {
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(bar(kKvFull0 + st), (j >> 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* vt = smem + C::kOffKV + st * 2 * C::kKVBytes + C::kKVBytes;
+                for (int idx = r; idx < kKeys * C::kPanels * 8; idx += kRows) {
+                    const int chunk = idx & 7, row = (idx >> 3) % kKeys, pn = (idx >> 3) / kKeys;
+                    if (key0 + row >= ctx)
+                        *reinterpret_cast<uint4*>(vt + pn * (kKeys * 128) + row * 128 +
+                                                  chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(bar(kPFull0 + st));
+
+            if constexpr (TWO_LEVEL) {
+                // O_acc (fp32, TMEM columns [kOCol, kOCol + D)) = alpha * O_acc + P V of this tile
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(bar(kPvDone0 + st), (j >> 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int cch = 0; cch < D / 32; ++cch) {
+                    uint32_t pv[32], acc[32];
+                    tmem_ld32(tmem + lane_addr + cch * 32, pv);
+                    if (j > 0) tmem_ld32(tmem + lane_addr + C::kOCol + cch * 32, acc);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float prev = j > 0 ? __uint_as_float(acc[i]) * alpha : 0.f;
+                        acc[i] = __float_as_uint(prev + __uint_as_float(pv[i]));
+                    }
+                    tmem_st32(tmem + lane_addr + C::kOCol + cch * 32, acc);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(kPvtFree));
+            }
+        }
+        // ---- epilogue: out = O * (v_scale * prob_scale) / l
+        if (ok) {
+            const int last = n_tiles - 1;
+            if (!TWO_LEVEL &&
+                !__all_sync(0xffffffffu, wait_or_abort(bar(kPvDone0 + (last & 1)),
+                                                       (last >> 1) & 1, abort_flag, p.err)))
+                ok = false;
+        }
+        if (ok) {
+            tc_fence_after();
+            const float f = l > 0.f ? vconst * p.prob_scale / l : 0.f;
+            const int head = r % G;
+            for (int cch = 0; cch < D / 32; ++cch) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + C::kOCol + cch * 32, rr);
+                tmem_wait_ld();
+                if (row_ok) {
+                    const size_t o = (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D +
+                                     cch * 32;
+                    if (p.out_bf16) {
+                        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(
+                                __uint_as_float(rr[i]) * f, __uint_as_float(rr[i + 1]) * f);
+                    } else {
+                        float* dst = reinterpret_cast<float*>(p.out) + o;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) = make_float4(
+                                __uint_as_float(rr[i]) * f, __uint_as_float(rr[i + 1]) * f,
+                                __uint_as_float(rr[i + 2]) * f, __uint_as_float(rr[i + 3]) * f);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool TWO>
+cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
+    auto kern = prefill_fp8_kernel<D, TWO>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PCfg<D>::kSmem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    dim3 grid(grid_x, p.Hkv, p.B);
+    kern<<<grid, kThreads, PCfg<D>::kSmem, stream>>>(kmap, vmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int D, int two_level, int grid_x,
+                           cudaStream_t stream) {
+    if (D == 128)
+        return two_level ? launch_prefill_t<128, true>(p, kmap, vmap, grid_x, stream)
+                         : launch_prefill_t<128, false>(p, kmap, vmap, grid_x, stream);
+    return two_level ? launch_prefill_t<256, true>(p, kmap, vmap, grid_x, stream)
+                     : launch_prefill_t<256, false>(p, kmap, vmap, grid_x, stream);
+}
+
+}  // namespace fp8kv

@@ -146,6 +146,39 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
                             int out_dtype, int32_t* err_flag, void* cuda_stream);
 
 /*
+ * fp8kv_prefill_attn -- chunked causal prefill in FP8 on the tcgen05 tensor
+ * cores.  [KO] opening paragraph (FP8 e4m3 attention compute), "커널 및 퓨전
+ * 최적화" (query quantization fused into the kernel), "정확도를 위한 2단계 누적"
+ * and "아키텍처별 결과" (two-level FP32 accumulation and its switch); [KVQ] "Q/Prob
+ * 스케일과 FP8 Attention" (q_scale, prob_scale and the uncalibrated warning).
+ *
+ *   q              bf16 [Tq][Hq][D]: the new queries of every sequence back to back.
+ *   cu_seqlens_q   int32 [B+1] (device): sequence b owns q rows cu[b] .. cu[b+1]-1.
+ *   max_seqlen_q   host upper bound of cu[b+1] - cu[b] (sizes the grid).
+ *   k_cache, v_cache  e4m3 [num_blocks][Hkv][16][D] holding every key of the
+ *                  sequence, the chunk's own keys included (written before).
+ *   scale_mode     PER_TENSOR (k_scale[0], v_scale[0]) or PER_HEAD (k_scale[h]).
+ *   q_scale, prob_scale  host floats > 0: Q and the softmax weights are stored
+ *                  as e4m3(q / q_scale) and e4m3(p / prob_scale) for the MMAs.
+ *   context_lens   int32 [B]: keys of sequence b, the chunk included; query i of
+ *                  the chunk sits at position ctx - n_b + i and sees keys 0..that.
+ *   two_level      1: each KV tile's P V is added into a separate fp32
+ *                  accumulator on the CUDA cores; 0: the tensor core accumulates
+ *                  across tiles (enough on Blackwell).
+ *   out            [Tq][Hq][D] fp32 or bf16.
+ * Supported: e4m3 cache, D in {128, 256}, Hq / Hkv dividing 128.  Other modes
+ * return FP8KV_ERR_UNSUPPORTED.  With q_scale or prob_scale equal to 1.0 the
+ * call succeeds and sets fp8kv_last_warning().
+ */
+int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
+                       const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
+                       const float* k_scale, const float* v_scale, float q_scale,
+                       float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
+                       const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                       int64_t num_blocks, float softmax_scale, int two_level, void* out,
+                       int out_dtype, int32_t* err_flag, void* cuda_stream);
+
+/*
  * fp8kv_quantize_e4m3 -- the cache writer's encoder on its own: out[i] =
  * e4m3_rn_satfinite(fp32(x[i] / scale)) for n fp32 values (device arrays).
  * [PR] "코드 분석" (torch.float8_e4m3fn storage).  A zero scale writes code 0.

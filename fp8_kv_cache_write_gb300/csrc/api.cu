@@ -333,7 +333,7 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
         !(prob_scale < 3.0e38f) || !(softmax_scale == softmax_scale))
         return FP8KV_ERR_INVALID;
     const int G = Hq / Hkv;
-    if (kv_dtype != FP8KV_KV_E4M3 || scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD ||
+    if ((kv_dtype == FP8KV_KV_E4M3 && scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) ||
         (D != 128 && D != 256) || G > 128 || (128 % G) != 0)
         return FP8KV_ERR_UNSUPPORTED;
     if (B == 0 || max_seqlen_q == 0) return FP8KV_OK;
@@ -342,14 +342,15 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     if (num_blocks * static_cast<int64_t>(Hkv) >= (int64_t{1} << 31) ||
         static_cast<int64_t>(max_blocks_per_seq) * FP8KV_PAGE_SIZE >= (int64_t{1} << 31))
         return FP8KV_ERR_UNSUPPORTED;
-    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_table || !context_lens || !out ||
-        !k_scale || !v_scale)
+    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_table || !context_lens || !out)
         return FP8KV_ERR_INVALID;
+    if (kv_dtype == FP8KV_KV_E4M3 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return FP8KV_ERR_INVALID;
     CUtensorMap kmap, vmap;
     const int64_t nbh = num_blocks * Hkv;
-    if (!make_kv_map(k_cache, D, nbh, &kmap) || !make_kv_map(v_cache, D, nbh, &vmap))
+    const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
+    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap) || !make_kv_map(v_cache, row_bytes, nbh, &vmap))
         return FP8KV_ERR_CUDA;
     PrefillParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -367,16 +368,16 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     p.prob_scale = prob_scale;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    p.scale_mode = scale_mode;
+    p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
     p.err = err_flag;
     const int tpt = 128 / G;
     const int grid_x = (max_seqlen_q + tpt - 1) / tpt;
-    cudaError_t e = launch_prefill(p, kmap, vmap, D, two_level, grid_x,
+    cudaError_t e = launch_prefill(p, kmap, vmap, D, kv_dtype, two_level, grid_x,
                                    static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return FP8KV_ERR_CUDA;
-    if (q_scale == 1.0f || prob_scale == 1.0f)
+    if (kv_dtype == FP8KV_KV_E4M3 && (q_scale == 1.0f || prob_scale == 1.0f))
         g_warning = "fp8 attention with uncalibrated q_scale and/or prob_scale of 1.0";
     return FP8KV_OK;
 }

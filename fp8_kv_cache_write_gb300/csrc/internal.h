@@ -84,8 +84,8 @@ struct PrefillParams {
 };
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int D, int two_level, int grid_x,
-                           cudaStream_t stream);
+                           const CUtensorMap& vmap, int D, int kv_dtype, int two_level,
+                           int grid_x, cudaStream_t stream);
 
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;

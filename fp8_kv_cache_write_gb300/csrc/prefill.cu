@@ -39,20 +39,24 @@ namespace fp8kv {
 namespace {
 
 constexpr int kRows = 128;          // MMA M: query rows of a CTA
-constexpr int kKeys = 128;          // keys per KV tile (8 pages)
 constexpr int kThreads = 192;
 constexpr float kMaxInitP = -1.0e30f;
 
-template <int D>
+template <int D, bool BF16>
 struct PCfg {
+    // e4m3 tiles hold 128 keys (8 pages), bf16 tiles 64 keys (4 pages) so that
+    // D = 256 still fits in shared memory; every MMA k-step is 32 bytes wide
+    static constexpr int kElem = BF16 ? 2 : 1;
+    static constexpr int kKeys = BF16 ? 64 : 128;
+    static constexpr int kRowB = D * kElem;                 // bytes of a Q / K / V row
     // tensor memory: S (or the two-level P V tile) from column 0, O from kOCol;
     // D 128 takes 256 columns so two co-resident CTAs never wait on each other
     static constexpr uint32_t kTmemCols = D <= 128 ? 256u : 512u;
     static constexpr uint32_t kOCol = D <= 128 ? 128u : 256u;
-    static constexpr int kPanels = D / 128;                 // 128-byte K panels of a row
-    static constexpr int kQBytes = kRows * D;               // Q8 tile
-    static constexpr int kKVBytes = kKeys * D;              // one K (or V) tile
-    static constexpr int kPBytes = kRows * kKeys;           // one P8 tile
+    static constexpr int kPanels = kRowB / 128;             // 128-byte panels of a row
+    static constexpr int kQBytes = kRows * kRowB;           // Q tile
+    static constexpr int kKVBytes = kKeys * kRowB;          // one K (or V) tile
+    static constexpr int kPBytes = kRows * kKeys * kElem;   // one P tile (128-byte rows)
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;          // [stage][K | V]
     static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes; // [2] P8 tiles
@@ -90,11 +94,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
-template <int D, bool TWO_LEVEL>
+template <int D, bool TWO_LEVEL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
+    prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-    using C = PCfg<D>;
+    using C = PCfg<D, BF16>;
+    constexpr int kKeys = C::kKeys;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -144,29 +149,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 5) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
-    // ---- Q8 = e4m3(q / q_scale) into the K-major, 128-byte-swizzled A tile
+    // ---- Q tile (K-major, 128-byte swizzle): e4m3(q / q_scale), or q itself (bf16)
     if (warp < 4) {
         const int r = tid;
         const int tk = tok0 + r / G, head = r % G;
-        uint8_t* qrow_s = smem + C::kOffQ;
+        uint8_t* qtile = smem + C::kOffQ;
 #pragma unroll 4
-        for (int c = 0; c < D / 16; ++c) {              // 16 e4m3 bytes per chunk
+        for (int c = 0; c < C::kRowB / 16; ++c) {       // 16-byte chunks of the row
             uint32_t w[4] = {0u, 0u, 0u, 0u};
             if (tk < nq) {
                 const __nv_bfloat16* src =
-                    p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D + c * 16;
-                const uint4 a = *reinterpret_cast<const uint4*>(src);
-                const uint4 bq = *reinterpret_cast<const uint4*>(src + 8);
-                const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+                    p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D +
+                    c * (16 / C::kElem);
+                if constexpr (BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(src);
+                    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4*>(src);
+                    const uint4 bq = *reinterpret_cast<const uint4*>(src + 8);
+                    const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float lo = __fdiv_rn(bf16_bits_to_float(in[i] & 0xffffu), p.q_scale);
-                    const float hi = __fdiv_rn(bf16_bits_to_float(in[i] >> 16), p.q_scale);
-                    w[i >> 1] |= static_cast<uint32_t>(e4m3x2_from_f32(lo, hi)) << (16 * (i & 1));
+                    for (int i = 0; i < 8; ++i) {
+                        const float lo = __fdiv_rn(bf16_bits_to_float(in[i] & 0xffffu), p.q_scale);
+                        const float hi = __fdiv_rn(bf16_bits_to_float(in[i] >> 16), p.q_scale);
+                        w[i >> 1] |= static_cast<uint32_t>(e4m3x2_from_f32(lo, hi))
+                                     << (16 * (i & 1));
+                    }
                 }
             }
             const int panel = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(qrow_s + panel * (kRows * 128) + r * 128 +
+            *reinterpret_cast<uint4*>(qtile + panel * (kRows * 128) + r * 128 +
                                       ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async();                            // generic writes -> tensor core reads
@@ -191,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_pages = n_pages > kKeys / kPage ? kKeys / kPage : n_pages;
             if (lane == 0)
                 mbar_arrive_expect_tx(bar(kKvFull0 + st),
-                                      static_cast<uint32_t>(n_pages) * 2u * kPage * D);
+                                      static_cast<uint32_t>(n_pages) * 2u * kPage * C::kRowB);
             __syncwarp();
             if (lane < n_pages) {
                 int blk = bt_row[page0 + lane];
@@ -222,8 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 5) {
         // =============================== MMA issuer (one thread)
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, kKeys, kRows);
-            constexpr uint32_t idesc_pv = instr_desc(0, 0, 0, 1, D, kRows);
+            // e4m3 operands (kind::f8f6f4, format 0) or bf16 (kind::f16, format 1)
+            constexpr uint32_t kFmt = BF16 ? 1u : 0u;
+            constexpr uint32_t idesc_qk = instr_desc(kFmt, kFmt, 0, 0, kKeys, kRows);
+            constexpr uint32_t idesc_pv = instr_desc(kFmt, kFmt, 0, 1, D, kRows);
+            auto mma = [&](uint32_t d, uint64_t a, uint64_t bdsc, uint32_t id, uint32_t acc) {
+                if constexpr (BF16)
+                    mma_f16kind(d, a, bdsc, id, acc);
+                else
+                    mma_f8f6f4(d, a, bdsc, id, acc);
+            };
             const uint32_t tS = tmem;                           // S: columns [0, 128)
             const uint32_t tO = tmem + (TWO_LEVEL ? 0u : C::kOCol); // PV target
             for (int j = 0; j < n_tiles; ++j) {
@@ -239,26 +259,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kbase = sbase + C::kOffKV + st * 2 * C::kKVBytes;
                 const uint32_t vbase = kbase + C::kKVBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
+                for (int kk = 0; kk < C::kRowB / 32; ++kk) {    // 32-byte k-steps over D
                     const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
                     const uint64_t ad = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * (kKeys * 128) +
                                                             (kk & 3) * 32, 16, 1024);
-                    mma_f8f6f4(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    mma(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(kSFull));
                 if (!wait_or_abort(bar(kPFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t pbase = sbase + C::kOffP + st * C::kPBytes;
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 32; ++kk) {
+                for (int kk = 0; kk < kKeys * C::kElem / 32; ++kk) {   // 32-byte k-steps over keys
                     const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
                     // V: MN-major; 8-key groups 1024 B apart, 128-byte D panels
-                    // kKeys * 128 B apart; 32 keys further = 4 groups
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 4096, kKeys * 128, 1024);
+                    // kKeys * 128 B apart; one k-step = 32 / elem keys
+                    const uint64_t bd = smem_desc_sw128(vbase + kk * (32 / C::kElem) * 128,
+                                                        kKeys * 128, 1024);
                     const uint32_t acc = TWO_LEVEL ? (kk > 0 ? 1u : 0u)
                                                    : ((j > 0 || kk > 0) ? 1u : 0u);
-                    mma_f8f6f4(tO, ad, bd, idesc_pv, acc);
+                    mma(tO, ad, bd, idesc_pv, acc);
                 }
                 mma_commit(bar(kPvDone0 + st));
                 mma_commit(bar(kKvEmpty0 + st));
@@ -276,10 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = tk < nq;
         const int pos_r = row_ok ? pos_base + tk : -1;
         const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-        const float kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
-        const float vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
-        const float sc = p.q_scale * kconst * p.scale_log2;
-        const float inv_ps = 1.0f / p.prob_scale;
+        // the bf16 cache has no scales and keeps Q and P in bf16
+        float kconst = 1.f, vconst = 1.f, qs = 1.f, ps = 1.f;
+        if constexpr (!BF16) {
+            kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
+            vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
+            qs = p.q_scale;
+            ps = p.prob_scale;
+        }
+        const float sc = qs * kconst * p.scale_log2;
+        const float inv_ps = 1.0f / ps;
         float m = kMaxInitP, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -352,21 +379,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             uint8_t* prow = smem + C::kOffP + st * C::kPBytes + r * 128;
+            constexpr int kPerChunk = 16 / C::kElem;    // keys per 16-byte chunk
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {            // 16 keys per chunk
+            for (int cc = 0; cc < 8; ++cc) {
                 uint32_t w[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float pa = ex2p(s[cc * 16 + 2 * i] - m) * inv_ps;
-                    const float pb = ex2p(s[cc * 16 + 2 * i + 1] - m) * inv_ps;
-                    const uint32_t code = e4m3x2_from_f32(pa, pb);
-                    if (i & 1)
-                        w[i >> 1] |= code << 16;
-                    else
-                        w[i >> 1] = code;
-                    // the denominator sums the same quantized weights
-                    const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
-                    l += q2.x + q2.y;
+                for (int i = 0; i < kPerChunk / 2; ++i) {
+                    const float pa = ex2p(s[cc * kPerChunk + 2 * i] - m) * inv_ps;
+                    const float pb = ex2p(s[cc * kPerChunk + 2 * i + 1] - m) * inv_ps;
+                    // the denominator sums the same rounded weights the MMA uses
+                    if constexpr (BF16) {
+                        w[i] = pack_bf16x2(pa, pb);
+                        const float2 q2 = unpack_bf16x2(w[i]);
+                        l += q2.x + q2.y;
+                    } else {
+                        const uint32_t code = e4m3x2_from_f32(pa, pb);
+                        if (i & 1)
+                            w[i >> 1] |= code << 16;
+                        else
+                            w[i >> 1] = code;
+                        const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
+                        l += q2.x + q2.y;
+                    }
                 }
                 *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
@@ -427,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
-            const float f = l > 0.f ? vconst * p.prob_scale / l : 0.f;
+            const float f = l > 0.f ? vconst * ps / l : 0.f;
             const int head = r % G;
             for (int cch = 0; cch < D / 32; ++cch) {
                 uint32_t rr[32];
@@ -463,35 +497,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool TWO>
+template <int D, bool TWO, bool BF16>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
-    auto kern = prefill_fp8_kernel<D, TWO>;
+    auto kern = prefill_kernel<D, TWO, BF16>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PCfg<D>::kSmem);
+                                 PCfg<D, BF16>::kSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     dim3 grid(grid_x, p.Hkv, p.B);
-    kern<<<grid, kThreads, PCfg<D>::kSmem, stream>>>(kmap, vmap, p);
+    kern<<<grid, kThreads, PCfg<D, BF16>::kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_two(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       int two_level, int grid_x, cudaStream_t stream) {
+    return two_level ? launch_prefill_t<D, true, BF16>(p, kmap, vmap, grid_x, stream)
+                     : launch_prefill_t<D, false, BF16>(p, kmap, vmap, grid_x, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int D, int two_level, int grid_x,
-                           cudaStream_t stream) {
+                           const CUtensorMap& vmap, int D, int kv_dtype, int two_level,
+                           int grid_x, cudaStream_t stream) {
+    const bool bf = kv_dtype == FP8KV_KV_BF16;
     if (D == 128)
-        return two_level ? launch_prefill_t<128, true>(p, kmap, vmap, grid_x, stream)
-                         : launch_prefill_t<128, false>(p, kmap, vmap, grid_x, stream);
-    return two_level ? launch_prefill_t<256, true>(p, kmap, vmap, grid_x, stream)
-                     : launch_prefill_t<256, false>(p, kmap, vmap, grid_x, stream);
+        return bf ? launch_two<128, true>(p, kmap, vmap, two_level, grid_x, stream)
+                  : launch_two<128, false>(p, kmap, vmap, two_level, grid_x, stream);
+    return bf ? launch_two<256, true>(p, kmap, vmap, two_level, grid_x, stream)
+              : launch_two<256, false>(p, kmap, vmap, two_level, grid_x, stream);
 }
 
 }  // namespace fp8kv

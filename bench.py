@@ -252,7 +252,7 @@ def run_ours(args, dev, w, world, rank):
         splits, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0, args.splits)
         ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-        launches_per_step[name] = 2 + (1 if splits > 1 else 0)
+        launches_per_step[name] = 3          # cache write, decode, split_merge
         d_b, w_b = step_bytes(w, 1 if kv_dtype == fk.KV_E4M3 else 2, kv_dtype == fk.KV_E4M3)
         dec_bytes[name] = d_b
 
@@ -434,6 +434,187 @@ def run_reference(args, w, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+
+# ----------------------------------------------------------------- extras
+def _time_graph(fn, n_calls, stream, warmup=3):
+    """Mean ms of fn(i) over n_calls calls captured in one CUDA graph (after
+    eager warm-up calls), replayed twice; events on the capture stream."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i)
+    torch.cuda.synchronize()
+    g = _graph(fn, n_calls, stream)
+    g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        g.replay()
+        g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / (2 * n_calls)
+
+
+def _decode_caller(fk, w, kv_dtype, mode, caches, dev, window=0):
+    q, bt, cl = w.q.to(dev), w.block_table.to(dev), w.context_lens.to(dev)
+    _, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, bt.shape[1], window)
+    ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
+    ksc = w.k_scale.to(dev) if w.k_scale is not None else None
+    vsc = w.v_scale.to(dev) if w.v_scale is not None else None
+
+    def decode(i):
+        kc, vc, ks, vs = caches[i % len(caches)]
+        fk.paged_decode_attn(q, kc, vc, bt, cl, kv_dtype=kv_dtype, scale_mode=mode,
+                             k_scale=ksc, v_scale=vsc, k_scale_cache=ks, v_scale_cache=vs,
+                             window=window, workspace=ws, out=out)
+    return decode
+
+
+def _caches_for(fk, w, kv_dtype, mode, dev, copies):
+    dt = torch.uint8 if kv_dtype == fk.KV_E4M3 else torch.bfloat16
+    k_hist, v_hist, hs = w.k_hist.to(dev), w.v_hist.to(dev), w.hist_slots.to(dev)
+    k_new, v_new, ns = w.k_new.to(dev), w.v_new.to(dev), w.new_slots.to(dev)
+    ksc = w.k_scale.to(dev) if w.k_scale is not None else None
+    vsc = w.v_scale.to(dev) if w.v_scale is not None else None
+    out = []
+    for _ in range(copies):
+        kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=dt, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.num_blocks, w.Hkv, 16, dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        for k_in, v_in, s_in in ((k_hist, v_hist, hs), (k_new, v_new, ns)):
+            fk.kv_cache_write(k_in, v_in, s_in, kc, vc, kv_dtype=kv_dtype, scale_mode=mode,
+                              k_scale=ksc, v_scale=vsc, k_scale_cache=ks, v_scale_cache=vs)
+        out.append((kc, vc, ks, vs))
+    torch.cuda.synchronize()
+    return out
+
+
+def _copies_for(bytes_per_copy):
+    """Cache copies to rotate over so that consecutive calls never find the
+    previous call's data in the 129 MB L2."""
+    return max(2, math.ceil(260e6 / max(bytes_per_copy, 1)))
+
+
+def run_extras(args, dev):
+    """The other workloads: decode time against context length (fp8 vs bf16),
+    the 131k needle, the 24-layer hybrid model, chunked FP8 prefill and the
+    bulk cache write.  One JSON line each."""
+    import fp8_kv_cache_write_gb300 as fk
+    from fp8_kv_cache_write_gb300 import synth
+    stream = torch.cuda.Stream(dev)
+    emit = lambda d: print(json.dumps(d), flush=True)
+    E4, BF = fk.KV_E4M3, fk.KV_BF16
+
+    # (1) inter-token latency against context: B=8, 32/8 heads, D=128, decode only
+    for ctx in (2048, 4096, 8192, 16384, 32768):
+        w = synth.decode_workload(2000 + ctx, [ctx] * 8, 32, 8, 128, 2, device=dev)
+        row = {"extra": "itl_vs_context", "B": 8, "context": ctx}
+        for kv, name in ((E4, "fp8"), (BF, "bf16")):
+            mode = 2 if kv == E4 else 0
+            d_b, _ = step_bytes(w, 1 if kv == E4 else 2, kv == E4)
+            caches = _caches_for(fk, w, kv, mode, dev, _copies_for(d_b))
+            ms = _time_graph(_decode_caller(fk, w, kv, mode, caches, dev), 64, stream)
+            row[name + "_us"] = ms * 1e3
+            row[name + "_gbs"] = d_b / ms / 1e6
+            del caches
+            torch.cuda.empty_cache()
+        row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
+        emit(row)
+        del w
+
+    # (2) 131072-token needle: B=1, 64/8 heads, per-KV-head scales
+    w = synth.needle(device=dev)
+    row = {"extra": "needle_131k", "B": 1, "context": 131072}
+    for kv, name in ((E4, "fp8"), (BF, "bf16")):
+        mode = 1 if kv == E4 else 0
+        d_b, _ = step_bytes(w, 1 if kv == E4 else 2, False)
+        caches = _caches_for(fk, w, kv, mode, dev, _copies_for(d_b))
+        ms = _time_graph(_decode_caller(fk, w, kv, mode, caches, dev), 32, stream)
+        row[name + "_us"], row[name + "_gbs"] = ms * 1e3, d_b / ms / 1e6
+        del caches
+        torch.cuda.empty_cache()
+    row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
+    emit(row)
+    del w
+
+    # (3) hybrid model, 24 layers alternating sliding-window-128 / full attention:
+    #     one step = the decode of all 24 layers (each layer type rotates over
+    #     its own cache copies); tokens/s = B / step time
+    wl = {0: synth.hybrid_layer(layer=0, device=dev), 1: synth.hybrid_layer(layer=1, device=dev)}
+    for variant, dtypes in (("all_bf16", (BF, BF)), ("all_fp8", (E4, E4)),
+                            ("window_bf16_full_fp8", (BF, E4))):
+        calls = []
+        for lt in (0, 1):
+            w, kv = wl[lt], dtypes[lt]
+            mode = 2 if kv == E4 else 0
+            d_b, _ = step_bytes(w, 1 if kv == E4 else 2, kv == E4)
+            caches = _caches_for(fk, w, kv, mode, dev, 2 if lt == 0 else _copies_for(d_b))
+            calls.append(_decode_caller(fk, w, kv, mode, caches, dev, window=w.window))
+
+        def step(i):
+            for layer in range(24):
+                calls[layer % 2](i * 12 + layer // 2)
+        ms = _time_graph(step, 8, stream)
+        per_type = [_time_graph(calls[lt], 24, stream) * 1e3 for lt in (0, 1)]
+        emit({"extra": "hybrid_24_layers", "variant": variant, "B": 32,
+              "ms_per_step": ms, "tokens_per_s": 32 / (ms / 1e3),
+              "window_layer_us": per_type[0], "full_layer_us": per_type[1]})
+        del calls
+        torch.cuda.empty_cache()
+    del wl
+
+    # (4) chunked prefill: 4096 new queries over 32768 cached tokens, 8/1 heads, D=256
+    w = synth.prefill(device=dev)
+    q, cu = w.q.to(dev), w.cu_seqlens_q.to(dev)
+    bt, cl = w.block_table.to(dev), w.context_lens.to(dev)
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    out = torch.empty(q.shape[0], w.Hq, w.D, dtype=torch.float32, device=dev)
+    c0 = int(w.context_lens[0]) - int(w.cu_seqlens_q[1])
+    pairs = sum(c0 + i + 1 for i in range(int(w.cu_seqlens_q[1])))
+    flops = 4.0 * w.D * w.Hq * pairs
+    for kv, name in ((E4, "fp8"), (BF, "bf16")):
+        dt = torch.uint8 if kv == E4 else torch.bfloat16
+        kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=dt, device=dev)
+        vc = torch.zeros_like(kc)
+        fk.kv_cache_write(w.k_all.to(dev), w.v_all.to(dev), w.all_slots.to(dev), kc, vc,
+                          kv_dtype=kv, scale_mode=0, k_scale=one, v_scale=one)
+        for two in (False, True):
+            fn = lambda i, kc=kc, vc=vc, kv=kv, two=two: fk.prefill_attn(
+                q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=kv, k_scale=one, v_scale=one,
+                two_level=two, out=out)
+            ms = _time_graph(fn, 10, stream)
+            emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": name, "two_level": two,
+                  "ms": ms, "tflops": flops / ms / 1e9})
+        del kc, vc
+        torch.cuda.empty_cache()
+    del w
+
+    # (5) bulk cache write: 32768 tokens x 8 KV heads x 128, per-token-head e4m3
+    T, H, D = 32768, 8, 128
+    gen = torch.Generator(device=dev).manual_seed(6)
+    sets = []
+    for _ in range(2):
+        k = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
+        sets.append((k, v))
+    nb = T // 16 + 16
+    slots = torch.randperm(nb * 16, generator=gen, device=dev)[:T].to(torch.int64)
+    kc = torch.zeros(nb, H, 16, D, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(nb, H, 16, dtype=torch.float32, device=dev)
+    vs = torch.zeros_like(ks)
+    fn = lambda i: fk.kv_cache_write(sets[i % 2][0], sets[i % 2][1], slots, kc, vc,
+                                     kv_dtype=E4, scale_mode=2, k_scale_cache=ks,
+                                     v_scale_cache=vs)
+    ms = _time_graph(fn, 20, stream)
+    nbytes = T * H * (2 * D * 2 + 2 * D + 8) + T * 8
+    emit({"extra": "bulk_cache_write", "tokens": T, "Hkv": H, "D": D, "us": ms * 1e3,
+          "gbs": nbytes / ms / 1e6})
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,6 +628,9 @@ def main():
     ap.add_argument("--rotations", type=int, default=ROTATIONS,
                     help="cache copies rotated between steps (each larger than L2)")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planner)")
+    ap.add_argument("--extras", action="store_true",
+                    help="time the other workloads (context sweep, needle, hybrid, prefill, "
+                         "bulk write) instead of the headline step; one JSON line each")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -459,6 +643,15 @@ def main():
         else:
             torch.cuda.set_device(local)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    if args.extras and args.impl == "ours":
+        import fp8_kv_cache_write_gb300 as fk
+        fk.lib()
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        if rank == 0:
+            run_extras(args, dev)
+        return
 
     from fp8_kv_cache_write_gb300 import synth
     w = synth.llama8b(seed=1002 + rank)

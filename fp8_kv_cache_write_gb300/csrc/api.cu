@@ -108,15 +108,17 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out)
 }
 
 struct Plan {
-    int num_splits;
-    int pages_per_split;
+    int num_splits;          // CTAs of the decode grid (work partitions)
     size_t workspace_bytes;
 };
 
-// Split planner.  The visible pages of a sequence are at most max_blocks (or,
-// with a window w, ceil(w/16)+1).  Automatic: about 4 CTAs per SM of page
-// work in total, 16..128 pages per split; the split count is then rebalanced
-// so every split but the last has the same number of pages.
+// Decode planner.  The launch's (seq, KV head, page) tiles are split evenly over
+// the 4 warps of `num_splits` CTAs.  Automatic: one wave of resident CTAs, but no fewer than
+// 16 tiles per CTA for the upper bound of the work (B * Hkv * visible pages);
+// an explicit count n asks for about n partitions per (seq, KV head) unit.
+// Workspace: one (m, l, O) slot per (warp, unit) pair a warp can touch, i.e.
+// 4 * num_splits + B * Hkv slots of G query heads, then the first / last worker
+// of every unit.
 int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out) {
     int maxvis = max_blocks;
     if (window > 0) {
@@ -124,27 +126,25 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
         if (wp < maxvis) maxvis = wp;
     }
     if (maxvis < 1) maxvis = 1;
-    int S;
+    const int64_t units = static_cast<int64_t>(B) * Hkv;
+    const int64_t work = units * maxvis;
+    int64_t n;
     if (req > 0) {
-        S = req < maxvis ? req : maxvis;
+        n = static_cast<int64_t>(req) * units;
     } else {
-        // fill one wave of resident CTAs (3 per SM for the shipped tile sizes),
-        // keeping at least 16 pages (4 per warp) in a split
-        const int64_t units = static_cast<int64_t>(B) * Hkv;
-        const int64_t slots = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0);
-        int64_t s_wave = slots / (units > 0 ? units : 1);
-        if (s_wave < 1) s_wave = 1;
-        const int64_t s_min_pages = (maxvis + 15) / 16;
-        S = static_cast<int>(s_wave < s_min_pages ? s_wave : s_min_pages);
+        n = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0);
+        const int64_t by_work = (work + 15) / 16;
+        if (by_work < n) n = by_work;
     }
-    if (S > 1024) S = 1024;
-    if (S < 1) S = 1;
-    int pps = (maxvis + S - 1) / S;
-    S = (maxvis + pps - 1) / pps;
-    out->num_splits = S;
-    out->pages_per_split = pps;
-    out->workspace_bytes =
-        S > 1 ? static_cast<size_t>(B) * Hq * S * (static_cast<size_t>(D) + 2) * sizeof(float) : 0;
+    if (n > work) n = work;
+    if (n > 1024) n = 1024;
+    if (n < 1) n = 1;
+    out->num_splits = static_cast<int>(n);
+    const int64_t G = Hkv > 0 ? Hq / Hkv : 1;
+    const int64_t workers = n * kDecodeWarps;      // every warp is a worker
+    out->workspace_bytes = static_cast<size_t>(workers + units) * G *
+                               (static_cast<size_t>(D) + 2) * sizeof(float) +
+                           static_cast<size_t>(units) * 2 * sizeof(int);
     return FP8KV_OK;
 }
 
@@ -254,6 +254,13 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
         return FP8KV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * FP8KV_PAGE_SIZE >= (int64_t{1} << 31))
         return FP8KV_ERR_UNSUPPORTED;
+    // the partition arithmetic multiplies tile counts (<= B * Hkv * pages) by
+    // worker counts (<= 4096) in 64 bits
+    if (static_cast<int64_t>(B) * Hkv * max_blocks_per_seq >= (int64_t{1} << 50))
+        return FP8KV_ERR_UNSUPPORTED;
+    // one sequence's (KV head, page) tiles are indexed in 32 bits
+    if (static_cast<int64_t>(max_blocks_per_seq) * Hkv >= (int64_t{1} << 31))
+        return FP8KV_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
         return FP8KV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
@@ -270,10 +277,8 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
     }
     Plan pl;
     plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &pl);
-    if (pl.num_splits > 1) {
-        if (!workspace || workspace_bytes < pl.workspace_bytes) return FP8KV_ERR_WORKSPACE;
-        if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
-    }
+    if (!workspace || workspace_bytes < pl.workspace_bytes) return FP8KV_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
     const int64_t nbh = num_blocks * Hkv;
     CUtensorMap kmap, vmap;
@@ -297,13 +302,15 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.window = window;
     p.num_splits = pl.num_splits;
-    p.pages_per_split = pl.pages_per_split;
-    if (pl.num_splits > 1) {
+    {
         float* ws = static_cast<float*>(workspace);
-        const size_t rows = static_cast<size_t>(B) * Hq * pl.num_splits;
+        const size_t rows = (static_cast<size_t>(pl.num_splits) * kDecodeWarps +
+                             static_cast<size_t>(B) * Hkv) * (Hq / Hkv);
         p.ws_o = ws;
         p.ws_m = ws + rows * D;
         p.ws_l = p.ws_m + rows;
+        p.ws_first = reinterpret_cast<int*>(p.ws_l + rows);
+        p.ws_last = p.ws_first + static_cast<size_t>(B) * Hkv;
     }
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;

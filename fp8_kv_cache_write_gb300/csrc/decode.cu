@@ -10,10 +10,14 @@
 // over the visible positions t (all ctx keys, or the last `window`).
 //
 // Design (GB300):
-//   * grid (split, kv head, seq); 4 warps per CTA share one split's pages
-//     round-robin; each warp runs its own TMA ring: lane 0 issues 3-D tiled
-//     tensor copies (128-byte swizzle) of the K and V page tiles -- plus the
-//     64-byte per-token scale rows -- onto an mbarrier, S stages ahead.
+//   * one wave of CTAs of 4 warps; every warp is an independent worker: the
+//     (seq, KV head, page) tiles of the whole launch are flattened and each warp
+//     takes an equal consecutive share, crossing (seq, KV head) units where its
+//     share does, so any mix of context lengths keeps all SMs equally busy.
+//     Each warp runs its own TMA ring that streams straight across unit
+//     boundaries: lane 0 issues 3-D tiled tensor copies (128-byte swizzle) of the
+//     K and V page tiles -- plus the 64-byte per-token scale rows -- onto an
+//     mbarrier, S stages ahead; two pages per iteration.
 //   * math on the legacy tensor pipe (mma.sync m16n8k16, fp32 accumulate):
 //     S^T = K_page . Q^T with M = 16 page tokens, N = 8 query heads of the GQA
 //     group, K = D; then O^T += V_page^T . P^T with M = D, N = heads, K = the 16
@@ -24,13 +28,15 @@
 //     logit (k) and per weight (v).  Per-tensor / per-head scales multiply the
 //     logit scale and the final output.
 //   * online softmax in base 2 with a lazy max (the running max moves only when
-//     a page exceeds it by 2^8), fp32 everywhere.
+//     a page exceeds it by 2^4 for e4m3, 2^8 for bf16), fp32 everywhere.
 //   * the fragment row/column orders are permuted (token pi(g), d-chunk pi(g))
 //     so that every 16-byte shared-memory read of the swizzled tiles is free of
 //     bank conflicts for D = 128 e4m3; the permutation is undone when writing.
-//   * each split writes (m, l, unnormalised O) to the workspace; split_merge
-//     combines the valid splits of a (seq, head).  One split writes `out`
-//     directly.
+//   * a warp that covers a whole unit writes `out` directly; otherwise it leaves
+//     (m, l, unnormalised O) in workspace slot worker + unit and split_merge
+//     combines the workers that touched each unit.  (A merge inside this kernel,
+//     by the CTA that completes a unit, ran slower: its loads queue behind the
+//     other SMs' streaming, while split_merge runs on an idle memory system.)
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -64,10 +70,13 @@ struct Cfg {
     static constexpr int kBoxes = kRowB >= 128 ? kRowB / 128 : 1;
     static constexpr int kWarpSmem = kStages * kStageB;
     static constexpr int kScaleB = 128;               // k scales + v scales of one page
-    static constexpr int kSmem = 1024 + kWarps * kWarpSmem + kWarps * kStages * kPPI * kScaleB +
-                                 kWarps * kStages * 8 + 16;
+    static constexpr int kMaxSeg = 16;                // segments a warp lists per pass
+    static constexpr int kSegInts = 9;                // ints of one segment record
+    static constexpr int kOffBars = kWarps * kWarpSmem + kWarps * kStages * kPPI * kScaleB;
+    static constexpr int kOffSegs = kOffBars + kWarps * kStages * 8;
+    static constexpr int kOffShare = kOffSegs + kWarps * kMaxSeg * kSegInts * 4;  // [warp][resume, end]
+    static constexpr int kSmem = 1024 + kOffShare + kWarps * 16;
     static_assert(kSegs * kKPerSeg == kKSteps, "k-step split");
-    static_assert(kWarps * 8 * (D + 2) * 4 <= kWarps * kWarpSmem, "merge area fits the rings");
 };
 
 // The fragment permutation: M row g <-> token pi(g) (and pi(g)+8); lane group g
@@ -135,6 +144,13 @@ __device__ __forceinline__ void visible(const DecodeParams& p, int b, int& lo, i
     p_hi = (ctx + kPage - 1) / kPage;
 }
 
+// Visible pages of sequence b (0 when its context is empty).
+__device__ __forceinline__ int vis_pages(const DecodeParams& p, int b) {
+    int lo, ctx, p_lo, p_hi;
+    visible(p, b, lo, ctx, p_lo, p_hi, false);
+    return p_hi > p_lo ? p_hi - p_lo : 0;
+}
+
 template <bool BF16>
 __device__ __forceinline__ void store_out(void* out, int out_bf16, size_t idx, float v) {
     if (out_bf16)
@@ -143,56 +159,139 @@ __device__ __forceinline__ void store_out(void* out, int out_bf16, size_t idx, f
         reinterpret_cast<float*>(out)[idx] = v;
 }
 
+// D <= 128 keeps 3 CTAs (12 warps) resident per SM: 168 registers at most
 template <int D, bool BF16, bool PER_TOKEN>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
     using C = Cfg<D, BF16>;
+    constexpr int PPI = C::kPPI;
+    constexpr int kMaxSeg = C::kMaxSeg;
+    constexpr int kSegInts = C::kSegInts;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = p.G;
+    pdl_trigger();                        // split_merge may launch while this runs
+    pdl_wait();                           // inputs of earlier kernels are visible
 
-    int lo, ctx, p_lo, p_hi;
-    visible(p, b, lo, ctx, p_lo, p_hi, split == 0 && h == 0 && threadIdx.x == 0);
-    const int pb = p_lo + split * p.pages_per_split;
-    const int pe = min(pb + p.pages_per_split, p_hi);
-    if (pb >= pe) {
-        if (p.num_splits == 1 && split == 0) {   // empty context: zero rows
-            for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-                const int hq = h * G + i / D;
-                store_out<BF16>(p.out, p.out_bf16, (static_cast<size_t>(b) * p.Hq + hq) * D + i % D,
-                                0.f);
-            }
-        }
-        return;
-    }
-
-    constexpr int PPI = C::kPPI;
     uint8_t* ring = smem + warp * C::kWarpSmem;
     uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * C::kWarpSmem +
-                                                 kWarps * C::kStages * PPI * C::kScaleB) +
-                     warp * C::kStages;
-    int* abort_flag = reinterpret_cast<int*>(smem + kWarps * C::kWarpSmem +
-                                             kWarps * C::kStages * PPI * C::kScaleB +
-                                             kWarps * C::kStages * 8);
-    if (threadIdx.x == 0) *abort_flag = 0;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars) + warp * C::kStages;
+    int* seg = reinterpret_cast<int*>(smem + C::kOffSegs) + warp * kMaxSeg * kSegInts;
+    // segment record i: seg[9i + 0..8] = sequence b, KV head h, first page, end
+    // page, flags (2: starts the unit, 4: ends it), visible positions [lo, ctx),
+    // and the bits of the per-tensor / per-head K and V scales (1 otherwise)
+
+    // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
+    //      tiles; every warp is an independent worker (no block-wide barrier)
+    long long W = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int bb = b0 + lane;
+        long long w = 0;
+        if (bb < p.B) {
+            int lo_, ctx_, plo_, phi_;
+            visible(p, bb, lo_, ctx_, plo_, phi_, blockIdx.x == 0 && warp == 0);
+            w = phi_ > plo_ ? static_cast<long long>(phi_ - plo_) * p.Hkv : 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+        W += w;
+    }
+    const long long n_workers = W < static_cast<long long>(gridDim.x) * kWarps
+                                    ? W : static_cast<long long>(gridDim.x) * kWarps;
+    // worker id, recomputed where needed so it does not hold registers
+#define FP8KV_WORKER (static_cast<long long>(blockIdx.x) * kWarps + warp)
+    if (FP8KV_WORKER >= n_workers) return;
+    // [resume, end) of the share lives in shared memory (kept out of registers)
+    volatile long long* share = reinterpret_cast<volatile long long*>(smem + C::kOffShare) + 2 * warp;
+    if (lane == 0) {
+        share[0] = FP8KV_WORKER * W / n_workers;
+        share[1] = (FP8KV_WORKER + 1) * W / n_workers;
+    }
+    __syncwarp();
+
     if (lane == 0) {
         for (int s = 0; s < C::kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
         mbar_init_fence();
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
     }
-    __syncthreads();
+    __syncwarp();
 
-    // ---- query fragments (B operand of S^T = K Q^T): head g, elements d0..d0+3
-    const int hq_g = h * G + g;
+    // segments of [resume, t1), at most kMaxSeg per pass, into this warp's list.
+    // Lane j holds sequence b0 + j's visible range and tile offset; the sequences
+    // the share meets come in order from a ballot.
+    auto build_segments = [&]() -> int {
+        long long t = share[0];
+        const long long t1 = share[1];
+        int k = 0;
+        long long acc = 0;
+        for (int b0 = 0; b0 < p.B && t < t1 && k < kMaxSeg; b0 += 32) {
+            const int bb = b0 + lane;
+            int lo_ = 0, ctx_ = 0, plo_ = 0, phi_ = 0;
+            if (bb < p.B) visible(p, bb, lo_, ctx_, plo_, phi_, false);
+            const int n = phi_ > plo_ ? phi_ - plo_ : 0;
+            const long long w = static_cast<long long>(n) * p.Hkv;
+            long long incl = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const long long base = acc + incl - w;
+            acc += __shfl_sync(0xffffffffu, incl, 31);
+            unsigned hit = __ballot_sync(0xffffffffu, w > 0 && base + w > t && base < t1);
+            while (hit != 0u && t < t1 && k < kMaxSeg) {
+                const int src = __ffs(hit) - 1;
+                hit &= hit - 1u;
+                const long long sb = __shfl_sync(0xffffffffu, base, src);
+                const int sn = __shfl_sync(0xffffffffu, n, src);
+                const int slo = __shfl_sync(0xffffffffu, lo_, src);
+                const int sctx = __shfl_sync(0xffffffffu, ctx_, src);
+                const int splo = __shfl_sync(0xffffffffu, plo_, src);
+                while (t < t1 && t < sb + static_cast<long long>(sn) * p.Hkv && k < kMaxSeg) {
+                    // t - sb < pages * Hkv < 2^31 (checked on the host)
+                    const int hq = static_cast<int>(t - sb) / sn;
+                    const long long unit_base = sb + static_cast<long long>(hq) * sn;
+                    const long long seg_end = t1 < unit_base + sn ? t1 : unit_base + sn;
+                    if (lane == 0) {
+                        int* r = seg + kSegInts * k;
+                        r[0] = b0 + src;
+                        r[1] = hq;
+                        r[2] = splo + static_cast<int>(t - unit_base);
+                        r[3] = splo + static_cast<int>(seg_end - unit_base);
+                        r[4] = (t == unit_base ? 2 : 0) | (seg_end == unit_base + sn ? 4 : 0);
+                        r[5] = slo;
+                        r[6] = sctx;
+                        float ks = 1.f, vs = 1.f;
+                        if constexpr (!BF16 && !PER_TOKEN) {
+                            const int si = p.scale_mode == FP8KV_SCALE_PER_HEAD ? hq : 0;
+                            ks = p.k_scale[si];
+                            vs = p.v_scale[si];
+                        }
+                        r[7] = __float_as_int(ks);
+                        r[8] = __float_as_int(vs);
+                    }
+                    t = seg_end;
+                    ++k;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) share[0] = t;
+        __syncwarp();
+        return k;
+    };
+
     uint32_t qb[C::kKSteps][2];
+    float hs0 = 0.f, hs1 = 0.f;
+    // ---- query fragments (B operand of S^T = K Q^T): head g, elements d0..d0+3
+    auto load_q = [&](int b, int h, float kconst) {
+    const int hq_g = h * G + g;
     float qscale;                           // log2-domain logit multiplier of head g
     {
         const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(b) * p.Hq + hq_g) * D;
@@ -203,9 +302,6 @@ __global__ void __launch_bounds__(kWarps * 32)
             const int d0 = s * (64 / C::kElem) + c * (16 / C::kElem) + 4 * jj;
             raw[ks] = g < G ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
         }
-        float kconst = 1.f;
-        if constexpr (!BF16 && !PER_TOKEN)
-            kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
         if constexpr (BF16) {
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
@@ -242,89 +338,26 @@ __global__ void __launch_bounds__(kWarps * 32)
             qscale = p.scale_log2 * kconst / f;
         }
     }
-    // this lane's S^T / O^T columns are heads 2c and 2c+1
-    const float hs0 = __shfl_sync(0xffffffffu, qscale, (2 * c) * 4);
-    const float hs1 = __shfl_sync(0xffffffffu, qscale, (2 * c + 1) * 4);
-
-    // ---- work: groups of PPI consecutive pages; this warp takes groups
-    //      warp, warp + 4, ...; its j-th group starts at page pb + PPI*(warp + 4j)
-    const int n_groups = (pe - pb + PPI - 1) / PPI;
-    const int n_my = n_groups > warp ? (n_groups - warp + kWarps - 1) / kWarps : 0;
-    const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    constexpr int kGroupsPerBatch = 32 / PPI;
-    auto bt_load = [&](int batch) -> int {   // lane L: page L%PPI of group batch*GPB + L/PPI
-        const int grp = warp + (batch * kGroupsPerBatch + lane / PPI) * kWarps;
-        const int pg = pb + PPI * grp + lane % PPI;
-        return pg < pe ? bt_row[pg] : -1;
-    };
-    int bt_cur = 0, bt_next = 0;
-    uint32_t bad_mask = 0u;                 // bit st*PPI+k: page k of stage st is absent/invalid
-
-    auto issue = [&](int j) {               // called by all lanes of the warp
-        if ((j % kGroupsPerBatch) == 0) {
-            bt_cur = (j == 0) ? bt_load(0) : bt_next;
-            bt_next = bt_load(j / kGroupsPerBatch + 1);
-        }
-        const int st = j % C::kStages;
-        const int pg0 = pb + PPI * (warp + j * kWarps);
-        int blk[PPI];
-        bool here[PPI];
-        uint32_t tx = 0;
-#pragma unroll
-        for (int k = 0; k < PPI; ++k) {
-            blk[k] = __shfl_sync(0xffffffffu, bt_cur, (j % kGroupsPerBatch) * PPI + k);
-            here[k] = pg0 + k < pe;
-            const bool ok = here[k] && blk[k] >= 0 && static_cast<int64_t>(blk[k]) < p.num_blocks;
-            const uint32_t bit = 1u << (st * PPI + k);
-            bad_mask = ok ? (bad_mask & ~bit) : (bad_mask | bit);
-            if (here[k] && !ok) {
-                if (lane == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-                blk[k] = 0;                  // load an in-range page, masked later
-            }
-            if (here[k]) tx += 2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0);
-        }
-        if (lane == 0) {
-            const uint32_t bar = smem_addr(&bars[st]);
-            const uint32_t base = smem_addr(ring + st * C::kStageB);
-            fence_proxy_async();
-            mbar_arrive_expect_tx(bar, tx);
-#pragma unroll
-            for (int k = 0; k < PPI; ++k) {
-                if (!here[k]) continue;
-                const int z = blk[k] * p.Hkv + h;
-#pragma unroll
-                for (int box = 0; box < C::kBoxes; ++box) {
-                    tma_load_3d(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0, z, bar);
-                    tma_load_3d(base + (PPI + k) * C::kTileB + box * 2048, &vmap, box * 128, 0, z,
-                                bar);
-                }
-                if constexpr (PER_TOKEN) {
-                    const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
-                    bulk_load(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
-                    bulk_load(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64,
-                              bar);
-                }
-            }
-        }
+    hs0 = __shfl_sync(0xffffffffu, qscale, (2 * c) * 4);
+    hs1 = __shfl_sync(0xffffffffu, qscale, (2 * c + 1) * 4);
     };
 
-    // fp8 path: P = hi + lo with lo scaled by 2^11 into f16's normal range and
-    // accumulated separately (O = o + 2^-11 olo); bf16 P has no subnormal issue
-    constexpr int kLoTiles = BF16 ? 1 : C::kMTiles;
-    constexpr float kLoScale = 2048.f;
+    // The PV weights w = p * s_v enter the MMA as hi + lo halves (f16 for the
+    // e4m3 cache, bf16 for the bf16 cache).  e4m3 path: w is pre-scaled by 16
+    // and the lazy max keeps p <= 16, so hi stays below f16's max and lo is a
+    // normal f16 for every w >= 2^-7; both accumulate into the same fp32 O
+    // (divided by 16 at the end, exactly).
+    constexpr float kWScale = BF16 ? 1.f : 16.f;
+    constexpr float kLazy = BF16 ? 8.f : 4.f;          // log2 headroom of the lazy max
     float o[C::kMTiles][4];
-    float olo[kLoTiles][4];
+    float m0, m1, l0, l1;
+    auto reset_state = [&]() {
 #pragma unroll
-    for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < kLoTiles; ++i) olo[i][0] = olo[i][1] = olo[i][2] = olo[i][3] = 0.f;
-    // running max starts finite so that a fully masked group gives ex2(-inf) = 0
-    float m0 = kMaxInit, m1 = kMaxInit, l0 = 0.f, l1 = 0.f;
-    bool timed_out = false;
-    int drain_from = 0;
-
-    const int pre = n_my < C::kStages ? n_my : C::kStages;
-    for (int j = 0; j < pre; ++j) issue(j);
+        for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        // running max starts finite so that a fully masked group gives ex2(-inf) = 0
+        m0 = m1 = kMaxInit;
+        l0 = l1 = 0.f;
+    };
 
     // per-thread shared-memory offsets inside a page tile (fixed for the kernel)
     const int tA = perm8(g), tB = tA + 8;
@@ -347,17 +380,178 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
     }
 
-    for (int j = 0; j < n_my; ++j) {
-        const int st = j % C::kStages;
-        const bool arrived =
-            mbar_wait_bounded(smem_addr(&bars[st]), static_cast<uint32_t>((j / C::kStages) & 1));
-        if (!__all_sync(0xffffffffu, arrived)) {   // leave together
-            timed_out = true;
-            drain_from = j;
-            break;
+
+    // Finish the segment in `si`: a whole unit writes `out`; otherwise the warp's
+    // (m, l, unnormalised O) goes to workspace slot worker + unit.
+    auto finish_segment = [&](int si) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
+        const int ub = seg[kSegInts * si + 0], uh = seg[kSegInts * si + 1];
+        const int flags = seg[kSegInts * si + 4];
+        const bool whole = flags == 6;           // starts and ends the unit
+        const float vconst = __int_as_float(seg[kSegInts * si + 8]) / kWScale;
+        const int head0 = 2 * c, head1 = 2 * c + 1;
+        const int dbase = perm8(g) * (D / 8);
+        const size_t unit = static_cast<size_t>(ub) * p.Hkv + uh;
+        const size_t slot = static_cast<size_t>(FP8KV_WORKER) + unit;
+        const float f0 = whole ? (l0 > 0.f ? vconst / l0 : 0.f) : vconst;
+        const float f1 = whole ? (l1 > 0.f ? vconst / l1 : 0.f) : vconst;
+#pragma unroll
+        for (int i = 0; i < C::kMTiles; ++i) {
+            const int d = dbase + 2 * i;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int head = hh ? head1 : head0;
+                if (head >= G) continue;
+                const float f = hh ? f1 : f0;
+                const float va = o[i][hh] * f, vb = o[i][2 + hh] * f;
+                if (whole) {
+                    const size_t row = static_cast<size_t>(ub) * p.Hq + uh * G + head;
+                    store_out<BF16>(p.out, p.out_bf16, row * D + d, va);
+                    store_out<BF16>(p.out, p.out_bf16, row * D + d + 1, vb);
+                } else {
+                    float* dst = p.ws_o + (slot * G + head) * D + d;
+                    *reinterpret_cast<float2*>(dst) = make_float2(va, vb);
+                }
+            }
+        }
+        // the workers that start and end the unit, for split_merge (a whole unit
+        // records first == last, so the merge leaves its output alone)
+        if (lane == 0) {
+            if (flags & 2) p.ws_first[unit] = static_cast<int>(FP8KV_WORKER);
+            if (flags & 4) p.ws_last[unit] = static_cast<int>(FP8KV_WORKER);
+        }
+        if (whole) return;
+        if (g == 0) {
+            if (head0 < G) {
+                p.ws_m[slot * G + head0] = m0;
+                p.ws_l[slot * G + head0] = l0;
+            }
+            if (head1 < G) {
+                p.ws_m[slot * G + head1] = m1;
+                p.ws_l[slot * G + head1] = l1;
+            }
+        }
+    };
+
+    // ---- the warp's page stream: issue side runs kStages groups ahead of the
+    //      consume side; both walk the same segments in order
+    int jring = 0;                          // groups consumed so far (ring phase)
+    bool timed_out = false;
+    while (share[0] < share[1] && !timed_out) {
+        const int nseg = build_segments();
+        // issue cursor: segment is_ (its end page, KV head and page-table row
+        // cached in registers), next page ipg; block ids of pages
+        // [bt_base, bt_base + 32) in bt_cur, the next 32 in bt_next
+        int is_ = 0, ipg = seg[2], ipe = seg[3], ih = seg[1];
+        const int32_t* ibt = p.block_table + static_cast<size_t>(seg[0]) * p.max_blocks_per_seq;
+        int bt_base = ipg, bt_cur = 0, bt_next = 0;
+        auto bt_fetch = [&](int base) -> int {
+            const int pg = base + lane;
+            return pg < ipe ? ibt[pg] : -1;
+        };
+        // block ids of the first pages of segment si (a segment switch on the issue
+        // side then needs no load it waits for)
+        auto seg_fetch = [&](int si) -> int {
+            const int pg = seg[kSegInts * si + 2] + lane;
+            return pg < seg[kSegInts * si + 3]
+                       ? p.block_table[static_cast<size_t>(seg[kSegInts * si]) * p.max_blocks_per_seq + pg]
+                       : -1;
+        };
+        bt_cur = bt_fetch(bt_base);
+        bt_next = bt_fetch(bt_base + 32);
+        int bt_nseg = nseg > 1 ? seg_fetch(1) : -1;
+        uint32_t bad_mask = 0u;
+        int issued = 0;
+        auto issue_next = [&]() {           // called by all lanes of the warp
+            if (ipg >= ipe) {               // next segment
+                ++is_;
+                ipg = seg[kSegInts * is_ + 2];
+                ipe = seg[kSegInts * is_ + 3];
+                ih = seg[kSegInts * is_ + 1];
+                ibt = p.block_table + static_cast<size_t>(seg[kSegInts * is_]) * p.max_blocks_per_seq;
+                bt_base = ipg;
+                bt_cur = bt_nseg;
+                bt_next = bt_fetch(bt_base + 32);
+                bt_nseg = is_ + 1 < nseg ? seg_fetch(is_ + 1) : -1;
+            } else if (ipg >= bt_base + 32) {
+                bt_base += 32;
+                bt_cur = bt_next;
+                bt_next = bt_fetch(bt_base + 32);
+            }
+            const int pe_i = ipe;
+            const int h_i = ih;
+            const int st = (jring + issued) % C::kStages;
+            int blk[PPI];
+            bool here[PPI];
+            uint32_t tx = 0;
+#pragma unroll
+            for (int k = 0; k < PPI; ++k) {
+                blk[k] = __shfl_sync(0xffffffffu, bt_cur, (ipg - bt_base + k) & 31);
+                here[k] = ipg + k < pe_i;
+                const bool ok = here[k] && blk[k] >= 0 && static_cast<int64_t>(blk[k]) < p.num_blocks;
+                const uint32_t bit = 1u << (st * PPI + k);
+                bad_mask = ok ? (bad_mask & ~bit) : (bad_mask | bit);
+                if (here[k] && !ok) {
+                    if (lane == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+                    blk[k] = 0;              // load an in-range page, masked later
+                }
+                if (here[k]) tx += 2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0);
+            }
+            if (lane == 0) {
+                const uint32_t bar = smem_addr(&bars[st]);
+                const uint32_t base = smem_addr(ring + st * C::kStageB);
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+                for (int k = 0; k < PPI; ++k) {
+                    if (!here[k]) continue;
+                    const int z = blk[k] * p.Hkv + h_i;
+#pragma unroll
+                    for (int box = 0; box < C::kBoxes; ++box) {
+                        tma_load_3d(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0, z, bar);
+                        tma_load_3d(base + (PPI + k) * C::kTileB + box * 2048, &vmap, box * 128, 0,
+                                    z, bar);
+                    }
+                    if constexpr (PER_TOKEN) {
+                        const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
+                        bulk_load(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
+                        bulk_load(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                                  bar);
+                    }
+                }
+            }
+            ipg += PPI;
+            ++issued;
+        };
+        // groups in this pass
+        int total_groups = 0;
+        for (int si = 0; si < nseg; ++si)
+            total_groups += (seg[kSegInts * si + 3] - seg[kSegInts * si + 2] + PPI - 1) / PPI;
+        const int pre = total_groups < C::kStages ? total_groups : C::kStages;
+        for (int q = 0; q < pre; ++q) issue_next();
+
+        int consumed = 0;
+        for (int si = 0; si < nseg && !timed_out; ++si) {
+            const int b = seg[kSegInts * si + 0];
+            const int pb = seg[kSegInts * si + 2], pe = seg[kSegInts * si + 3];
+            const int lo = seg[kSegInts * si + 5], ctx = seg[kSegInts * si + 6];
+            load_q(b, seg[kSegInts * si + 1], __int_as_float(seg[kSegInts * si + 7]));
+            reset_state();
+            for (int cpg = pb; cpg < pe; cpg += PPI) {
+                const int j = jring + consumed;
+                const int st = j % C::kStages;
+                const bool arrived = mbar_wait_bounded(smem_addr(&bars[st]),
+                                                       static_cast<uint32_t>((j / C::kStages) & 1));
+                if (!__all_sync(0xffffffffu, arrived)) {   // leave together
+                    timed_out = true;
+                    break;
+                }
         const uint8_t* stage = ring + st * C::kStageB;
-        const int pos0 = (pb + PPI * (warp + j * kWarps)) * kPage;
+        const int pos0 = cpg * kPage;
 
         bool bad[PPI], interior[PPI];
 #pragma unroll
@@ -429,8 +623,8 @@ __global__ void __launch_bounds__(kWarps * 32)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        // lazy running max: move it only when the group exceeds it by 2^8
-        if (mx0 > m0 + 8.f) {
+        // lazy running max: move it only when the group exceeds it by 2^kLazy
+        if (mx0 > m0 + kLazy) {
             const float a = ex2(m0 - mx0);
             l0 *= a;
 #pragma unroll
@@ -438,29 +632,15 @@ __global__ void __launch_bounds__(kWarps * 32)
                 o[i][0] *= a;
                 o[i][2] *= a;
             }
-            if constexpr (!BF16) {
-#pragma unroll
-                for (int i = 0; i < kLoTiles; ++i) {
-                    olo[i][0] *= a;
-                    olo[i][2] *= a;
-                }
-            }
             m0 = mx0;
         }
-        if (mx1 > m1 + 8.f) {
+        if (mx1 > m1 + kLazy) {
             const float a = ex2(m1 - mx1);
             l1 *= a;
 #pragma unroll
             for (int i = 0; i < C::kMTiles; ++i) {
                 o[i][1] *= a;
                 o[i][3] *= a;
-            }
-            if constexpr (!BF16) {
-#pragma unroll
-                for (int i = 0; i < kLoTiles; ++i) {
-                    olo[i][1] *= a;
-                    olo[i][3] *= a;
-                }
             }
             m1 = mx1;
         }
@@ -472,8 +652,11 @@ __global__ void __launch_bounds__(kWarps * 32)
             const float p2 = ex2(z[k][2] - m0), p3 = ex2(z[k][3] - m1);
             l0 += p0 + p2;
             l1 += p1 + p3;
-            const float w0 = p0 * vs[k][0], w1 = p1 * vs[k][0];
-            const float w2 = p2 * vs[k][1], w3 = p3 * vs[k][1];
+            // (clamped: only a per-token V scale above ~256 could reach f16's max)
+            const float w0 = fminf(p0 * vs[k][0] * kWScale, 65504.f);
+            const float w1 = fminf(p1 * vs[k][0] * kWScale, 65504.f);
+            const float w2 = fminf(p2 * vs[k][1] * kWScale, 65504.f);
+            const float w3 = fminf(p3 * vs[k][1] * kWScale, 65504.f);
 
             // ---- P^T as the B operand: hi + lo halves, transposed by movmatrix
             uint32_t bh0, bh1, bl0, bl1;
@@ -489,8 +672,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                 const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
                 bh0 = movmatrix_trans(hA);
                 bh1 = movmatrix_trans(hB);
-                bl0 = movmatrix_trans(pack_f16x2((w0 - fA.x) * kLoScale, (w1 - fA.y) * kLoScale));
-                bl1 = movmatrix_trans(pack_f16x2((w2 - fB.x) * kLoScale, (w3 - fB.y) * kLoScale));
+                bl0 = movmatrix_trans(pack_f16x2(w0 - fA.x, w1 - fA.y));
+                bl1 = movmatrix_trans(pack_f16x2(w2 - fB.x, w3 - fB.y));
             }
 
             // ---- V rows of tokens c, c+4, c+8, c+12 (k-slots 2c, 2c+1, 2c+8, 2c+9)
@@ -544,134 +727,106 @@ __global__ void __launch_bounds__(kWarps * 32)
                     f16x2x2_from_e4m3x4(x01, a0, a1);
                     f16x2x2_from_e4m3x4(x23, a2, a3);
                     mma_f16(o[i], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16(olo[i < kLoTiles ? i : 0], a0, a1, a2, a3, bl0, bl1);
+                    mma_f16(o[i], a0, a1, a2, a3, bl0, bl1);
                 }
             }
         }
 
         __syncwarp();
-        if (j + C::kStages < n_my) issue(j + C::kStages);
-    }
-
-    if (timed_out) {
-        if (lane == 0) report(p.err, FP8KV_ERR_TIMEOUT);
-        // let this warp's copies still in flight land (each wait bounded) before
-        // the CTA leaves; the output of this split is not written
-        const int last = min(drain_from + C::kStages, n_my);
-        for (int j = drain_from; j < last; ++j)
-            (void)mbar_wait_bounded(smem_addr(&bars[j % C::kStages]),
-                                    static_cast<uint32_t>((j / C::kStages) & 1));
-        if (lane == 0) *abort_flag = 1;
-    }
-
-    // ---- per-warp softmax denominators: sum the 8 lane groups
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-
-    // ---- combine the 4 warps in shared memory (the rings are free now)
-    __syncthreads();
-    if (*abort_flag) return;
-    float* mw = reinterpret_cast<float*>(smem);              // [warp][8]
-    float* lw = mw + kWarps * 8;                            // [warp][8]
-    float* ow = lw + kWarps * 8;                            // [warp][8][D]
-    if (g == 0) {
-        mw[warp * 8 + 2 * c] = m0;
-        mw[warp * 8 + 2 * c + 1] = m1;
-        lw[warp * 8 + 2 * c] = l0;
-        lw[warp * 8 + 2 * c + 1] = l1;
-    }
-    {
-        const int dbase = perm8(g) * (D / 8);
-        float* o0 = ow + (warp * 8 + 2 * c) * D;
-        float* o1 = ow + (warp * 8 + 2 * c + 1) * D;
-        if constexpr (!BF16) {
-#pragma unroll
-            for (int i = 0; i < C::kMTiles; ++i)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) o[i][r] += olo[i < kLoTiles ? i : 0][r] * (1.f / kLoScale);
-        }
-#pragma unroll
-        for (int i = 0; i < C::kMTiles; ++i) {
-            const int d = dbase + 2 * i;
-            o0[d] = o[i][0];
-            o1[d] = o[i][1];
-            o0[d + 1] = o[i][2];
-            o1[d + 1] = o[i][3];
-        }
-    }
-    __syncthreads();
-
-    float vconst = 1.f;
-    if constexpr (!BF16 && !PER_TOKEN)
-        vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int head = i / D, d = i % D;
-        float M = neg_inf();
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 8 + head]);
-        float L = 0.f, O = 0.f;
-        if (M != neg_inf()) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float a = ex2(mw[w * 8 + head] - M);
-                L += a * lw[w * 8 + head];
-                O += a * ow[(w * 8 + head) * D + d];
+                ++consumed;
+                if (issued < total_groups) issue_next();
             }
+            if (!timed_out) finish_segment(si);
         }
-        O *= vconst;
-        const int hq = h * G + head;
-        const size_t row = static_cast<size_t>(b) * p.Hq + hq;
-        if (p.num_splits == 1) {
-            store_out<BF16>(p.out, p.out_bf16, row * D + d, L > 0.f ? O / L : 0.f);
-        } else {
-            const size_t ws = row * p.num_splits + split;
-            p.ws_o[ws * D + d] = O;
-            if (d == 0) {
-                p.ws_m[ws] = M;
-                p.ws_l[ws] = L;
-            }
+        if (timed_out) {
+            if (lane == 0) report(p.err, FP8KV_ERR_TIMEOUT);
+            // let this warp's copies still in flight land (each wait bounded)
+            for (int j = consumed; j < issued; ++j)
+                (void)mbar_wait_bounded(smem_addr(&bars[(jring + j) % C::kStages]),
+                                        static_cast<uint32_t>(((jring + j) / C::kStages) & 1));
         }
+        jring += consumed;
     }
+#undef FP8KV_WORKER
 }
 
-// split_merge: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over the splits
-// that hold visible pages of the sequence.
+// split_merge, one block per query head (b, hq) of unit (b, h = hq / G): the
+// workers (warps) whose shares touched a unit left partials (m, l, O) in slots
+// worker + unit and recorded the first and last of them; combine them as
+// O = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w.  A unit one worker covered
+// whole was written by that worker; an empty unit gets a zero row.  The block's
+// warps (4 to 16, sized by the launch to the parts per unit) take the parts
+// round-robin, each lane D/32 columns, all loads of a chunk of parts in flight
+// together, and meet in shared memory ([warps][D + 2] floats, dynamic).
 template <int D>
-__global__ void __launch_bounds__(128) split_merge_kernel(const DecodeParams p) {
-    __shared__ float wgt[1024];
-    __shared__ float inv_l;
+__global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) {
+    constexpr int kCols = D / 32;
+    extern __shared__ float merge_smem[];
+    const int nw = blockDim.x >> 5;
+    float* sm_o = merge_smem;                   // [nw][D]
+    float* sm_m = sm_o + nw * D;                // [nw]
+    float* sm_l = sm_m + nw;                    // [nw]
     const int row = blockIdx.x;                 // b * Hq + hq
-    const int b = row / p.Hq;
-    int lo, ctx, p_lo, p_hi;
-    visible(p, b, lo, ctx, p_lo, p_hi, false);
-    const int n_vis = p_hi > p_lo ? p_hi - p_lo : 0;
-    int n_valid = (n_vis + p.pages_per_split - 1) / p.pages_per_split;
-    if (n_valid > p.num_splits) n_valid = p.num_splits;
-    if (n_valid > 1024) n_valid = 1024;
-    const float* m = p.ws_m + static_cast<size_t>(row) * p.num_splits;
-    const float* l = p.ws_l + static_cast<size_t>(row) * p.num_splits;
-    if (threadIdx.x < 32) {
-        float M = neg_inf();
-        for (int s = threadIdx.x; s < n_valid; s += 32) M = fmaxf(M, m[s]);
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        for (int s = threadIdx.x; s < n_valid; s += 32) {
-            const float a = (M == neg_inf()) ? 0.f : ex2(m[s] - M);
-            wgt[s] = a;
-            L += a * l[s];
-        }
-        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        if (threadIdx.x == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
+    const int b = row / p.Hq, hq = row % p.Hq;
+    const int G = p.G, h = hq / G, head = hq % G;
+    const int unit = b * p.Hkv + h;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();                                 // the decode kernel's partials are visible
+    if (vis_pages(p, b) == 0) {
+        for (int d = threadIdx.x; d < D; d += blockDim.x)
+            store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, 0.f);
+        return;
     }
+    // the unit's workers, recorded by them in this call (first == last: one
+    // worker covered the unit whole and wrote the output itself)
+    const int first = p.ws_first[unit], last = p.ws_last[unit];
+    const long long workers = static_cast<long long>(p.num_splits) * kWarps;
+    if (last <= first || first < 0 || last >= workers) return;
+    float M = neg_inf(), L = 0.f, acc[kCols];
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
+    constexpr int kChunk = 8;
+    for (int w0 = first + warp; w0 <= last; w0 += nw * kChunk) {
+        float mi[kChunk], li[kChunk], oi[kChunk][kCols];
+#pragma unroll
+        for (int q = 0; q < kChunk; ++q) {
+            const int w = w0 + nw * q;
+            const bool ok = w <= last;
+            const size_t sl = (static_cast<size_t>(ok ? w : first) + unit) * G + head;
+            mi[q] = ok ? p.ws_m[sl] : neg_inf();
+            li[q] = ok ? p.ws_l[sl] : 0.f;
+#pragma unroll
+            for (int k = 0; k < kCols; ++k) oi[q][k] = ok ? p.ws_o[sl * D + lane + 32 * k] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kChunk; ++q) {
+            const float Mn = fmaxf(M, mi[q]);
+            const float a = (M == neg_inf()) ? 0.f : ex2(M - Mn);
+            const float bi = (mi[q] == neg_inf()) ? 0.f : ex2(mi[q] - Mn);
+            L = L * a + li[q] * bi;
+#pragma unroll
+            for (int k = 0; k < kCols; ++k) acc[k] = acc[k] * a + oi[q][k] * bi;
+            M = Mn;
+        }
+    }
+    if (lane == 0) {
+        sm_m[warp] = M;
+        sm_l[warp] = L;
+    }
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) sm_o[warp * D + lane + 32 * k] = acc[k];
     __syncthreads();
-    const float* o = p.ws_o + static_cast<size_t>(row) * p.num_splits * D;
+    float Mt = neg_inf();
+    for (int w = 0; w < nw; ++w) Mt = fmaxf(Mt, sm_m[w]);
+    float Lt = 0.f;
+    for (int w = 0; w < nw; ++w)
+        if (sm_m[w] != neg_inf()) Lt += ex2(sm_m[w] - Mt) * sm_l[w];
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < n_valid; ++s) acc += wgt[s] * o[static_cast<size_t>(s) * D + d];
-        store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, acc * inv_l);
+        float o = 0.f;
+        for (int w = 0; w < nw; ++w)
+            if (sm_m[w] != neg_inf()) o += ex2(sm_m[w] - Mt) * sm_o[w * D + d];
+        store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, o * inv);
     }
 }
 
@@ -690,12 +845,30 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    dim3 grid(p.num_splits, p.Hkv, p.B);
-    kern<<<grid, kWarps * 32, C::kSmem, stream>>>(kmap, vmap, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || p.num_splits == 1) return e;
-    split_merge_kernel<D><<<p.B * p.Hq, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    // both kernels may start before their predecessor in the stream ends (they
+    // wait for its results in-kernel): launch latency and set-up overlap
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_splits);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
+    if (e != cudaSuccess) return e;
+    // merge block: about 4 parts per warp at the launch's mean parts per unit
+    const long long units = static_cast<long long>(p.B) * p.Hkv;
+    const long long mean_parts = (static_cast<long long>(p.num_splits) * kWarps + units - 1) / units + 1;
+    long long mw = (mean_parts + 3) / 4;
+    mw = mw < 4 ? 4 : (mw > 16 ? 16 : mw);
+    cudaLaunchConfig_t mcfg = cfg;
+    mcfg.gridDim = dim3(p.B * p.Hq);
+    mcfg.blockDim = dim3(static_cast<unsigned>(32 * mw));
+    mcfg.dynamicSmemBytes = static_cast<size_t>(mw) * (D + 2) * sizeof(float);
+    return cudaLaunchKernelEx(&mcfg, split_merge_kernel<D>, p);
 }
 
 template <int D>

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/fp8kv.h"
+
 namespace fp8kv {
 
 struct WriteParams {
@@ -30,9 +32,9 @@ cudaError_t launch_kv_cache_write(const WriteParams& p, int D, int kv_dtype, int
 cudaError_t launch_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
                                  cudaStream_t stream, int num_sms);
 
-// Split-K decode.  Split s of (seq b, KV head h) covers visible pages
-// [p_lo + s*pages_per_split, min(p_lo + (s+1)*pages_per_split, p_hi)) where
-// p_lo/p_hi bound the pages holding positions [lo, ctx).
+// Split-K decode over a balanced partition: the (seq, KV head, page) tiles of
+// the launch (pages [p_lo, p_hi) hold positions [lo, ctx)) are split evenly over
+// num_splits CTAs; a CTA's share may span several (seq, KV head) units.
 struct DecodeParams {
     const __nv_bfloat16* q;
     const float* k_scale;        // per tensor / per head (fp8 only)
@@ -46,18 +48,19 @@ struct DecodeParams {
     int64_t num_blocks;
     float scale_log2;            // softmax_scale * log2(e)
     int window;
-    int num_splits;
-    int pages_per_split;
-    float* ws_m;                 // [B*Hq][num_splits] running max (log2 units)
-    float* ws_l;                 // [B*Hq][num_splits] softmax denominator
-    float* ws_o;                 // [B*Hq][num_splits][D] unnormalised output
+    int num_splits;              // CTAs of the decode grid
+    float* ws_m;                 // [4*num_splits + B*Hkv][G] running max (log2 units)
+    float* ws_l;                 // [4*num_splits + B*Hkv][G] softmax denominator
+    float* ws_o;                 // [4*num_splits + B*Hkv][G][D] unnormalised output
+    int* ws_first;               // [B*Hkv] first worker of a split unit
+    int* ws_last;                // [B*Hkv] last worker of a split unit
     void* out;                   // [B][Hq][D]
     int out_bf16;
     int scale_mode;
     int32_t* err;
 };
 
-// Launches the split kernel and (when num_splits > 1) the merge kernel.
+// Launches the split kernel and the merge kernel.
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, int D, int kv_dtype,
                                 cudaStream_t stream);

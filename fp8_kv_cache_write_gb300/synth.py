@@ -258,10 +258,10 @@ def prefill(seed=1005, device="cpu", ctx=(32768,), chunk=(4096,), Hq=8, Hkv=1,
 
 
 def decode_workload(seed, context_lens, Hq, Hkv, D, scale_mode, outlier_frac=0.0,
-                    spare_blocks=0, window=0, name="custom") -> DecodeWorkload:
+                    spare_blocks=0, window=0, name="custom", device="cpu") -> DecodeWorkload:
     """A decode step with explicit context lengths (parity tests' ragged cases).
     Per-tensor / per-head scales default to 1.0 / a per-head calibration."""
-    w = _decode_common(name, seed, context_lens, Hq, Hkv, D, scale_mode,
+    w = _decode_common(name, seed, context_lens, Hq, Hkv, D, scale_mode, device,
                        outlier_frac=outlier_frac, spare_blocks=spare_blocks)
     w.window = window
     if scale_mode == 1:

@@ -107,7 +107,7 @@ int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mappi
  *   window              0 = full attention, else the last `window` keys
  *   num_splits          0 = choose automatically, else the requested split count
  *   *num_splits_out     the split count the kernel will use
- *   *workspace_bytes_out  bytes of fp32 workspace needed (0 when one split)
+ *   *workspace_bytes_out  bytes of workspace needed (split partials)
  */
 int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int window,
                       int num_splits, int* num_splits_out, size_t* workspace_bytes_out);
@@ -131,8 +131,9 @@ int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int
  *   softmax_scale  logits are softmax_scale * q . k (usually 1/sqrt(D)).
  *   window         0 = all keys; w > 0 = keys at positions >= ctx - w.
  *   num_splits     0 = automatic (see fp8kv_decode_plan).
- *   workspace      fp32 scratch of at least the planned bytes (may be NULL when
- *                  the plan needs none); its contents need no initialisation.
+ *   workspace      scratch of at least the planned bytes, 16-byte aligned; its
+ *                  contents need no initialisation.  Calls that share one
+ *                  workspace must not overlap on the GPU.
  *   out            [B][Hq][D] fp32 or bf16 (out_dtype).
  * Output: softmax(z) V over the visible keys, accumulated in fp32.
  */

@@ -28,6 +28,14 @@ def test_header_declares_the_exports():
     assert _declared_functions() == sorted(fk.EXPORTS)
 
 
+def test_binding_constants_match_the_header():
+    text = open(os.path.join(os.path.dirname(__file__), "..", "include", "fp8kv.h")).read()
+    def define(name):
+        m = re.search(r"#define\s+" + name + r"\s+\((\d+)u << (\d+)\)", text)
+        return int(m.group(1)) << int(m.group(2))
+    assert define("FP8KV_NOALLOC_DECODE_SCRATCH_BYTES") == fk.NOALLOC_DECODE_SCRATCH_BYTES
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
@@ -41,17 +49,23 @@ def test_status_strings(lib):
 
 
 def test_decode_plan_is_consistent(lib):
+    # num_splits = CTAs of the balanced partition (4 worker warps each); one
+    # workspace slot of G query heads x (D + 2) floats per warp plus one per unit,
+    # then the first / last worker of every unit
     for B, Hq, Hkv, D, mbs, win in [(8, 32, 8, 128, 1375, 0), (1, 64, 8, 128, 8192, 0),
                                     (32, 64, 8, 64, 2048, 128), (1, 32, 8, 128, 64, 0)]:
         s, ws = fk.decode_plan(B, Hq, Hkv, D, mbs, win)
         assert 1 <= s <= 1024
-        assert ws == (0 if s == 1 else B * Hq * s * (D + 2) * 4)
+        assert ws == (4 * s + B * Hkv) * (Hq // Hkv) * (D + 2) * 4 + B * Hkv * 8
         for req in (1, 2, 7):
             s2, _ = fk.decode_plan(B, Hq, Hkv, D, mbs, win, req)
-            assert 1 <= s2 <= req
-    # a window bounds the visible pages: 128 keys touch at most 9 pages
+            assert 1 <= s2 <= min(1024, req * B * Hkv)
+    # a window bounds the visible pages: 128 keys touch at most 9 pages per unit
     s, _ = fk.decode_plan(1, 8, 8, 64, 4096, 128, 1000)
-    assert s <= 9
+    assert s <= 9 * 8
+    # small work: at least 16 tiles per CTA
+    s, _ = fk.decode_plan(1, 32, 8, 128, 64, 0)
+    assert s <= (8 * 64 + 15) // 16
 
 
 def _null():

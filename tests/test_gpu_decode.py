@@ -201,3 +201,48 @@ def test_unwritten_slots_holding_nan_do_not_leak(kv_dtype, mode):
     b = gpu_decode(w, dirty).cpu()
     assert torch.isfinite(b).all()
     assert torch.equal(a, b)
+
+
+
+def test_graph_replays_match_eager_calls():
+    # The decode (split kernel + split_merge, both programmatically serialized)
+    # captured in a CUDA graph and replayed with new queries gives the bits of an
+    # eager call on its own workspace, and agrees with the oracle.
+    w = synth.decode_workload(15, [3000, 5000, 1, 0, 7000], 32, 8, 128, 2)
+    gc = gpu_fill(w, 0)
+    oc = oracle_cache(w, 0)
+    mbs = w.block_table.shape[1]
+    _, need = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0)
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt, cl = w.block_table.cuda(), w.context_lens.cuda()
+    qbuf = w.q.cuda().clone()
+    out = torch.empty(w.B, w.Hq, w.D, device="cuda")
+
+    def call():
+        fk.paged_decode_attn(qbuf, gc["k"], gc["v"], bt, cl, kv_dtype=0, scale_mode=2,
+                             k_scale_cache=gc["ks"], v_scale_cache=gc["vs"], workspace=ws,
+                             out=out, err_flag=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = oracle_decode(w, oc)
+    assert float(np.abs(out.cpu().numpy().reshape(-1, w.D) - ref).max()) <= DECODE_TOL
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        call()
+    g = torch.Generator().manual_seed(16)
+    for _ in range(3):
+        qbuf.copy_(torch.randn(w.B, w.Hq, w.D, generator=g).to(torch.bfloat16).cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        fresh = fk.paged_decode_attn(qbuf, gc["k"], gc["v"], bt, cl, kv_dtype=0, scale_mode=2,
+                                     k_scale_cache=gc["ks"], v_scale_cache=gc["vs"])
+        torch.cuda.synchronize()
+        assert torch.equal(got, fresh)
+        assert int(err.item()) == 0

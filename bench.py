@@ -508,8 +508,10 @@ def run_extras(args, dev):
     emit = lambda d: print(json.dumps(d), flush=True)
     E4, BF = fk.KV_E4M3, fk.KV_BF16
 
+    want = lambda name: args.extras in ("all", name)
+
     # (1) inter-token latency against context: B=8, 32/8 heads, D=128, decode only
-    for ctx in (2048, 4096, 8192, 16384, 32768):
+    for ctx in (2048, 4096, 8192, 16384, 32768) if want("itl") else ():
         w = synth.decode_workload(2000 + ctx, [ctx] * 8, 32, 8, 128, 2, device=dev)
         row = {"extra": "itl_vs_context", "B": 8, "context": ctx}
         for kv, name in ((E4, "fp8"), (BF, "bf16")):
@@ -525,7 +527,20 @@ def run_extras(args, dev):
         emit(row)
         del w
 
-    # (2) 131072-token needle: B=1, 64/8 heads, per-KV-head scales
+    # (2)-(5) the 131072-token needle, the hybrid model, prefill, the bulk write
+    if want("needle"):
+        _extra_needle(fk, synth, dev, stream, emit)
+    if want("hybrid"):
+        _extra_hybrid(fk, synth, dev, stream, emit)
+    if want("prefill"):
+        _extra_prefill(fk, synth, dev, stream, emit)
+    if want("write"):
+        _extra_write(fk, dev, stream, emit)
+
+
+def _extra_needle(fk, synth, dev, stream, emit):
+    # 131072-token needle: B=1, 64/8 heads, per-KV-head scales
+    E4, BF = fk.KV_E4M3, fk.KV_BF16
     w = synth.needle(device=dev)
     row = {"extra": "needle_131k", "B": 1, "context": 131072}
     for kv, name in ((E4, "fp8"), (BF, "bf16")):
@@ -538,11 +553,13 @@ def run_extras(args, dev):
         torch.cuda.empty_cache()
     row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
     emit(row)
-    del w
 
-    # (3) hybrid model, 24 layers alternating sliding-window-128 / full attention:
+
+def _extra_hybrid(fk, synth, dev, stream, emit):
+    # hybrid model, 24 layers alternating sliding-window-128 / full attention:
     #     one step = the decode of all 24 layers (each layer type rotates over
     #     its own cache copies); tokens/s = B / step time
+    E4, BF = fk.KV_E4M3, fk.KV_BF16
     wl = {0: synth.hybrid_layer(layer=0, device=dev), 1: synth.hybrid_layer(layer=1, device=dev)}
     for variant, dtypes in (("all_bf16", (BF, BF)), ("all_fp8", (E4, E4)),
                             ("window_bf16_full_fp8", (BF, E4))):
@@ -564,9 +581,11 @@ def run_extras(args, dev):
               "window_layer_us": per_type[0], "full_layer_us": per_type[1]})
         del calls
         torch.cuda.empty_cache()
-    del wl
 
-    # (4) chunked prefill: 4096 new queries over 32768 cached tokens, 8/1 heads, D=256
+
+def _extra_prefill(fk, synth, dev, stream, emit):
+    # chunked prefill: 4096 new queries over 32768 cached tokens, 8/1 heads, D=256
+    E4, BF = fk.KV_E4M3, fk.KV_BF16
     w = synth.prefill(device=dev)
     q, cu = w.q.to(dev), w.cu_seqlens_q.to(dev)
     bt, cl = w.block_table.to(dev), w.context_lens.to(dev)
@@ -590,9 +609,11 @@ def run_extras(args, dev):
                   "ms": ms, "tflops": flops / ms / 1e9})
         del kc, vc
         torch.cuda.empty_cache()
-    del w
 
-    # (5) bulk cache write: 32768 tokens x 8 KV heads x 128, per-token-head e4m3
+
+def _extra_write(fk, dev, stream, emit):
+    # bulk cache write: 32768 tokens x 8 KV heads x 128, per-token-head e4m3
+    E4 = fk.KV_E4M3
     T, H, D = 32768, 8, 128
     gen = torch.Generator(device=dev).manual_seed(6)
     sets = []
@@ -628,9 +649,11 @@ def main():
     ap.add_argument("--rotations", type=int, default=ROTATIONS,
                     help="cache copies rotated between steps (each larger than L2)")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planner)")
-    ap.add_argument("--extras", action="store_true",
+    ap.add_argument("--extras", nargs="?", const="all", default=None,
+                    choices=["all", "itl", "needle", "hybrid", "prefill", "write"],
                     help="time the other workloads (context sweep, needle, hybrid, prefill, "
-                         "bulk write) instead of the headline step; one JSON line each")
+                         "bulk write; all by default) instead of the headline step; one JSON "
+                         "line each")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

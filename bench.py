@@ -312,24 +312,21 @@ def run_ours(args, dev, w, world, rank):
         if name == "fp8" and not args.no_e2e:
             # end to end through the public API: every step copies its inputs from
             # pinned host memory and reads the output back (captured as graph nodes)
-            hq = w.q.pin_memory()
-            hk, hv = w.k_new.pin_memory(), w.v_new.pin_memory()
+            # the step's inputs (q, new K/V, slots, lengths) live in pinned host memory
+            # and the output goes to pinned host memory: the write and decode kernels
+            # read and write them directly over the host link (no staging copies)
+            hq, hk, hv = w.q.pin_memory(), w.k_new.pin_memory(), w.v_new.pin_memory()
             hs, hc = w.new_slots.pin_memory(), w.context_lens.pin_memory()
             hout = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32).pin_memory()
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
-            ds, dc = torch.empty_like(slots), torch.empty_like(cl)
             h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hc))
             d2h = hout.numel() * hout.element_size()
 
             def e2e_step(i):
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                ds.copy_(hs, non_blocking=True)
-                dc.copy_(hc, non_blocking=True)
-                write(i, k_in=dk, v_in=dv, s_in=ds)
-                decode(i, q_in=dq, cl_in=dc)
-                hout.copy_(out, non_blocking=True)
+                write(i, k_in=hk, v_in=hv, s_in=hs)
+                kc, vc, ks, vs = caches[i % args.rotations]
+                fk.paged_decode_attn(hq, kc, vc, bt, hc, kv_dtype=kv_dtype, scale_mode=mode,
+                                     k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=hout,
+                                     num_splits=args.splits, err_flag=err)
 
             with torch.cuda.stream(cap):
                 for i in range(3):
@@ -349,8 +346,10 @@ def run_ours(args, dev, w, world, rank):
             e_gbs, e_tok, _ = aggregate(d_b + w_b, w.B, e_secs, K)
             results["e2e"] = {"value": e_gbs, "unit": "GB/s", "tokens_per_s": e_tok,
                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                              "how": "each step: 5 H2D copies from pinned memory, cache write, "
-                                     "decode, 1 D2H copy; steps replayed as CUDA graphs"}
+                              "how": "each step: cache write and decode reading q, new K/V, "
+                                     "slots and lengths from pinned host memory and writing the "
+                                     "output to pinned host memory (kernel loads/stores over the "
+                                     "host link); steps replayed as CUDA graphs"}
             del egraphs
         del graphs, dgraph, caches
         torch.cuda.synchronize(dev)
@@ -621,8 +620,10 @@ def _extra_write(fk, dev, stream, emit):
         k = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
         v = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
         sets.append((k, v))
+    # prefill-style slots: 16 consecutive tokens per page, pages in shuffled order
     nb = T // 16 + 16
-    slots = torch.randperm(nb * 16, generator=gen, device=dev)[:T].to(torch.int64)
+    pages = torch.randperm(nb, generator=gen, device=dev)[:T // 16].to(torch.int64)
+    slots = (pages[:, None] * 16 + torch.arange(16, device=dev)).reshape(-1)
     kc = torch.zeros(nb, H, 16, D, dtype=torch.uint8, device=dev)
     vc = torch.zeros_like(kc)
     ks = torch.zeros(nb, H, 16, dtype=torch.float32, device=dev)

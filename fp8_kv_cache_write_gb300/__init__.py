@@ -102,13 +102,16 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t, name, dtype=None, device=True, contiguous=True):
+def _check(t, name, dtype=None, device=True, contiguous=True, pinned_ok=False):
+    """dtype / contiguity / placement check.  pinned_ok: pinned host memory is
+    accepted too (the kernels read or write it directly over the host link)."""
     if t is None:
         return
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
-    if device and not t.is_cuda:
-        raise ValueError(f"{name}: expected a CUDA tensor")
+    if device and not t.is_cuda and not (pinned_ok and t.is_pinned()):
+        raise ValueError(f"{name}: expected a CUDA tensor" +
+                         (" or pinned host memory" if pinned_ok else ""))
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name}: expected a contiguous tensor")
 
@@ -123,9 +126,9 @@ def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, *, kv_dtype, scale_mode
                    err_flag=None, stream=None) -> None:
     """Store bf16 K/V rows [T][Hkv][D] at slot_mapping into the paged cache
     (uint8 e4m3 or bf16 [num_blocks][Hkv][16][D]); see fp8kv_kv_cache_write."""
-    _check(k, "k", torch.bfloat16)
-    _check(v, "v", torch.bfloat16)
-    _check(slot_mapping, "slot_mapping", torch.int64)
+    _check(k, "k", torch.bfloat16, pinned_ok=True)
+    _check(v, "v", torch.bfloat16, pinned_ok=True)
+    _check(slot_mapping, "slot_mapping", torch.int64, pinned_ok=True)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
     for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
@@ -157,11 +160,11 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
                       stream=None):
     """Decode attention of q [B][Hq][D] (bf16) over the paged cache; returns out
     [B][Hq][D] (fp32 or bf16).  See fp8kv_paged_decode_attn."""
-    _check(q, "q", torch.bfloat16)
+    _check(q, "q", torch.bfloat16, pinned_ok=True)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
     _check(block_table, "block_table", torch.int32)
-    _check(context_lens, "context_lens", torch.int32)
+    _check(context_lens, "context_lens", torch.int32, pinned_ok=True)
     for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
                  ("v_scale_cache", v_scale_cache)):
         _check(t, n, torch.float32)
@@ -173,11 +176,12 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
     splits, ws_bytes = decode_plan(B, Hq, Hkv, D, mbs, window, num_splits)
     if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size()
                          < ws_bytes):
-        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=k_cache.device)
     if out is None:
-        out = torch.empty(B, Hq, D, device=q.device,
+        out = torch.empty(B, Hq, D, device=k_cache.device,
                           dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
-    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+           pinned_ok=True)
     st = lib().fp8kv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), kv_dtype, scale_mode, _ptr(k_scale),
         _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache), _ptr(block_table), mbs,
@@ -199,12 +203,13 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
     (NOALLOC_DECODE_SCRATCH_BYTES per GPU).  `out` must be passed.  Calls that
     overlap on the GPU race on that array; the first call on a device should
     come before any stream capture."""
-    _check(q, "q", torch.bfloat16)
+    _check(q, "q", torch.bfloat16, pinned_ok=True)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
     _check(block_table, "block_table", torch.int32)
-    _check(context_lens, "context_lens", torch.int32)
-    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    _check(context_lens, "context_lens", torch.int32, pinned_ok=True)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+           pinned_ok=True)
     B, Hq, D = q.shape
     Hkv = k_cache.shape[1]
     mbs = block_table.shape[1]

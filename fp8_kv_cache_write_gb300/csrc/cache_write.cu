@@ -13,7 +13,9 @@
 // bytes (8 bf16), the group reduces max|x| with shuffles, each lane divides its
 // 8 values by s (IEEE fp32 divide), converts pairs with the satfinite e4m3 cvt
 // and stores 8 bytes.  Rows are K and V of every (token, head); the grid strides
-// over them.  Reads 4*Hkv*D and writes 2*Hkv*D (+8*Hkv scale) bytes per token.
+// over them, and each lane has the loads of 4 rows in flight before it converts
+// any (the data load does not wait for the slot lookup).  Launched with
+// programmatic stream serialization: it waits in-kernel for its predecessor.  Reads 4*Hkv*D and writes 2*Hkv*D (+8*Hkv scale) bytes per token.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -32,67 +34,84 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(WriteParams p) {
         kLanes == 32 ? 0xffffffffu : (((1u << kLanes) - 1u) << (sub * kLanes));
 
     pdl_trigger();                           // the decode step may start setting up
+    pdl_wait();                              // inputs of earlier kernels are visible
     const int64_t rows = p.T * p.Hkv * 2;    // (token, head, K|V)
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+    const int64_t step = warp_stride * kRowsPerWarp;   // rows between a lane's unrolled rows
+    constexpr int kUnroll = 4;               // row groups whose loads are in flight together
 
-    for (int64_t base = warp_global * kRowsPerWarp; base < rows;
-         base += warp_stride * kRowsPerWarp) {
-        const int64_t r = base + sub;
-        if (r >= rows) continue;             // whole group leaves together
-        const int which = static_cast<int>(r & 1);          // 0 = K, 1 = V
-        const int64_t th = r >> 1;
-        const int64_t t = th / p.Hkv;
-        const int h = static_cast<int>(th - t * p.Hkv);
-        const int64_t slot = p.slot_mapping[t];
-        if (slot < 0) continue;
-        const int64_t blk = slot / kPage;
-        const int off = static_cast<int>(slot - blk * kPage);
-        if (blk >= p.num_blocks) {
-            if (l == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-            continue;
+    for (int64_t base = warp_global * kRowsPerWarp + sub; base < rows; base += kUnroll * step) {
+        // all loads of the kUnroll rows first (the data load does not wait for the slot)
+        uint4 x[kUnroll];
+        int64_t slot[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * step;
+            slot[u] = -1;
+            x[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) {
+                const int64_t th = r >> 1;
+                const int64_t t = th / p.Hkv;
+                const int h = static_cast<int>(th - t * p.Hkv);
+                slot[u] = p.slot_mapping[t];
+                const __nv_bfloat16* src = ((r & 1) ? p.v : p.k) + (t * p.Hkv + h) * D;
+                x[u] = *reinterpret_cast<const uint4*>(src + l * 8);
+            }
         }
-        const __nv_bfloat16* src = (which ? p.v : p.k) + (t * p.Hkv + h) * D;
-        const uint4 x = *reinterpret_cast<const uint4*>(src + l * 8);
-        const int64_t row = (blk * p.Hkv + h) * kPage + off;
-        if constexpr (BF16) {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which ? p.v_cache : p.k_cache);
-            *reinterpret_cast<uint4*>(dst + row * D + l * 8) = x;
-            continue;
-        } else {
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-            float f[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
-                f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t r = base + u * step;
+            if (r >= rows || slot[u] < 0) continue;   // whole row group leaves together
+            const int which = static_cast<int>(r & 1);          // 0 = K, 1 = V
+            const int64_t th = r >> 1;
+            const int h = static_cast<int>(th - (th / p.Hkv) * p.Hkv);
+            const int64_t blk = slot[u] / kPage;
+            const int off = static_cast<int>(slot[u] - blk * kPage);
+            if (blk >= p.num_blocks) {
+                if (l == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+                continue;
             }
-            float s;
-            if constexpr (MODE == FP8KV_SCALE_PER_TOKEN_HEAD) {
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-                for (int o = kLanes / 2; o > 0; o >>= 1)
-                    amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
-                s = __fdiv_rn(amax, 448.0f);
-                if (l == 0) (which ? p.v_scale_cache : p.k_scale_cache)[row] = s;
-            } else if constexpr (MODE == FP8KV_SCALE_PER_HEAD) {
-                s = (which ? p.v_scale : p.k_scale)[h];
+            const int64_t row = (blk * p.Hkv + h) * kPage + off;
+            if constexpr (BF16) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which ? p.v_cache : p.k_cache);
+                *reinterpret_cast<uint4*>(dst + row * D + l * 8) = x[u];
+                continue;
             } else {
-                s = (which ? p.v_scale : p.k_scale)[0];
-            }
-            uint32_t packed[2] = {0u, 0u};
-            if (s != 0.0f) {
+                const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                float f[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint32_t c = e4m3x2_from_f32(__fdiv_rn(f[2 * i], s),
-                                                       __fdiv_rn(f[2 * i + 1], s));
-                    packed[i >> 1] |= c << (16 * (i & 1));
+                    f[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
+                    f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
                 }
+                float s;
+                if constexpr (MODE == FP8KV_SCALE_PER_TOKEN_HEAD) {
+                    float amax = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+                    for (int o = kLanes / 2; o > 0; o >>= 1)
+                        amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
+                    s = __fdiv_rn(amax, 448.0f);
+                    if (l == 0) (which ? p.v_scale_cache : p.k_scale_cache)[row] = s;
+                } else if constexpr (MODE == FP8KV_SCALE_PER_HEAD) {
+                    s = (which ? p.v_scale : p.k_scale)[h];
+                } else {
+                    s = (which ? p.v_scale : p.k_scale)[0];
+                }
+                uint32_t packed[2] = {0u, 0u};
+                if (s != 0.0f) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t c = e4m3x2_from_f32(__fdiv_rn(f[2 * i], s),
+                                                           __fdiv_rn(f[2 * i + 1], s));
+                        packed[i >> 1] |= c << (16 * (i & 1));
+                    }
+                }
+                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
+                *reinterpret_cast<uint2*>(dst + row * D + l * 8) = make_uint2(packed[0], packed[1]);
             }
-            uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
-            *reinterpret_cast<uint2*>(dst + row * D + l * 8) = make_uint2(packed[0], packed[1]);
         }
     }
 }
@@ -105,8 +124,16 @@ static cudaError_t launch_write(const WriteParams& p, cudaStream_t stream, int n
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    kv_cache_write_kernel<D, MODE, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kv_cache_write_kernel<D, MODE, BF16>, p);
 }
 
 template <int D>

@@ -78,7 +78,9 @@ typedef enum { FP8KV_OUT_F32 = 0, FP8KV_OUT_BF16 = 1 } fp8kv_out_dtype;
  * [KO] opening paragraph (e4m3 storage), [KVQ] "Per-Token-Head vs Per-Tensor
  * 양자화" (scale modes).
  *
- *   k, v          bf16 [T][Hkv][D], row-major.
+ *   k, v          bf16 [T][Hkv][D], row-major.  k, v and slot_mapping may be
+ *                 device memory or pinned host memory (read by the kernel over
+ *                 the host link; one pass, so no staging copy is needed).
  *   slot_mapping  int64 [T]: slot = block * 16 + offset; a negative slot skips
  *                 the token (padding).  A slot at or past num_blocks * 16 sets
  *                 FP8KV_ERR_BAD_INDEX in err_flag and is skipped.
@@ -120,6 +122,9 @@ int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int
  * cache); [KVQ] "Per-Token-Head vs Per-Tensor 양자화" (per-token-head scales).
  *
  *   q              bf16 [B][Hq][D]; query head hq reads KV head hq / (Hq / Hkv).
+ *                  q, context_lens and out may be device memory or pinned host
+ *                  memory (read / written by the kernels over the host link);
+ *                  every other pointer is device memory.
  *   k_cache, v_cache, kv_dtype, scale_mode  as written by fp8kv_kv_cache_write;
  *                  the bf16 cache ignores scales.
  *   k_scale, v_scale              fp32 [1] or [Hkv] (PER_TENSOR / PER_HEAD).

@@ -33,8 +33,10 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(WriteParams p) {
     const unsigned group_mask =
         kLanes == 32 ? 0xffffffffu : (((1u << kLanes) - 1u) << (sub * kLanes));
 
-    pdl_trigger();                           // the decode step may start setting up
+    // wait first: a dependent decode may start its set-up (which reads tables that
+    // kernels before this one may have written) as soon as this kernel triggers
     pdl_wait();                              // inputs of earlier kernels are visible
+    pdl_trigger();                           // the decode step may start setting up
     const int64_t rows = p.T * p.Hkv * 2;    // (token, head, K|V)
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;

@@ -176,7 +176,10 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     const int g = lane >> 2, c = lane & 3;
     const int G = p.G;
     pdl_trigger();                        // split_merge may launch while this runs
-    pdl_wait();                           // inputs of earlier kernels are visible
+    // The set-up below -- shares, segments, page-table rows -- reads only
+    // context_lens, block_table and the constant scales, which must be complete
+    // before the preceding kernel of the stream starts; it overlaps that kernel's
+    // tail.  The wait for it comes before the first cache load or workspace write.
 
     uint8_t* ring = smem + warp * C::kWarpSmem;
     uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
@@ -532,6 +535,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int si = 0; si < nseg; ++si)
             total_groups += (seg[kSegInts * si + 3] - seg[kSegInts * si + 2] + PPI - 1) / PPI;
         const int pre = total_groups < C::kStages ? total_groups : C::kStages;
+        pdl_wait();                       // the preceding kernel's results are visible
         for (int q = 0; q < pre; ++q) issue_next();
 
         int consumed = 0;
@@ -771,8 +775,9 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     const int G = p.G, h = hq / G, head = hq % G;
     const int unit = b * p.Hkv + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvis = vis_pages(p, b);           // context_lens: complete before the chain
     pdl_wait();                                 // the decode kernel's partials are visible
-    if (vis_pages(p, b) == 0) {
+    if (nvis == 0) {
         for (int d = threadIdx.x; d < D; d += blockDim.x)
             store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, 0.f);
         return;

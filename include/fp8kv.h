@@ -139,6 +139,12 @@ int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int
  *   workspace      scratch of at least the planned bytes, 16-byte aligned; its
  *                  contents need no initialisation.  Calls that share one
  *                  workspace must not overlap on the GPU.
+ * Ordering: the kernels launch with programmatic stream serialization.  The
+ * set-up (shares of the work, page-table rows) reads context_lens, block_table
+ * and k_scale / v_scale while the preceding kernel of the stream is still
+ * finishing, so those must be complete before that kernel starts (written by a
+ * copy, or by any earlier kernel); q, the caches and the workspace are accessed
+ * only after the preceding kernel has completed.
  *   out            [B][Hq][D] fp32 or bf16 (out_dtype).
  * Output: softmax(z) V over the visible keys, accumulated in fp32.
  */

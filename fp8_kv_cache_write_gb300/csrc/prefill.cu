@@ -49,10 +49,10 @@ struct PCfg {
     static constexpr int kElem = BF16 ? 2 : 1;
     static constexpr int kKeys = BF16 ? 64 : 128;
     static constexpr int kRowB = D * kElem;                 // bytes of a Q / K / V row
-    // tensor memory: S (or the two-level P V tile) from column 0, O from kOCol;
-    // D 128 takes 256 columns so two co-resident CTAs never wait on each other
+    // tensor memory: S (or the two-level P V tile) from column 0, O from the
+    // kernel's kOCol; D 128 takes 256 columns so two co-resident CTAs never wait
+    // on each other
     static constexpr uint32_t kTmemCols = D <= 128 ? 256u : 512u;
-    static constexpr uint32_t kOCol = D <= 128 ? 128u : 256u;
     static constexpr int kPanels = kRowB / 128;             // 128-byte panels of a row
     static constexpr int kQBytes = kRows * kRowB;           // Q tile
     static constexpr int kKVBytes = kKeys * kRowB;          // one K (or V) tile
@@ -60,14 +60,19 @@ struct PCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;          // [stage][K | V]
     static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes; // [2] P8 tiles
-    static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    static constexpr int kNumBars = 12;
+    // e4m3 only: 16 x 128-byte rows of 1.0 (the bf16 D 256 tiles leave no room)
+    static constexpr int kOffOnes = kOffP + 2 * kPBytes;
+    static constexpr int kOffBar = kOffOnes + (BF16 ? 0 : 16 * 128);
+    static constexpr int kNumBars = 16;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8; // tmem slot, abort flag
     static constexpr int kSmem = 1024 + kOffMisc + 16;
 };
 
 // barrier indices
-enum { kKvFull0 = 0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull, kSEmpty, kPFull0, kPFull1,
+// K and V stages fill and free separately: a K slot is free as soon as its QK
+// has run, so the next K tile loads while the softmax of the current one runs
+enum { kKFull0 = 0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
+       kSFull, kSEmpty, kPFull0, kPFull1,
        kPvDone0, kPvDone1, kPvtFree, kMmaIdle };
 
 __device__ __forceinline__ float ex2p(float x) {
@@ -100,6 +105,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using C = PCfg<D, BF16>;
     constexpr int kKeys = C::kKeys;
+    // TMEM columns: S [0, 128); O from kOCol (two-level on: the P V tile takes
+    // [0, D) and O [kOCol, kOCol + D)).  e4m3, D 256, two-level off: the row sums
+    // l of the quantized weights come from the tensor core too, as P times a
+    // block of ones, into [kLCol, kLCol + 16).
+    constexpr uint32_t kOCol = D <= 128 ? 128u : (TWO_LEVEL ? 256u : 128u);
+    constexpr bool kLMma = D == 256 && !TWO_LEVEL && !BF16;
+    constexpr uint32_t kLCol = kOCol + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -132,10 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
     if (tid == 0) {
-        mbar_init(bar(kKvFull0), 1);
-        mbar_init(bar(kKvFull1), 1);
-        mbar_init(bar(kKvEmpty0), 1);
-        mbar_init(bar(kKvEmpty1), 1);
+        for (int i = kKFull0; i <= kVEmpty1; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kSFull), 1);
         mbar_init(bar(kSEmpty), kRows);
         mbar_init(bar(kPFull0), kRows);
@@ -181,6 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(qtile + panel * (kRows * 128) + r * 128 +
                                       ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        if constexpr (kLMma) {                          // 16 rows of 128 bytes of 1.0
+            const uint32_t one = 0x38383838u;
+            for (int i = tid; i < 16 * 128 / 16; i += kRows)
+                *reinterpret_cast<uint4*>(smem + C::kOffOnes + i * 16) =
+                    make_uint4(one, one, one, one);
+        }
         fence_proxy_async();                            // generic writes -> tensor core reads
     }
     tc_fence_before();
@@ -191,44 +206,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 4) {
         // =============================== TMA producer
         const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-        int issued = 0;
+        int issued_k = 0, issued_v = 0;
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
-            bool go = true;
-            if (j >= 2 && lane == 0)
-                go = wait_or_abort(bar(kKvEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
-            if (!__shfl_sync(0xffffffffu, go, 0)) break;
             const int page0 = j * (kKeys / kPage);
             int n_pages = ctx_pages - page0;
             n_pages = n_pages > kKeys / kPage ? kKeys / kPage : n_pages;
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar(kKvFull0 + st),
-                                      static_cast<uint32_t>(n_pages) * 2u * kPage * C::kRowB);
-            __syncwarp();
+            int z = 0;
             if (lane < n_pages) {
                 int blk = bt_row[page0 + lane];
                 if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
                     report(p.err, FP8KV_ERR_BAD_INDEX);
                     blk = 0;
                 }
-                const int z = blk * p.Hkv + h;
-                const uint32_t kdst = sbase + C::kOffKV + st * 2 * C::kKVBytes;
-                const uint32_t vdst = kdst + C::kKVBytes;
+                z = blk * p.Hkv + h;
+            }
+            const uint32_t tile_bytes = static_cast<uint32_t>(n_pages) * kPage * C::kRowB;
+            const uint32_t kdst = sbase + C::kOffKV + st * 2 * C::kKVBytes;
+            const uint32_t vdst = kdst + C::kKVBytes;
+            // K tile j (its slot held K of tile j - 2 until that QK ran)
+            bool go = true;
+            if (j >= 2 && lane == 0)
+                go = wait_or_abort(bar(kKEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(kKFull0 + st), tile_bytes);
+            __syncwarp();
+            if (lane < n_pages) {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn) {
+                for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_3d(kdst + pn * (kKeys * 128) + lane * 2048, &kmap, pn * 128, 0, z,
-                                bar(kKvFull0 + st));
-                    tma_load_3d(vdst + pn * (kKeys * 128) + lane * 2048, &vmap, pn * 128, 0, z,
-                                bar(kKvFull0 + st));
-                }
+                                bar(kKFull0 + st));
             }
             __syncwarp();
-            issued = j + 1;
+            issued_k = j + 1;
+            // V tile j (its slot held V of tile j - 2 until that PV ran)
+            if (j >= 2 && lane == 0)
+                go = wait_or_abort(bar(kVEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + st), tile_bytes);
+            __syncwarp();
+            if (lane < n_pages) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_3d(vdst + pn * (kKeys * 128) + lane * 2048, &vmap, pn * 128, 0, z,
+                                bar(kVFull0 + st));
+            }
+            __syncwarp();
+            issued_v = j + 1;
         }
         // copies still in flight land before the CTA can leave (each wait bounded)
         if (lane == 0 && *abort_flag) {
-            for (int j = issued - 2 > 0 ? issued - 2 : 0; j < issued; ++j)
-                (void)mbar_wait_bounded(bar(kKvFull0 + (j & 1)), (j >> 1) & 1);
+            for (int j = issued_k - 2 > 0 ? issued_k - 2 : 0; j < issued_k; ++j)
+                (void)mbar_wait_bounded(bar(kKFull0 + (j & 1)), (j >> 1) & 1);
+            for (int j = issued_v - 2 > 0 ? issued_v - 2 : 0; j < issued_v; ++j)
+                (void)mbar_wait_bounded(bar(kVFull0 + (j & 1)), (j >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -238,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kFmt = BF16 ? 1u : 0u;
             constexpr uint32_t idesc_qk = instr_desc(kFmt, kFmt, 0, 0, kKeys, kRows);
             constexpr uint32_t idesc_pv = instr_desc(kFmt, kFmt, 0, 1, D, kRows);
+            constexpr uint32_t idesc_l = instr_desc(kFmt, kFmt, 0, 0, 16, kRows);
             auto mma = [&](uint32_t d, uint64_t a, uint64_t bdsc, uint32_t id, uint32_t acc) {
                 if constexpr (BF16)
                     mma_f16kind(d, a, bdsc, id, acc);
@@ -245,19 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f8f6f4(d, a, bdsc, id, acc);
             };
             const uint32_t tS = tmem;                           // S: columns [0, 128)
-            const uint32_t tO = tmem + (TWO_LEVEL ? 0u : C::kOCol); // PV target
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (!wait_or_abort(bar(kKvFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
-                if (j > 0) {
-                    if (!wait_or_abort(bar(kSEmpty), (j - 1) & 1, abort_flag, p.err)) break;
-                    if (TWO_LEVEL &&
-                        !wait_or_abort(bar(kPvtFree), (j - 1) & 1, abort_flag, p.err))
-                        break;
-                }
-                tc_fence_after();
-                const uint32_t kbase = sbase + C::kOffKV + st * 2 * C::kKVBytes;
-                const uint32_t vbase = kbase + C::kKVBytes;
+            const uint32_t tO = tmem + (TWO_LEVEL ? 0u : kOCol); // PV target
+            auto issue_qk = [&](int j) {
+                const uint32_t kbase = sbase + C::kOffKV + (j & 1) * 2 * C::kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < C::kRowB / 32; ++kk) {    // 32-byte k-steps over D
                     const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
@@ -267,9 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(kSFull));
-                if (!wait_or_abort(bar(kPFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                const uint32_t pbase = sbase + C::kOffP + st * C::kPBytes;
+                mma_commit(bar(kKEmpty0 + (j & 1)));
+            };
+            auto issue_pv = [&](int j) {
+                const uint32_t vbase = sbase + C::kOffKV + (j & 1) * 2 * C::kKVBytes + C::kKVBytes;
+                const uint32_t pbase = sbase + C::kOffP + (j & 1) * C::kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kKeys * C::kElem / 32; ++kk) {   // 32-byte k-steps over keys
                     const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
@@ -280,9 +304,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t acc = TWO_LEVEL ? (kk > 0 ? 1u : 0u)
                                                    : ((j > 0 || kk > 0) ? 1u : 0u);
                     mma(tO, ad, bd, idesc_pv, acc);
+                    if constexpr (kLMma) {
+                        const uint64_t od = smem_desc_sw128(sbase + C::kOffOnes + kk * 32, 16, 1024);
+                        mma(tmem + kLCol, ad, od, idesc_l, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                mma_commit(bar(kPvDone0 + st));
-                mma_commit(bar(kKvEmpty0 + st));
+                mma_commit(bar(kPvDone0 + (j & 1)));
+                mma_commit(bar(kVEmpty0 + (j & 1)));
+            };
+            if constexpr (!TWO_LEVEL) {
+                // S of tile j+1 is computed while the softmax warps work on tile j:
+                // the QK of j+1 waits only for S(j) to have been read, not for P(j)
+                if (n_tiles > 0 && wait_or_abort(bar(kKFull0), 0, abort_flag, p.err)) {
+                    tc_fence_after();
+                    issue_qk(0);
+                    for (int j = 0; j < n_tiles; ++j) {
+                        if (j + 1 < n_tiles) {
+                            if (!wait_or_abort(bar(kKFull0 + ((j + 1) & 1)), ((j + 1) >> 1) & 1,
+                                               abort_flag, p.err))
+                                break;
+                            if (!wait_or_abort(bar(kSEmpty), j & 1, abort_flag, p.err)) break;
+                            tc_fence_after();
+                            issue_qk(j + 1);
+                        }
+                        if (!wait_or_abort(bar(kPFull0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))
+                            break;
+                        if (!wait_or_abort(bar(kVFull0 + (j & 1)), (j >> 1) & 1, abort_flag, p.err))
+                            break;
+                        tc_fence_after();
+                        issue_pv(j);
+                    }
+                }
+            } else {
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int st = j & 1;
+                    if (!wait_or_abort(bar(kKFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
+                    if (j > 0) {
+                        if (!wait_or_abort(bar(kSEmpty), (j - 1) & 1, abort_flag, p.err)) break;
+                        if (!wait_or_abort(bar(kPvtFree), (j - 1) & 1, abort_flag, p.err)) break;
+                    }
+                    tc_fence_after();
+                    issue_qk(j);
+                    if (!wait_or_abort(bar(kPFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
+                    if (!wait_or_abort(bar(kVFull0 + st), (j >> 1) & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    issue_pv(j);
+                }
             }
             // every issued MMA finishes before tensor memory is released (bounded
             // wait that does not stop early on an abort)
@@ -305,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             qs = p.q_scale;
             ps = p.prob_scale;
         }
-        const float sc = qs * kconst * p.scale_log2;
-        const float inv_ps = 1.0f / ps;
+        const float sc = qs * kconst * p.scale_log2;   // > 0: the max of raw S scales
+        const float lps = log2f(ps);                   // p / prob_scale = 2^(s sc - m - lps)
         float m = kMaxInitP, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -316,29 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            float s[kKeys];
+            uint32_t sb[kKeys];                 // raw S of this row: all loads, then one wait
 #pragma unroll
             for (int cch = 0; cch < kKeys / 32; ++cch) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + cch * 32, rr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[cch * 32 + i] = __uint_as_float(rr[i]);
+                uint32_t* dst = sb + cch * 32;
+                tmem_ld32(tmem + lane_addr + cch * 32,
+                          *reinterpret_cast<uint32_t(*)[32]>(dst));
             }
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(kSEmpty));
 
-            // logits (base 2) with the causal mask; keys past ctx are always masked
+            // causal mask on the raw logits (keys past ctx always masked), the row
+            // max of raw S, then base-2 logits s * sc - m inside one FFMA below
             const int key0 = j * kKeys;
-            float mx = -__int_as_float(0x7f800000);
+            float s[kKeys];
+            float mx_raw = -__int_as_float(0x7f800000);
             const bool full = key0 + kKeys - 1 <= pos_r;
 #pragma unroll
             for (int i = 0; i < kKeys; ++i) {
-                const float x = (full || key0 + i <= pos_r) ? s[i] * sc
+                const float x = (full || key0 + i <= pos_r) ? __uint_as_float(sb[i])
                                                             : -__int_as_float(0x7f800000);
                 s[i] = x;
-                mx = fmaxf(mx, x);
+                mx_raw = fmaxf(mx_raw, x);
             }
+            const float mx = mx_raw * sc;
             float alpha = 1.f;
             if (mx > m + 8.f) {                 // lazy running max
                 alpha = ex2p(m - mx);
@@ -357,10 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // O's columns (and, when the tensor core sums l, l's columns)
 #pragma unroll 1
-                    for (int cch = 0; cch < D / 32; ++cch) {
+                    for (int cch = 0; cch < D / 32 + (kLMma ? 1 : 0); ++cch) {
                         uint32_t rr[32];
-                        const uint32_t ta = tmem + lane_addr + C::kOCol + cch * 32;
+                        const uint32_t ta = tmem + lane_addr + kOCol + cch * 32;
                         tmem_ld32(ta, rr);
                         tmem_wait_ld();
 #pragma unroll
@@ -383,23 +453,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t w[4];
+                const float moff = m + lps;
 #pragma unroll
                 for (int i = 0; i < kPerChunk / 2; ++i) {
-                    const float pa = ex2p(s[cc * kPerChunk + 2 * i] - m) * inv_ps;
-                    const float pb = ex2p(s[cc * kPerChunk + 2 * i + 1] - m) * inv_ps;
+                    const float pa = ex2p(fmaf(s[cc * kPerChunk + 2 * i], sc, -moff));
+                    const float pb = ex2p(fmaf(s[cc * kPerChunk + 2 * i + 1], sc, -moff));
                     // the denominator sums the same rounded weights the MMA uses
+                    // (on the tensor core for D 256, two-level off)
                     if constexpr (BF16) {
                         w[i] = pack_bf16x2(pa, pb);
-                        const float2 q2 = unpack_bf16x2(w[i]);
-                        l += q2.x + q2.y;
+                        if constexpr (!kLMma) {
+                            const float2 q2 = unpack_bf16x2(w[i]);
+                            l += q2.x + q2.y;
+                        }
                     } else {
                         const uint32_t code = e4m3x2_from_f32(pa, pb);
                         if (i & 1)
                             w[i >> 1] |= code << 16;
                         else
                             w[i >> 1] = code;
-                        const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
-                        l += q2.x + q2.y;
+                        if constexpr (!kLMma) {
+                            const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
+                            l += q2.x + q2.y;
+                        }
                     }
                 }
                 *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
@@ -409,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bytes, NaN codes included): zero them so 0 * v stays 0
             if (key0 + kKeys > ctx) {
                 if (!__all_sync(0xffffffffu,
-                                wait_or_abort(bar(kKvFull0 + st), (j >> 1) & 1, abort_flag, p.err))) {
+                                wait_or_abort(bar(kVFull0 + st), (j >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
@@ -437,14 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cch = 0; cch < D / 32; ++cch) {
                     uint32_t pv[32], acc[32];
                     tmem_ld32(tmem + lane_addr + cch * 32, pv);
-                    if (j > 0) tmem_ld32(tmem + lane_addr + C::kOCol + cch * 32, acc);
+                    if (j > 0) tmem_ld32(tmem + lane_addr + kOCol + cch * 32, acc);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float prev = j > 0 ? __uint_as_float(acc[i]) * alpha : 0.f;
                         acc[i] = __float_as_uint(prev + __uint_as_float(pv[i]));
                     }
-                    tmem_st32(tmem + lane_addr + C::kOCol + cch * 32, acc);
+                    tmem_st32(tmem + lane_addr + kOCol + cch * 32, acc);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -461,11 +537,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
+            if constexpr (kLMma) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + kLCol, rr);
+                tmem_wait_ld();
+                l = __uint_as_float(rr[0]);
+            }
             const float f = l > 0.f ? vconst * ps / l : 0.f;
             const int head = r % G;
             for (int cch = 0; cch < D / 32; ++cch) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + C::kOCol + cch * 32, rr);
+                tmem_ld32(tmem + lane_addr + kOCol + cch * 32, rr);
                 tmem_wait_ld();
                 if (row_ok) {
                     const size_t o = (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D +

@@ -39,7 +39,6 @@ namespace fp8kv {
 namespace {
 
 constexpr int kRows = 128;          // MMA M: query rows of a CTA
-constexpr int kThreads = 192;
 constexpr float kMaxInitP = -1.0e30f;
 
 template <int D, bool BF16>
@@ -62,8 +61,16 @@ struct PCfg {
     static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes; // [2] P8 tiles
     // e4m3 only: 16 x 128-byte rows of 1.0 (the bf16 D 256 tiles leave no room)
     static constexpr int kOffOnes = kOffP + 2 * kPBytes;
-    static constexpr int kOffBar = kOffOnes + (BF16 ? 0 : 16 * 128);
-    static constexpr int kNumBars = 16;
+    static constexpr int kOffOnes2 = kOffOnes + (BF16 ? 0 : 16 * 128);
+    // softmax warps: two per row quarter, each on half of a tile's keys (the
+    // row maxima meet in shared memory), except bf16 D 256 whose tiles leave
+    // no shared memory for that exchange (one warp per quarter)
+    static constexpr int kHalves = (BF16 && D == 256) ? 1 : 2;
+    static constexpr int kSoftWarps = 4 * kHalves;
+    static constexpr int kThreads = 32 * (kSoftWarps + 2);   // + TMA warp + MMA warp
+    static constexpr int kOffPMax = kOffOnes2;               // [2][kHalves][128] partial maxima
+    static constexpr int kOffBar = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
+    static constexpr int kNumBars = 20;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8; // tmem slot, abort flag
     static constexpr int kSmem = 1024 + kOffMisc + 16;
 };
@@ -73,7 +80,7 @@ struct PCfg {
 // has run, so the next K tile loads while the softmax of the current one runs
 enum { kKFull0 = 0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
        kSFull, kSEmpty, kPFull0, kPFull1,
-       kPvDone0, kPvDone1, kPvtFree, kMmaIdle };
+       kPvDone0, kPvDone1, kPvtFree, kMmaIdle, kPair0 };   // kPair0 .. kPair0 + 3
 
 __device__ __forceinline__ float ex2p(float x) {
     float y;
@@ -100,11 +107,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 template <int D, bool TWO_LEVEL, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using C = PCfg<D, BF16>;
     constexpr int kKeys = C::kKeys;
+    constexpr int kHalves = C::kHalves;
+    constexpr int kSoft = 32 * C::kSoftWarps;          // softmax threads
+    constexpr int kTmaWarp = C::kSoftWarps, kMmaWarp = C::kSoftWarps + 1;
     // TMEM columns: S [0, 128); O from kOCol (two-level on: the P V tile takes
     // [0, D) and O [kOCol, kOCol + D)).  e4m3, D 256, two-level off: the row sums
     // l of the quantized weights come from the tensor core too, as P times a
@@ -146,25 +156,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = kKFull0; i <= kVEmpty1; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kSFull), 1);
-        mbar_init(bar(kSEmpty), kRows);
-        mbar_init(bar(kPFull0), kRows);
-        mbar_init(bar(kPFull1), kRows);
+        mbar_init(bar(kSEmpty), kSoft);
+        mbar_init(bar(kPFull0), kSoft);
+        mbar_init(bar(kPFull1), kSoft);
         mbar_init(bar(kPvDone0), 1);
         mbar_init(bar(kPvDone1), 1);
-        mbar_init(bar(kPvtFree), kRows);
+        mbar_init(bar(kPvtFree), kSoft);
         mbar_init(bar(kMmaIdle), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(kPair0 + i), 64);   // the two warps of a quarter
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 5) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
     // ---- Q tile (K-major, 128-byte swizzle): e4m3(q / q_scale), or q itself (bf16)
-    if (warp < 4) {
-        const int r = tid;
+    if (warp < C::kSoftWarps) {
+        const int r = tid & (kRows - 1);
+        const int half = tid / kRows;                   // which chunks of the row
         const int tk = tok0 + r / G, head = r % G;
         uint8_t* qtile = smem + C::kOffQ;
+        constexpr int kChunks = C::kRowB / 16 / kHalves;
 #pragma unroll 4
-        for (int c = 0; c < C::kRowB / 16; ++c) {       // 16-byte chunks of the row
+        for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {   // 16-byte chunks
             uint32_t w[4] = {0u, 0u, 0u, 0u};
             if (tk < nq) {
                 const __nv_bfloat16* src =
@@ -192,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (kLMma) {                          // 16 rows of 128 bytes of 1.0
             const uint32_t one = 0x38383838u;
-            for (int i = tid; i < 16 * 128 / 16; i += kRows)
+            for (int i = tid; i < 16 * 128 / 16; i += kSoft)
                 *reinterpret_cast<uint4*>(smem + C::kOffOnes + i * 16) =
                     make_uint4(one, one, one, one);
         }
@@ -203,18 +216,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kTmaWarp) {
         // =============================== TMA producer
         const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
         int issued_k = 0, issued_v = 0;
+        // block ids of tile j's pages (lane = page), loaded one tile ahead so that
+        // no iteration waits for its page-table row
+        auto tile_blk = [&](int j) -> int {
+            const int pg = j * (kKeys / kPage) + lane;
+            return (j < n_tiles && lane < kKeys / kPage && pg < ctx_pages) ? bt_row[pg] : 0;
+        };
+        int blk_next = tile_blk(0);
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
             const int page0 = j * (kKeys / kPage);
             int n_pages = ctx_pages - page0;
             n_pages = n_pages > kKeys / kPage ? kKeys / kPage : n_pages;
+            int blk = blk_next;
+            blk_next = tile_blk(j + 1);
             int z = 0;
             if (lane < n_pages) {
-                int blk = bt_row[page0 + lane];
                 if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
                     report(p.err, FP8KV_ERR_BAD_INDEX);
                     blk = 0;
@@ -262,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait_bounded(bar(kVFull0 + (j & 1)), (j >> 1) & 1);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // =============================== MMA issuer (one thread)
         if (lane == 0) {
             // e4m3 operands (kind::f8f6f4, format 0) or bf16 (kind::f16, format 1)
@@ -358,12 +379,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // =============================== softmax / correction / epilogue (row = tid)
-        const int r = tid;
+        // =============================== softmax / correction / epilogue
+        // row r of TMEM lane quarter warp % 4; key half kh of every tile (columns
+        // [kh * kKH, (kh + 1) * kKH)) and of O's columns
+        const int r = 32 * (warp & 3) + lane;
+        const int kh = warp / 4;
+        constexpr int kKH = kKeys / kHalves;            // keys of a tile this thread owns
+        constexpr int kDH = D / kHalves;                // O columns this thread owns
         const int tk = tok0 + r / G;
         const bool row_ok = tk < nq;
         const int pos_r = row_ok ? pos_base + tk : -1;
-        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        float* pmax = reinterpret_cast<float*>(smem + C::kOffPMax);   // [2][kHalves][128]
+        int pair_phase = 0;
+        // the two warps of a quarter meet (an mbarrier with a bounded wait, so a
+        // stuck partner ends in FP8KV_ERR_TIMEOUT rather than a hang)
+        auto pair_sync = [&]() -> bool {
+            mbar_arrive(bar(kPair0 + (warp & 3)));
+            const bool okp = wait_or_abort(bar(kPair0 + (warp & 3)), pair_phase & 1, abort_flag,
+                                           p.err);
+            ++pair_phase;
+            return __all_sync(0xffffffffu, okp);
+        };
         // the bf16 cache has no scales and keeps Q and P in bf16
         float kconst = 1.f, vconst = 1.f, qs = 1.f, ps = 1.f;
         if constexpr (!BF16) {
@@ -374,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float sc = qs * kconst * p.scale_log2;   // > 0: the max of raw S scales
         const float lps = log2f(ps);                   // p / prob_scale = 2^(s sc - m - lps)
-        float m = kMaxInitP, l = 0.f;
+        float m = kMaxInitP, l = 0.f;                  // l: this half's keys (summed at the end)
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
             const int st = j & 1;
@@ -383,11 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sb[kKeys];                 // raw S of this row: all loads, then one wait
+            uint32_t sb[kKH];                   // raw S of this row's half: all loads, one wait
 #pragma unroll
-            for (int cch = 0; cch < kKeys / 32; ++cch) {
+            for (int cch = 0; cch < kKH / 32; ++cch) {
                 uint32_t* dst = sb + cch * 32;
-                tmem_ld32(tmem + lane_addr + cch * 32,
+                tmem_ld32(tmem + lane_addr + kh * kKH + cch * 32,
                           *reinterpret_cast<uint32_t(*)[32]>(dst));
             }
             tmem_wait_ld();
@@ -396,20 +433,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // causal mask on the raw logits (keys past ctx always masked), the row
             // max of raw S, then base-2 logits s * sc - m inside one FFMA below
-            const int key0 = j * kKeys;
-            float s[kKeys];
-            float mx_raw = -__int_as_float(0x7f800000);
-            const bool full = key0 + kKeys - 1 <= pos_r;
+            const int key0 = j * kKeys + kh * kKH;
+            float s[kKH];
+            float mxp[8];                       // 8 independent partial maxima
 #pragma unroll
-            for (int i = 0; i < kKeys; ++i) {
-                const float x = (full || key0 + i <= pos_r) ? __uint_as_float(sb[i])
-                                                            : -__int_as_float(0x7f800000);
-                s[i] = x;
-                mx_raw = fmaxf(mx_raw, x);
+            for (int i = 0; i < 8; ++i) mxp[i] = -__int_as_float(0x7f800000);
+            const bool full = key0 + kKH - 1 <= pos_r;
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < kKH; ++i) {
+                    s[i] = __uint_as_float(sb[i]);
+                    mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kKH; ++i) {
+                    s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) : -__int_as_float(0x7f800000);
+                    mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                }
+            }
+            float mx_raw = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            if constexpr (kHalves == 2) {       // the row's max over both halves
+                pmax[(st * 2 + kh) * kRows + r] = mx_raw;
+                if (!pair_sync()) {
+                    ok = false;
+                    break;
+                }
+                mx_raw = fmaxf(mx_raw, pmax[(st * 2 + (kh ^ 1)) * kRows + r]);
             }
             const float mx = mx_raw * sc;
             float alpha = 1.f;
-            if (mx > m + 8.f) {                 // lazy running max
+            if (mx > m + 8.f) {                 // lazy running max (the same in both halves)
                 alpha = ex2p(m - mx);
                 m = mx;
                 l *= alpha;
@@ -417,31 +472,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a row whose max moved rescales its O row in TMEM (two-level off); the
             // tcgen05 loads are warp-wide, so the warp does it when any row needs it
             if (!TWO_LEVEL && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                {
-                    // O (TMEM) must hold PV of tile j-1 before it is rescaled
-                    if (!__all_sync(0xffffffffu,
-                                    wait_or_abort(bar(kPvDone0 + ((j - 1) & 1)),
-                                                  ((j - 1) >> 1) & 1, abort_flag, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // O's columns (and, when the tensor core sums l, l's columns)
-#pragma unroll 1
-                    for (int cch = 0; cch < D / 32 + (kLMma ? 1 : 0); ++cch) {
-                        uint32_t rr[32];
-                        const uint32_t ta = tmem + lane_addr + kOCol + cch * 32;
-                        tmem_ld32(ta, rr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                        tmem_st32(ta, rr);
-                    }
-                    tmem_wait_st();
+                // O (TMEM) must hold PV of tile j-1 before it is rescaled
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(bar(kPvDone0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
+                                              abort_flag, p.err))) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after();
+                // this half's O columns, and l's columns (tensor-core l) in half 0
+                constexpr int kChunks = kDH / 32;
+#pragma unroll 1
+                for (int cch = 0; cch < kChunks + ((kLMma) ? 1 : 0); ++cch) {
+                    if (cch == kChunks && kh != 0) break;
+                    uint32_t rr[32];
+                    const uint32_t ta = tmem + lane_addr +
+                                        (cch < kChunks ? kOCol + kh * kDH + cch * 32 : kLCol);
+                    tmem_ld32(ta, rr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                    tmem_st32(ta, rr);
+                }
+                tmem_wait_st();
             }
-            // P8 tile j&1 was read by PV of tile j-2
+            // P tile j&1 was read by PV of tile j-2
             if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(kPvDone0 + st),
                                                                  ((j - 2) >> 1) & 1, abort_flag,
                                                                  p.err))) {
@@ -450,16 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint8_t* prow = smem + C::kOffP + st * C::kPBytes + r * 128;
             constexpr int kPerChunk = 16 / C::kElem;    // keys per 16-byte chunk
+            constexpr int kMyChunks = 8 / kHalves;      // this half's chunks of the row
+            const float moff = m + lps;
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int c8 = 0; c8 < kMyChunks; ++c8) {
+                const int cc = kh * kMyChunks + c8;
                 uint32_t w[4];
-                const float moff = m + lps;
 #pragma unroll
                 for (int i = 0; i < kPerChunk / 2; ++i) {
-                    const float pa = ex2p(fmaf(s[cc * kPerChunk + 2 * i], sc, -moff));
-                    const float pb = ex2p(fmaf(s[cc * kPerChunk + 2 * i + 1], sc, -moff));
+                    const float pa = ex2p(fmaf(s[c8 * kPerChunk + 2 * i], sc, -moff));
+                    const float pb = ex2p(fmaf(s[c8 * kPerChunk + 2 * i + 1], sc, -moff));
                     // the denominator sums the same rounded weights the MMA uses
-                    // (on the tensor core for D 256, two-level off)
+                    // (on the tensor core for D 256, e4m3, two-level off)
                     if constexpr (BF16) {
                         w[i] = pack_bf16x2(pa, pb);
                         if constexpr (!kLMma) {
@@ -483,16 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // value rows past ctx in the last tile hold unwritten cache slots (any
             // bytes, NaN codes included): zero them so 0 * v stays 0
-            if (key0 + kKeys > ctx) {
+            if (j * kKeys + kKeys > ctx) {
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(bar(kVFull0 + st), (j >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 uint8_t* vt = smem + C::kOffKV + st * 2 * C::kKVBytes + C::kKVBytes;
-                for (int idx = r; idx < kKeys * C::kPanels * 8; idx += kRows) {
+                for (int idx = tid; idx < kKeys * C::kPanels * 8; idx += kSoft) {
                     const int chunk = idx & 7, row = (idx >> 3) % kKeys, pn = (idx >> 3) / kKeys;
-                    if (key0 + row >= ctx)
+                    if (j * kKeys + row >= ctx)
                         *reinterpret_cast<uint4*>(vt + pn * (kKeys * 128) + row * 128 +
                                                   chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -502,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(kPFull0 + st));
 
             if constexpr (TWO_LEVEL) {
-                // O_acc (fp32, TMEM columns [kOCol, kOCol + D)) = alpha * O_acc + P V of this tile
+                // O_acc (fp32, TMEM columns [kOCol, kOCol + D)) = alpha * O_acc + P V of
+                // this tile; this half's columns
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(bar(kPvDone0 + st), (j >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
@@ -510,17 +569,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int cch = 0; cch < D / 32; ++cch) {
+                for (int cch = 0; cch < kDH / 32; ++cch) {
+                    const int col = kh * kDH + cch * 32;
                     uint32_t pv[32], acc[32];
-                    tmem_ld32(tmem + lane_addr + cch * 32, pv);
-                    if (j > 0) tmem_ld32(tmem + lane_addr + kOCol + cch * 32, acc);
+                    tmem_ld32(tmem + lane_addr + col, pv);
+                    if (j > 0) tmem_ld32(tmem + lane_addr + kOCol + col, acc);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float prev = j > 0 ? __uint_as_float(acc[i]) * alpha : 0.f;
                         acc[i] = __float_as_uint(prev + __uint_as_float(pv[i]));
                     }
-                    tmem_st32(tmem + lane_addr + kOCol + cch * 32, acc);
+                    tmem_st32(tmem + lane_addr + kOCol + col, acc);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -542,16 +602,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_addr + kLCol, rr);
                 tmem_wait_ld();
                 l = __uint_as_float(rr[0]);
+            } else if constexpr (kHalves == 2) {     // the two halves' sums
+                // through the buffer of tile n-2, which both warps have finished with
+                const int lb = ((n_tiles - 1) & 1) ^ 1;
+                pmax[(lb * 2 + kh) * kRows + r] = l;
+                if (pair_sync()) {
+                    l += pmax[(lb * 2 + (kh ^ 1)) * kRows + r];
+                } else {
+                    ok = false;
+                }
             }
+        }
+        if (ok) {
             const float f = l > 0.f ? vconst * ps / l : 0.f;
             const int head = r % G;
-            for (int cch = 0; cch < D / 32; ++cch) {
+            for (int cch = 0; cch < kDH / 32; ++cch) {
+                const int col = kh * kDH + cch * 32;
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + kOCol + cch * 32, rr);
+                tmem_ld32(tmem + lane_addr + kOCol + col, rr);
                 tmem_wait_ld();
                 if (row_ok) {
-                    const size_t o = (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D +
-                                     cch * 32;
+                    const size_t o = (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D + col;
                     if (p.out_bf16) {
                         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
 #pragma unroll
@@ -573,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -594,7 +665,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     dim3 grid(grid_x, p.Hkv, p.B);
-    kern<<<grid, kThreads, PCfg<D, BF16>::kSmem, stream>>>(kmap, vmap, p);
+    kern<<<grid, PCfg<D, BF16>::kThreads, PCfg<D, BF16>::kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 

@@ -67,7 +67,7 @@ struct PCfg {
     // no shared memory for that exchange (one warp per quarter)
     static constexpr int kHalves = (BF16 && D == 256) ? 1 : 2;
     static constexpr int kSoftWarps = 4 * kHalves;
-    static constexpr int kThreads = 32 * (kSoftWarps + 2);   // + TMA warp + MMA warp
+    static constexpr int kThreads = 32 * (kSoftWarps + 3);   // + K loader, MMA, V loader
     static constexpr int kOffPMax = kOffOnes2;               // [2][kHalves][128] partial maxima
     static constexpr int kOffBar = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
     static constexpr int kNumBars = 20;
@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     constexpr int kKeys = C::kKeys;
     constexpr int kHalves = C::kHalves;
     constexpr int kSoft = 32 * C::kSoftWarps;          // softmax threads
-    constexpr int kTmaWarp = C::kSoftWarps, kMmaWarp = C::kSoftWarps + 1;
+    // K and V tiles come from two loader warps: a single warp issuing every copy
+    // of a tile held the pipeline back
+    constexpr int kTmaWarp = C::kSoftWarps, kMmaWarp = C::kSoftWarps + 1,
+                  kVWarp = C::kSoftWarps + 2;
     // TMEM columns: S [0, 128); O from kOCol (two-level on: the P V tile takes
     // [0, D) and O [kOCol, kOCol + D)).  e4m3, D 256, two-level off: the row sums
     // l of the quantized weights come from the tensor core too, as P times a
@@ -216,10 +219,13 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kTmaWarp) {
-        // =============================== TMA producer
+    if (warp == kTmaWarp || warp == kVWarp) {
+        // =============================== TMA producers: K tiles (kTmaWarp), V tiles (kVWarp)
+        const bool is_v = warp == kVWarp;
+        const CUtensorMap* map = is_v ? &vmap : &kmap;
+        const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-        int issued_k = 0, issued_v = 0;
+        int issued = 0;
         // block ids of tile j's pages (lane = page), loaded one tile ahead so that
         // no iteration waits for its page-table row
         auto tile_blk = [&](int j) -> int {
@@ -237,50 +243,33 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             int z = 0;
             if (lane < n_pages) {
                 if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
-                    report(p.err, FP8KV_ERR_BAD_INDEX);
+                    if (!is_v) report(p.err, FP8KV_ERR_BAD_INDEX);
                     blk = 0;
                 }
                 z = blk * p.Hkv + h;
             }
             const uint32_t tile_bytes = static_cast<uint32_t>(n_pages) * kPage * C::kRowB;
-            const uint32_t kdst = sbase + C::kOffKV + st * 2 * C::kKVBytes;
-            const uint32_t vdst = kdst + C::kKVBytes;
-            // K tile j (its slot held K of tile j - 2 until that QK ran)
+            const uint32_t dst = sbase + C::kOffKV + st * 2 * C::kKVBytes + (is_v ? C::kKVBytes : 0);
+            // the slot held the tile j - 2 until its QK (K) or PV (V) ran
             bool go = true;
             if (j >= 2 && lane == 0)
-                go = wait_or_abort(bar(kKEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
+                go = wait_or_abort(bar(empty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(kKFull0 + st), tile_bytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), tile_bytes);
             __syncwarp();
             if (lane < n_pages) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_3d(kdst + pn * (kKeys * 128) + lane * 2048, &kmap, pn * 128, 0, z,
-                                bar(kKFull0 + st));
+                    tma_load_3d(dst + pn * (kKeys * 128) + lane * 2048, map, pn * 128, 0, z,
+                                bar(full0 + st));
             }
             __syncwarp();
-            issued_k = j + 1;
-            // V tile j (its slot held V of tile j - 2 until that PV ran)
-            if (j >= 2 && lane == 0)
-                go = wait_or_abort(bar(kVEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
-            if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(kVFull0 + st), tile_bytes);
-            __syncwarp();
-            if (lane < n_pages) {
-#pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_3d(vdst + pn * (kKeys * 128) + lane * 2048, &vmap, pn * 128, 0, z,
-                                bar(kVFull0 + st));
-            }
-            __syncwarp();
-            issued_v = j + 1;
+            issued = j + 1;
         }
         // copies still in flight land before the CTA can leave (each wait bounded)
         if (lane == 0 && *abort_flag) {
-            for (int j = issued_k - 2 > 0 ? issued_k - 2 : 0; j < issued_k; ++j)
-                (void)mbar_wait_bounded(bar(kKFull0 + (j & 1)), (j >> 1) & 1);
-            for (int j = issued_v - 2 > 0 ? issued_v - 2 : 0; j < issued_v; ++j)
-                (void)mbar_wait_bounded(bar(kVFull0 + (j & 1)), (j >> 1) & 1);
+            for (int j = issued - 2 > 0 ? issued - 2 : 0; j < issued; ++j)
+                (void)mbar_wait_bounded(bar(full0 + (j & 1)), (j >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {

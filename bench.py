@@ -383,25 +383,30 @@ class OracleBaseline:
         self.q = self.bits(w.q)
         self.bt = w.block_table.numpy()
 
-    def run(self, n_seq=None, n_tok=None):
-        """Returns (GB/s, tokens/s, seconds, sample text)."""
+    def run(self, n_seq=None, n_tok=None, min_seconds=0.0):
+        """Returns (GB/s, tokens/s, seconds, sample text); repeats the pass until
+        min_seconds of wall time have been spent."""
         np, w = self.np, self.w
         seqs = list(range(w.B if n_seq is None else min(w.B, n_seq)))
         units = [(sq, h) for sq in seqs for h in range(w.Hq)]
         ctx = w.context_lens.numpy().copy()
         if n_tok is not None:
             ctx = np.minimum(ctx, n_tok)
-        t = time.perf_counter()
-        st, _ = self.oracle.decode_attn(self.q, self.kc, self.vc, self.bt, ctx, kv_dtype=0,
-                                        scale_mode=2, k_scale_cache=self.ks,
-                                        v_scale_cache=self.vs, units=units, nthreads=self.cores)
-        secs = time.perf_counter() - t
-        assert st == 0
+        passes, secs = 0, 0.0
+        while passes == 0 or secs < min_seconds:
+            t = time.perf_counter()
+            st, _ = self.oracle.decode_attn(self.q, self.kc, self.vc, self.bt, ctx, kv_dtype=0,
+                                            scale_mode=2, k_scale_cache=self.ks,
+                                            v_scale_cache=self.vs, units=units,
+                                            nthreads=self.cores)
+            secs += time.perf_counter() - t
+            assert st == 0
+            passes += 1
         n = int(ctx[seqs].sum())
-        bytes_ = n * w.Hkv * (2 * w.D + 8)
-        sample = (f"{len(seqs)} of {w.B} sequences x all {w.Hq} query heads, {n} context "
-                  f"tokens" + (f" (contexts cut to {n_tok})" if n_tok else ""))
-        return bytes_ / secs / 1e9, len(seqs) / secs, secs, sample
+        bytes_ = n * w.Hkv * (2 * w.D + 8) * passes
+        sample = (f"{passes} pass(es) over {len(seqs)} of {w.B} sequences x all {w.Hq} query "
+                  f"heads, {n} context tokens" + (f" (contexts cut to {n_tok})" if n_tok else ""))
+        return bytes_ / secs / 1e9, len(seqs) * passes / secs, secs, sample
 
 
 def run_reference(args, w, world, rank):
@@ -706,7 +711,7 @@ def main():
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             ob = OracleBaseline(w)
-            gbs, tps, secs, sample = ob.run()
+            gbs, tps, secs, sample = ob.run(min_seconds=10.0)   # ~10 s of host work
             cpu = {"value": gbs, "unit": "GB/s", "tokens_per_s": tps, "cores": ob.cores,
                    "kind": "oracle", "sample": sample + f"; {secs:.2f} s wall"}
         if rank == 0:

@@ -29,7 +29,7 @@ STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
 
 EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
            "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn", "fp8kv_quantize_e4m3",
-           "fp8kv_status_string", "fp8kv_last_warning")
+           "fp8kv_resolve_scales", "fp8kv_status_string", "fp8kv_last_warning")
 NOALLOC_DECODE_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_prefill_attn.restype = i32
         L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
         L.fp8kv_quantize_e4m3.restype = i32
+        FP = ctypes.POINTER(f32)
+        L.fp8kv_resolve_scales.argtypes = [i32, i32, i32, FP, FP, f32, f32, FP, FP, FP, FP]
+        L.fp8kv_resolve_scales.restype = i32
         L.fp8kv_status_string.argtypes = [i32]
         L.fp8kv_status_string.restype = ctypes.c_char_p
         L.fp8kv_last_warning.argtypes = []
@@ -270,3 +273,41 @@ def quantize_e4m3(x, scale=1.0, out=None, stream=None):
     st = lib().fp8kv_quantize_e4m3(_ptr(x), float(scale), _ptr(out), x.numel(), _stream(stream))
     _raise(st, "quantize_e4m3")
     return out
+
+
+def _floats(x):
+    if x is None:
+        return []
+    if isinstance(x, torch.Tensor):
+        return [float(e) for e in x.detach().cpu().reshape(-1).tolist()]
+    if isinstance(x, (int, float)):
+        return [float(x)]
+    return [float(e) for e in x]
+
+
+def resolve_scales(kv_dtype, scale_mode, k_loaded=None, v_loaded=None, q_loaded=-1.0,
+                   prob_loaded=-1.0):
+    """Scales to use from what a checkpoint loader found; -1.0 (any negative
+    value) means "not loaded".  k_loaded / v_loaded: one float (per-tensor) or a
+    sequence of Hkv floats (per-head); unused for per-token-head and bf16 caches.
+    Returns (k_scales, v_scales, q_scale, prob_scale) with k/v as lists (None
+    where the mode has no per-tensor scale).  Host-only (no GPU needed); the
+    rules are those of fp8kv_resolve_scales in include/fp8kv.h."""
+    per_tensor_like = kv_dtype == KV_E4M3 and scale_mode in (SCALE_PER_TENSOR, SCALE_PER_HEAD)
+    if per_tensor_like:
+        ks, vs = _floats(k_loaded), _floats(v_loaded)
+        if len(ks) != len(vs):
+            raise ValueError("k_loaded and v_loaded differ in length")
+    else:
+        ks = vs = []
+    n = len(ks)
+    FA = ctypes.c_float * max(n, 1)
+    kin, vin, kout, vout = FA(*ks), FA(*vs), FA(), FA()
+    q, pr = ctypes.c_float(), ctypes.c_float()
+    st = lib().fp8kv_resolve_scales(kv_dtype, scale_mode, n, kin, vin, float(q_loaded),
+                                    float(prob_loaded), kout, vout, ctypes.byref(q),
+                                    ctypes.byref(pr))
+    _raise(st, "resolve_scales")
+    if not per_tensor_like:
+        return None, None, q.value, pr.value
+    return list(kout[:n]), list(vout[:n]), q.value, pr.value

@@ -169,6 +169,49 @@ const char* fp8kv_status_string(int status) {
 
 const char* fp8kv_last_warning(void) { return g_warning.c_str(); }
 
+int fp8kv_resolve_scales(int kv_dtype, int scale_mode, int n, const float* k_loaded,
+                         const float* v_loaded, float q_loaded, float prob_loaded,
+                         float* k_out, float* v_out, float* q_out, float* prob_out) {
+    g_warning.clear();
+    if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
+    if (scale_mode < FP8KV_SCALE_PER_TENSOR || scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD)
+        return FP8KV_ERR_INVALID;
+    if (!q_out || !prob_out || q_loaded != q_loaded || prob_loaded != prob_loaded)
+        return FP8KV_ERR_INVALID;
+    const bool quantized = kv_dtype == FP8KV_KV_E4M3;
+    if (!quantized || scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) {
+        // nothing per-tensor to resolve; q / prob are dropped for these caches
+        *q_out = 1.0f;
+        *prob_out = 1.0f;
+        return FP8KV_OK;
+    }
+    if (n < 1 || (scale_mode == FP8KV_SCALE_PER_TENSOR && n != 1)) return FP8KV_ERR_INVALID;
+    if (!k_loaded || !v_loaded || !k_out || !v_out) return FP8KV_ERR_INVALID;
+    for (int i = 0; i < n; ++i) {
+        const float k = k_loaded[i], v = v_loaded[i];
+        if (k != k || v != v) return FP8KV_ERR_INVALID;
+        const bool both_loaded = k > 0.0f && v > 0.0f, none_loaded = k < 0.0f && v < 0.0f;
+        if (!both_loaded && !none_loaded && !(k > 0.0f)) return FP8KV_ERR_INVALID;
+    }
+    for (int i = 0; i < n; ++i) {
+        const float k = k_loaded[i], v = v_loaded[i];
+        if (k > 0.0f && v > 0.0f) {
+            k_out[i] = k;
+            v_out[i] = v;
+        } else if (k < 0.0f && v < 0.0f) {
+            k_out[i] = 1.0f;
+            v_out[i] = 1.0f;
+        } else {
+            k_out[i] = v_out[i] = k > v ? k : v;
+        }
+    }
+    *q_out = q_loaded > 0.0f ? q_loaded : 1.0f;
+    *prob_out = prob_loaded > 0.0f ? prob_loaded : 1.0f;
+    if (*q_out == 1.0f || *prob_out == 1.0f)
+        g_warning = "fp8 attention with uncalibrated q_scale and/or prob_scale of 1.0";
+    return FP8KV_OK;
+}
+
 int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T,
                          int Hkv, int D, void* k_cache, void* v_cache, int64_t num_blocks,
                          int kv_dtype, int scale_mode, const float* k_scale, const float* v_scale,

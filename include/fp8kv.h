@@ -232,6 +232,40 @@ int fp8kv_paged_decode_attn_noalloc(const void* q, const void* k_cache, const vo
                                     float softmax_scale, int window, int num_splits, void* out,
                                     int out_dtype, int32_t* err_flag, void* cuda_stream);
 
+/*
+ * fp8kv_resolve_scales -- turn the scales a checkpoint loader found (or did
+ * not find) into the scales the cache writer and the attention calls take.
+ * Host-only: every array here is HOST memory, no GPU is touched.  [KVQ]
+ * "BaseKVCacheMethod" (every scale starts at the sentinel -1.0, "not loaded"),
+ * "Per-Token-Head vs Per-Tensor 양자화" (which scales each mode uses),
+ * "Q/Prob 스케일과 FP8 Attention" (q_scale fallback and the uncalibrated
+ * warning) and "스케일 통합 로직" (a lone kv_scale serves both K and V).
+ *
+ *   kv_dtype, scale_mode  the cache the scales are for.
+ *   k_loaded, v_loaded    host float [n]: the loaded values, -1.0 (or any
+ *                  negative value) where nothing was loaded.  n = 1 for
+ *                  PER_TENSOR, Hkv for PER_HEAD; ignored (may be NULL) for
+ *                  PER_TOKEN_HEAD and for a bf16 cache.
+ *   q_loaded, prob_loaded  loaded q / prob scales, negative = not loaded.
+ *   k_out, v_out   host float [n]: resolved K/V scales (written for
+ *                  PER_TENSOR and PER_HEAD only).
+ *   q_out, prob_out  host float: resolved q / prob scales.
+ * Rules, per element i (PER_TENSOR and PER_HEAD on an e4m3 cache):
+ *   both k and v > 0  -> used as loaded;
+ *   both < 0          -> 1.0 each (the uncalibrated default);
+ *   otherwise         -> one scale was loaded for both: k must be > 0
+ *                        (else FP8KV_ERR_INVALID) and k_out = v_out = max(k, v).
+ * PER_TOKEN_HEAD and bf16 caches: the writer computes (or needs) no per-tensor
+ * scale; q_out = prob_out = 1.0.  Otherwise q_out = q_loaded if > 0 else 1.0,
+ * and the same for prob.  An e4m3 cache whose resolved q or prob scale is 1.0
+ * sets fp8kv_last_warning().  NaN anywhere returns FP8KV_ERR_INVALID; nothing
+ * is written on error.  The FNUZ (x2) adjustment of [KVQ] is for AMD GPUs and
+ * is not applied.
+ */
+int fp8kv_resolve_scales(int kv_dtype, int scale_mode, int n, const float* k_loaded,
+                         const float* v_loaded, float q_loaded, float prob_loaded,
+                         float* k_out, float* v_out, float* q_out, float* prob_out);
+
 /* Human-readable name of a status code (static string). */
 const char* fp8kv_status_string(int status);
 

@@ -3,9 +3,11 @@
 One step = the decode step of one attention layer of the Llama-3.1-8B-shaped
 workload under load: 8 sequences, contexts uniform in [18000, 22000], 32 query /
 8 KV heads, head_dim 128, page 16 with a shuffled page table, per-token-head
-e4m3 scales, 1% of (head, channel) pairs scaled x20.  Each step writes the 8 new
-tokens into the cache (kv_cache_write) and runs paged_decode_attn (+ split_merge)
-over all keys.  The same step on a bf16 cache is the in-run comparison.
+e4m3 scales, 1% of (head, channel) pairs scaled x20.  Each step stores the 8 new
+tokens into the cache and attends over all keys in one decode_step call (the
+attention kernel stores the new tokens itself, + split_merge); the same work as
+kv_cache_write followed by paged_decode_attn, which is timed beside it.  The same
+step on a bf16 cache is the in-run comparison.
 
 value = algorithmic HBM bytes of a step / step time (GB/s), with the cache
 resident in HBM; e2e = the same bytes over a step that also copies its inputs
@@ -252,7 +254,7 @@ def run_ours(args, dev, w, world, rank):
         splits, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, mbs, 0, args.splits)
         ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
         out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-        launches_per_step[name] = 3          # cache write, decode, split_merge
+        launches_per_step[name] = 2          # decode (stores the new tokens), split_merge
         d_b, w_b = step_bytes(w, 1 if kv_dtype == fk.KV_E4M3 else 2, kv_dtype == fk.KV_E4M3)
         dec_bytes[name] = d_b
 
@@ -267,18 +269,27 @@ def run_ours(args, dev, w, world, rank):
                                  k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=out,
                                  num_splits=args.splits, err_flag=err)
 
-        def step(i):
+        def split_step(i):
             write(i)
             decode(i)
 
+        def step(i, q_in=q, k_in=kn, v_in=vn, cl_in=cl, out_t=out):
+            kc, vc, ks, vs = caches[i % args.rotations]
+            fk.decode_step(q_in, k_in, v_in, kc, vc, bt, cl_in, kv_dtype=kv_dtype,
+                           scale_mode=mode, k_scale_cache=ks, v_scale_cache=vs, workspace=ws,
+                           out=out_t, num_splits=args.splits, err_flag=err)
+
         with torch.cuda.stream(cap):
             for i in range(args.warmup):             # eager warm-up (also first-call setup)
+                split_step(i)
                 step(i)
         torch.cuda.synchronize(dev)
         graphs = _capture_steps(step, K, per_graph, cap)
+        sgraph = _capture_steps(split_step, K, per_graph, cap)
         dgraph = _capture_steps(decode, K, per_graph, cap)
         for _ in range(max(1, args.warmup // per_graph)):
             graphs[0].replay()
+            sgraph[0].replay()
             dgraph[0].replay()
         torch.cuda.synchronize(dev)
 
@@ -295,17 +306,24 @@ def run_ours(args, dev, w, world, rank):
         clocks = sampler.stop() if sampler else None
         secs = t0.elapsed_time(t1) / 1e3
 
-        # the decode call alone (split kernel + split_merge), same caches
+        # the decode call alone (split kernel + split_merge), same caches, and the
+        # unfused step (kv_cache_write, then paged_decode_attn)
         with torch.cuda.stream(cap):
             t0.record(cap)
             _replay_steps(dgraph, K, cap)
             t1.record(cap)
         torch.cuda.synchronize(dev)
         dec_ms = t0.elapsed_time(t1) / K
+        with torch.cuda.stream(cap):
+            t0.record(cap)
+            _replay_steps(sgraph, K, cap)
+            t1.record(cap)
+        torch.cuda.synchronize(dev)
+        split_ms = t0.elapsed_time(t1) / K
         gbs, tok_s, tmax = aggregate(d_b + w_b, w.B, secs, K)
         results[name] = {"gbs": gbs, "tokens_per_s": tok_s, "ms_per_step": tmax / K * 1e3,
-                         "decode_ms": dec_ms, "num_splits": splits, "clocks": clocks,
-                         "secs": tmax}
+                         "decode_ms": dec_ms, "split_step_ms": split_ms, "num_splits": splits,
+                         "clocks": clocks, "secs": tmax}
         if int(err.item()) != 0:
             raise RuntimeError(f"device error flag {int(err.item())} during the {name} run")
 
@@ -316,17 +334,13 @@ def run_ours(args, dev, w, world, rank):
             # and the output goes to pinned host memory: the write and decode kernels
             # read and write them directly over the host link (no staging copies)
             hq, hk, hv = w.q.pin_memory(), w.k_new.pin_memory(), w.v_new.pin_memory()
-            hs, hc = w.new_slots.pin_memory(), w.context_lens.pin_memory()
+            hc = w.context_lens.pin_memory()
             hout = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32).pin_memory()
-            h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hc))
+            h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hc))
             d2h = hout.numel() * hout.element_size()
 
             def e2e_step(i):
-                write(i, k_in=hk, v_in=hv, s_in=hs)
-                kc, vc, ks, vs = caches[i % args.rotations]
-                fk.paged_decode_attn(hq, kc, vc, bt, hc, kv_dtype=kv_dtype, scale_mode=mode,
-                                     k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=hout,
-                                     num_splits=args.splits, err_flag=err)
+                step(i, q_in=hq, k_in=hk, v_in=hv, cl_in=hc, out_t=hout)
 
             with torch.cuda.stream(cap):
                 for i in range(3):
@@ -346,12 +360,12 @@ def run_ours(args, dev, w, world, rank):
             e_gbs, e_tok, _ = aggregate(d_b + w_b, w.B, e_secs, K)
             results["e2e"] = {"value": e_gbs, "unit": "GB/s", "tokens_per_s": e_tok,
                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                              "how": "each step: cache write and decode reading q, new K/V, "
-                                     "slots and lengths from pinned host memory and writing the "
-                                     "output to pinned host memory (kernel loads/stores over the "
-                                     "host link); steps replayed as CUDA graphs"}
+                              "how": "each step: decode_step reading q, new K/V and lengths "
+                                     "from pinned host memory and writing the output to pinned "
+                                     "host memory (kernel loads/stores over the host link); steps "
+                                     "replayed as CUDA graphs"}
             del egraphs
-        del graphs, dgraph, caches
+        del graphs, sgraph, dgraph, caches
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
     return results, dec_bytes, launches_per_step
@@ -701,7 +715,7 @@ def main():
         if rank == 0:
             print(json.dumps({"only": args.only, "splits": r["num_splits"],
                               "step_gbs": r["gbs"], "ms_per_step": r["ms_per_step"],
-                              "decode_ms": r["decode_ms"],
+                              "decode_ms": r["decode_ms"], "split_step_ms": r["split_step_ms"],
                               "decode_gbs": dec_bytes[args.only] / r["decode_ms"] / 1e6,
                               "tokens_per_s": r["tokens_per_s"], "clocks": r["clocks"]}),
                   flush=True)

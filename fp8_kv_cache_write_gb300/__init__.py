@@ -28,7 +28,7 @@ STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -6: "FP8KV_ERR_BAD_INDEX"}
 
 EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
-           "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn", "fp8kv_quantize_e4m3",
+           "fp8kv_decode_step", "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn", "fp8kv_quantize_e4m3",
            "fp8kv_resolve_scales", "fp8kv_status_string", "fp8kv_last_warning")
 NOALLOC_DECODE_SCRATCH_BYTES = 8 << 20
 
@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_paged_decode_attn.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
                                               i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
         L.fp8kv_paged_decode_attn.restype = i32
+        L.fp8kv_decode_step.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
+                                        i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
+        L.fp8kv_decode_step.restype = i32
         L.fp8kv_paged_decode_attn_noalloc.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P,
                                                       i32, i32, i32, i32, i64, f32, i32, i32, P,
                                                       i32, P, P]
@@ -193,6 +196,51 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
         out_dtype, _ptr(err_flag), _stream(stream))
     _raise(st, "paged_decode_attn")
+    return out
+
+
+def decode_step(q, k_new, v_new, k_cache, v_cache, block_table, context_lens, *, kv_dtype,
+                scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None, k_scale_cache=None,
+                v_scale_cache=None, softmax_scale=None, window=0, num_splits=0, workspace=None,
+                out=None, out_dtype=OUT_F32, err_flag=None, stream=None):
+    """One decode step in one call: stores the new token k_new / v_new [B][Hkv][D]
+    (bf16) of every sequence at position context_lens[b] - 1 of its page table
+    (quantized as kv_cache_write does), then attends q [B][Hq][D] over all its
+    keys.  Returns out [B][Hq][D].  See fp8kv_decode_step."""
+    _check(q, "q", torch.bfloat16, pinned_ok=True)
+    _check(k_new, "k_new", torch.bfloat16, pinned_ok=True)
+    _check(v_new, "v_new", torch.bfloat16, pinned_ok=True)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
+    _check(block_table, "block_table", torch.int32)
+    _check(context_lens, "context_lens", torch.int32, pinned_ok=True)
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
+                 ("v_scale_cache", v_scale_cache)):
+        _check(t, n, torch.float32)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError(f"k_new / v_new: expected shape {(B, Hkv, D)}")
+    mbs = block_table.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    splits, ws_bytes = decode_plan(B, Hq, Hkv, D, mbs, window, num_splits)
+    if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size()
+                         < ws_bytes):
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=k_cache.device)
+    if out is None:
+        out = torch.empty(B, Hq, D, device=k_cache.device,
+                          dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
+    _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+           pinned_ok=True)
+    st = lib().fp8kv_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), kv_dtype, scale_mode,
+        _ptr(k_scale), _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache),
+        _ptr(block_table), mbs, _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0],
+        float(softmax_scale), int(window), int(num_splits), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
+        out_dtype, _ptr(err_flag), _stream(stream))
+    _raise(st, "decode_step")
     return out
 
 

@@ -270,15 +270,20 @@ int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int
     return FP8KV_OK;
 }
 
-int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
-                            int kv_dtype, int scale_mode, const float* k_scale,
-                            const float* v_scale, const float* k_scale_cache,
-                            const float* v_scale_cache, const int32_t* block_table,
-                            int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
-                            int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
-                            int num_splits, void* workspace, size_t workspace_bytes, void* out,
-                            int out_dtype, int32_t* err_flag, void* cuda_stream) {
-    g_warning.clear();
+}  // extern "C"
+
+namespace {
+
+// Shared body of fp8kv_paged_decode_attn and fp8kv_decode_step (k_new / v_new
+// non-null: the split kernel stores the new tokens itself).
+int paged_decode(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                 const void* v_cache, int kv_dtype, int scale_mode, const float* k_scale,
+                 const float* v_scale, const float* k_scale_cache, const float* v_scale_cache,
+                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* context_lens,
+                 int B, int Hq, int Hkv, int D, int64_t num_blocks, float softmax_scale,
+                 int window, int num_splits, void* workspace, size_t workspace_bytes, void* out,
+                 int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    const bool fused = k_new != nullptr || v_new != nullptr;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || window < 0 || num_splits < 0 ||
         max_blocks_per_seq < 0 || num_blocks < 0)
         return FP8KV_ERR_INVALID;
@@ -308,6 +313,8 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
         return FP8KV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(out, 4))
+        return FP8KV_ERR_INVALID;
+    if (fused && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)))
         return FP8KV_ERR_INVALID;
     if (kv_dtype == FP8KV_KV_E4M3) {
         if (scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) {
@@ -359,9 +366,52 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
     p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
     p.err = err_flag;
-    cudaError_t e =
-        launch_paged_decode(p, kmap, vmap, D, kv_dtype, static_cast<cudaStream_t>(cuda_stream));
+    if (fused) {
+        p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+        p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+        p.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+        p.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
+    }
+    cudaError_t e = launch_paged_decode(p, kmap, vmap, D, kv_dtype, fused,
+                                        static_cast<cudaStream_t>(cuda_stream));
     return e == cudaSuccess ? FP8KV_OK : FP8KV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                            int kv_dtype, int scale_mode, const float* k_scale,
+                            const float* v_scale, const float* k_scale_cache,
+                            const float* v_scale_cache, const int32_t* block_table,
+                            int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
+                            int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
+                            int num_splits, void* workspace, size_t workspace_bytes, void* out,
+                            int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    g_warning.clear();
+    return paged_decode(q, nullptr, nullptr, k_cache, v_cache, kv_dtype, scale_mode, k_scale,
+                        v_scale, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
+                        context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, window,
+                        num_splits, workspace, workspace_bytes, out, out_dtype, err_flag,
+                        cuda_stream);
+}
+
+int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, int kv_dtype, int scale_mode, const float* k_scale,
+                      const float* v_scale, float* k_scale_cache, float* v_scale_cache,
+                      const int32_t* block_table, int max_blocks_per_seq,
+                      const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                      int64_t num_blocks, float softmax_scale, int window, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* out, int out_dtype,
+                      int32_t* err_flag, void* cuda_stream) {
+    g_warning.clear();
+    if (!k_new || !v_new) return FP8KV_ERR_INVALID;
+    return paged_decode(q, k_new, v_new, k_cache, v_cache, kv_dtype, scale_mode, k_scale,
+                        v_scale, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
+                        context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, window,
+                        num_splits, workspace, workspace_bytes, out, out_dtype, err_flag,
+                        cuda_stream);
 }
 
 int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,

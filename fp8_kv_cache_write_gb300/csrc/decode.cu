@@ -75,9 +75,22 @@ struct Cfg {
     static constexpr int kOffBars = kWarps * kWarpSmem + kWarps * kStages * kPPI * kScaleB;
     static constexpr int kOffSegs = kOffBars + kWarps * kStages * 8;
     static constexpr int kOffShare = kOffSegs + kWarps * kMaxSeg * kSegInts * 4;  // [warp][resume, end]
-    static constexpr int kSmem = 1024 + kOffShare + kWarps * 16;
+    static constexpr int kOffCtx = kOffShare + kWarps * 16;    // [warp][32] context lengths
+    static constexpr int kSmem = 1024 + kOffCtx + kWarps * 128;
+    // fused step only, after the above: per warp the new token's K row, V row
+    // (as stored in the cache) and its two per-token-head scales
+    static constexpr int kOffNew = kOffCtx + kWarps * 128;
+    static constexpr int kNewB = (2 * kRowB + 8 + 15) / 16 * 16;
+    static constexpr int kSmemFused = kSmem + kWarps * kNewB;
     static_assert(kSegs * kKPerSeg == kKSteps, "k-step split");
 };
+
+// An unsigned type of N bytes (2, 4, 8 or 16) for one lane's share of a row.
+template <int N> struct LaneBytes;
+template <> struct LaneBytes<2> { using T = uint16_t; };
+template <> struct LaneBytes<4> { using T = uint32_t; };
+template <> struct LaneBytes<8> { using T = uint2; };
+template <> struct LaneBytes<16> { using T = uint4; };
 
 // The fragment permutation: M row g <-> token pi(g) (and pi(g)+8); lane group g
 // reads V d-chunk pi(g).  pi = 0 4 1 5 2 6 3 7.
@@ -129,11 +142,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Visible page range of sequence b: positions [lo, ctx) live in pages
-// [p_lo, p_hi).  Clamps a context longer than the page table (and reports it).
-__device__ __forceinline__ void visible(const DecodeParams& p, int b, int& lo, int& ctx, int& p_lo,
-                                        int& p_hi, bool report_errors) {
-    ctx = p.context_lens[b];
+// Visible page range of a sequence with context length c: positions [lo, ctx)
+// live in pages [p_lo, p_hi).  Clamps a context longer than the page table (and
+// reports it).
+__device__ __forceinline__ void visible_of(const DecodeParams& p, int c, int& lo, int& ctx,
+                                           int& p_lo, int& p_hi, bool report_errors) {
+    ctx = c;
     if (ctx < 0) ctx = 0;
     if (ctx > p.max_blocks_per_seq * kPage) {
         if (report_errors) report(p.err, FP8KV_ERR_BAD_INDEX);
@@ -142,6 +156,11 @@ __device__ __forceinline__ void visible(const DecodeParams& p, int b, int& lo, i
     lo = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
     p_lo = lo / kPage;
     p_hi = (ctx + kPage - 1) / kPage;
+}
+
+__device__ __forceinline__ void visible(const DecodeParams& p, int b, int& lo, int& ctx, int& p_lo,
+                                        int& p_hi, bool report_errors) {
+    visible_of(p, p.context_lens[b], lo, ctx, p_lo, p_hi, report_errors);
 }
 
 // Visible pages of sequence b (0 when its context is empty).
@@ -159,8 +178,110 @@ __device__ __forceinline__ void store_out(void* out, int out_bf16, size_t idx, f
         reinterpret_cast<float*>(out)[idx] = v;
 }
 
-// D <= 128 keeps 3 CTAs (12 warps) resident per SM: 168 registers at most
+// The new token of unit (b, h) of a fused decode step: lane l quantizes elements
+// [l D/32, (l+1) D/32) of k_new / v_new exactly as kv_cache_write does
+// (per-token-head scale fp32(max|x| / 448) over the row, codes
+// e4m3_rn_satfinite(fp32(x / s)), a zero scale storing code 0; the bf16 cache
+// takes the values as they are), stores them at position ctx - 1 of the
+// sequence's page table (row bt_row[(ctx-1)/16] * Hkv + h, offset (ctx-1) % 16)
+// and keeps row, row and scales in `area` ([K row][V row][s_k, s_v]) for the
+// patch of the staged page.  Kept out of line: it runs once per unit and would
+// otherwise raise the register pressure of the streaming loop.
 template <int D, bool BF16, bool PER_TOKEN>
+__device__ __noinline__ bool store_new_token_row(const int32_t* bt_row, int64_t num_blocks, int Hkv,
+                                                 const __nv_bfloat16* k_new,
+                                                 const __nv_bfloat16* v_new, uint8_t* k_cache,
+                                                 uint8_t* v_cache, float* k_scale_cache,
+                                                 float* v_scale_cache, int32_t* err, uint8_t* area,
+                                                 int lane, int b, int h, int ctx, float ksc,
+                                                 float vsc) {
+    using C = Cfg<D, BF16>;
+    constexpr int kNE = D / 32;                       // elements per lane
+    constexpr int kLB = C::kRowB / 32;                // stored bytes per lane
+    using LaneT = typename LaneBytes<kLB>::T;
+    const int pos = ctx - 1;
+    const int blk = bt_row[pos / kPage];
+    const bool ok = blk >= 0 && static_cast<int64_t>(blk) < num_blocks;
+    const size_t src = (static_cast<size_t>(b) * Hkv + h) * D + lane * kNE;
+    LaneT kst, vst;
+    float sk = 1.f, sv = 1.f;
+    if constexpr (BF16) {
+        kst = *reinterpret_cast<const LaneT*>(k_new + src);
+        vst = *reinterpret_cast<const LaneT*>(v_new + src);
+    } else {
+        using RawT = typename LaneBytes<2 * kNE>::T;
+        const RawT kr = *reinterpret_cast<const RawT*>(k_new + src);
+        const RawT vr = *reinterpret_cast<const RawT*>(v_new + src);
+        uint32_t kw[kNE / 2], vw[kNE / 2];
+        memcpy(kw, &kr, 2 * kNE);
+        memcpy(vw, &vr, 2 * kNE);
+        float kf[kNE], vf[kNE];
+#pragma unroll
+        for (int i = 0; i < kNE / 2; ++i) {
+            kf[2 * i] = bf16_bits_to_float(kw[i] & 0xffffu);
+            kf[2 * i + 1] = bf16_bits_to_float(kw[i] >> 16);
+            vf[2 * i] = bf16_bits_to_float(vw[i] & 0xffffu);
+            vf[2 * i + 1] = bf16_bits_to_float(vw[i] >> 16);
+        }
+        if constexpr (PER_TOKEN) {
+            float ka = 0.f, va = 0.f;
+#pragma unroll
+            for (int i = 0; i < kNE; ++i) {
+                ka = fmaxf(ka, fabsf(kf[i]));
+                va = fmaxf(va, fabsf(vf[i]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, off));
+                va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, off));
+            }
+            sk = __fdiv_rn(ka, 448.0f);
+            sv = __fdiv_rn(va, 448.0f);
+        } else {
+            sk = ksc;
+            sv = vsc;
+        }
+        uint16_t kc[kNE / 2], vc[kNE / 2];
+#pragma unroll
+        for (int i = 0; i < kNE / 2; ++i) {
+            kc[i] = sk != 0.0f ? e4m3x2_from_f32(__fdiv_rn(kf[2 * i], sk),
+                                                 __fdiv_rn(kf[2 * i + 1], sk))
+                               : uint16_t{0};
+            vc[i] = sv != 0.0f ? e4m3x2_from_f32(__fdiv_rn(vf[2 * i], sv),
+                                                 __fdiv_rn(vf[2 * i + 1], sv))
+                               : uint16_t{0};
+        }
+        memcpy(&kst, kc, kLB);
+        memcpy(&vst, vc, kLB);
+    }
+    *reinterpret_cast<LaneT*>(area + lane * kLB) = kst;
+    *reinterpret_cast<LaneT*>(area + C::kRowB + lane * kLB) = vst;
+    if (lane == 0) {
+        reinterpret_cast<float*>(area + 2 * C::kRowB)[0] = sk;
+        reinterpret_cast<float*>(area + 2 * C::kRowB)[1] = sv;
+    }
+    if (ok) {
+        const size_t row = (static_cast<size_t>(blk) * Hkv + h) * kPage + pos % kPage;
+        *reinterpret_cast<LaneT*>(k_cache + row * C::kRowB + lane * kLB) = kst;
+        *reinterpret_cast<LaneT*>(v_cache + row * C::kRowB + lane * kLB) = vst;
+        if constexpr (PER_TOKEN) {
+            if (lane == 0) {
+                k_scale_cache[row] = sk;
+                v_scale_cache[row] = sv;
+            }
+        }
+    } else if (lane == 0) {
+        report(err, FP8KV_ERR_BAD_INDEX);
+    }
+    __syncwarp();
+    return ok;
+}
+
+// D <= 128 keeps 3 CTAs (12 warps) resident per SM: 168 registers at most.
+// FUSED: a decode step -- the kernel also stores every sequence's new token
+// (k_new / v_new at position ctx - 1) and starts streaming the older pages
+// before the preceding kernel has finished.
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -179,7 +300,9 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     // The set-up below -- shares, segments, page-table rows -- reads only
     // context_lens, block_table and the constant scales, which must be complete
     // before the preceding kernel of the stream starts; it overlaps that kernel's
-    // tail.  The wait for it comes before the first cache load or workspace write.
+    // tail.  The wait for it comes before the first cache load or workspace write
+    // (FUSED: before the first read of q, k_new or v_new and the first write; the
+    // cache pages, complete before the preceding kernel started, stream first).
 
     uint8_t* ring = smem + warp * C::kWarpSmem;
     uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
@@ -191,13 +314,17 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
 
     // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
     //      tiles; every warp is an independent worker (no block-wide barrier)
+    // the first 32 context lengths are read once and kept in shared memory
+    volatile int* ctx32 = reinterpret_cast<volatile int*>(smem + C::kOffCtx) + 32 * warp;
     long long W = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
         long long w = 0;
         if (bb < p.B) {
+            const int craw = p.context_lens[bb];
+            if (b0 == 0) ctx32[lane] = craw;
             int lo_, ctx_, plo_, phi_;
-            visible(p, bb, lo_, ctx_, plo_, phi_, blockIdx.x == 0 && warp == 0);
+            visible_of(p, craw, lo_, ctx_, plo_, phi_, blockIdx.x == 0 && warp == 0);
             w = phi_ > plo_ ? static_cast<long long>(phi_ - plo_) * p.Hkv : 0;
         }
 #pragma unroll
@@ -236,7 +363,9 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int b0 = 0; b0 < p.B && t < t1 && k < kMaxSeg; b0 += 32) {
             const int bb = b0 + lane;
             int lo_ = 0, ctx_ = 0, plo_ = 0, phi_ = 0;
-            if (bb < p.B) visible(p, bb, lo_, ctx_, plo_, phi_, false);
+            if (bb < p.B)
+                visible_of(p, b0 == 0 ? ctx32[lane] : p.context_lens[bb], lo_, ctx_, plo_, phi_,
+                           false);
             const int n = phi_ > plo_ ? phi_ - plo_ : 0;
             const long long w = static_cast<long long>(n) * p.Hkv;
             long long incl = w;
@@ -440,6 +569,39 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         }
     };
 
+    // ---- FUSED: the new token of unit (b, h) sits at position ctx - 1 on the
+    //      unit's last page, which exactly one warp's share holds.  That warp
+    //      stores it (store_new_token_row) and keeps it in its shared-memory
+    //      area to patch the staged copy of the page, which may have been taken
+    //      before the store.
+    constexpr int kLB = C::kRowB / 32;                // stored bytes per lane
+    using LaneT = typename LaneBytes<kLB>::T;
+    uint8_t* newtok = smem + C::kOffNew + warp * C::kNewB;
+    auto store_new_token = [&](int b, int h, int ctx, float ksc, float vsc) -> bool {
+        return store_new_token_row<D, BF16, PER_TOKEN>(
+            p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq, p.num_blocks, p.Hkv,
+            p.k_new, p.v_new, p.k_cache, p.v_cache, const_cast<float*>(p.k_scale_cache),
+            const_cast<float*>(p.v_scale_cache), p.err, newtok, lane, b, h, ctx, ksc, vsc);
+    };
+    // overwrite token row r of page k of stage st with the stored new token
+    auto patch_new_token = [&](uint8_t* stage, int st, int k, int r) {
+        const int off = chunk_off<C::kRowB>(r, (lane * kLB) >> 4) + ((lane * kLB) & 15);
+        *reinterpret_cast<LaneT*>(stage + k * C::kTileB + off) =
+            *reinterpret_cast<const LaneT*>(newtok + lane * kLB);
+        *reinterpret_cast<LaneT*>(stage + (PPI + k) * C::kTileB + off) =
+            *reinterpret_cast<const LaneT*>(newtok + C::kRowB + lane * kLB);
+        if constexpr (PER_TOKEN) {
+            if (lane == 0) {
+                float* sk = reinterpret_cast<float*>(scl + (st * PPI + k) * C::kScaleB);
+                sk[r] = reinterpret_cast<const float*>(newtok + 2 * C::kRowB)[0];
+                sk[16 + r] = reinterpret_cast<const float*>(newtok + 2 * C::kRowB)[1];
+            }
+        }
+        // the slot is refilled by TMA later: order these generic writes first
+        fence_proxy_async();
+        __syncwarp();
+    };
+
     // ---- the warp's page stream: issue side runs kStages groups ahead of the
     //      consume side; both walk the same segments in order
     int jring = 0;                          // groups consumed so far (ring phase)
@@ -535,8 +697,9 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int si = 0; si < nseg; ++si)
             total_groups += (seg[kSegInts * si + 3] - seg[kSegInts * si + 2] + PPI - 1) / PPI;
         const int pre = total_groups < C::kStages ? total_groups : C::kStages;
-        pdl_wait();                       // the preceding kernel's results are visible
+        if constexpr (!FUSED) pdl_wait();   // the preceding kernel's results are visible
         for (int q = 0; q < pre; ++q) issue_next();
+        if constexpr (FUSED) pdl_wait();
 
         int consumed = 0;
         for (int si = 0; si < nseg && !timed_out; ++si) {
@@ -544,6 +707,13 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
             const int pb = seg[kSegInts * si + 2], pe = seg[kSegInts * si + 3];
             const int lo = seg[kSegInts * si + 5], ctx = seg[kSegInts * si + 6];
             load_q(b, seg[kSegInts * si + 1], __int_as_float(seg[kSegInts * si + 7]));
+            bool new_tok = false;           // this segment holds the unit's new token
+            if constexpr (FUSED) {
+                if ((seg[kSegInts * si + 4] & 4) && ctx >= 1)
+                    new_tok = store_new_token(b, seg[kSegInts * si + 1], ctx,
+                                              __int_as_float(seg[kSegInts * si + 7]),
+                                              __int_as_float(seg[kSegInts * si + 8]));
+            }
             reset_state();
             for (int cpg = pb; cpg < pe; cpg += PPI) {
                 const int j = jring + consumed;
@@ -562,6 +732,17 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int k = 0; k < PPI; ++k) {
             bad[k] = (bad_mask >> (st * PPI + k)) & 1u;
             interior[k] = !bad[k] && pos0 + k * kPage >= lo && pos0 + (k + 1) * kPage <= ctx;
+        }
+        if constexpr (FUSED) {
+            // the unit's last page (pe - 1) holds position ctx - 1
+            if (new_tok && cpg + PPI >= pe) {
+                const int kn = pe - 1 - cpg;
+                bool badn = false;
+#pragma unroll
+                for (int k = 0; k < PPI; ++k) badn = k == kn ? bad[k] : badn;
+                if (!badn)
+                    patch_new_token(const_cast<uint8_t*>(stage), st, kn, (ctx - 1) % kPage);
+            }
         }
 
         // ---- S^T = K_page Q^T for each page (rows: tokens tA, tB; cols: heads 2c, 2c+1)
@@ -777,6 +958,10 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvis = vis_pages(p, b);           // context_lens: complete before the chain
     pdl_wait();                                 // the decode kernel's partials are visible
+    // The next kernel may now start its set-up.  Not earlier: a dependent grid
+    // launched while the decode grid still runs takes SM slots as they free up
+    // and spreads itself over several waves.
+    pdl_trigger();
     if (nvis == 0) {
         for (int d = threadIdx.x; d < D; d += blockDim.x)
             store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, 0.f);
@@ -835,18 +1020,19 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     }
 }
 
-template <int D, bool BF16, bool PER_TOKEN>
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          cudaStream_t stream) {
     using C = Cfg<D, BF16>;
-    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN>;
+    constexpr int kSmemBytes = FUSED ? C::kSmemFused : C::kSmem;
+    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED>;
     // opt in to the large dynamic shared-memory size once per device
     static bool attr_done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
@@ -858,7 +1044,7 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_splits);
     cfg.blockDim = dim3(kWarps * 32);
-    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -876,17 +1062,24 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     return cudaLaunchKernelEx(&mcfg, split_merge_kernel<D>, p);
 }
 
-template <int D>
+template <int D, bool FUSED>
 cudaError_t dispatch_dtype(const DecodeParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int kv_dtype, cudaStream_t s) {
-    if (kv_dtype == FP8KV_KV_BF16) return launch_split<D, true, false>(p, kmap, vmap, s);
+    if (kv_dtype == FP8KV_KV_BF16) return launch_split<D, true, false, FUSED>(p, kmap, vmap, s);
     if (p.scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD)
-        return launch_split<D, false, true>(p, kmap, vmap, s);
-    return launch_split<D, false, false>(p, kmap, vmap, s);
+        return launch_split<D, false, true, FUSED>(p, kmap, vmap, s);
+    return launch_split<D, false, false, FUSED>(p, kmap, vmap, s);
+}
+
+template <int D>
+cudaError_t dispatch_fused(const DecodeParams& p, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int kv_dtype, bool fused, cudaStream_t s) {
+    return fused ? dispatch_dtype<D, true>(p, kmap, vmap, kv_dtype, s)
+                 : dispatch_dtype<D, false>(p, kmap, vmap, kv_dtype, s);
 }
 
 template <int D, bool BF16>
-constexpr int smem_of() { return Cfg<D, BF16>::kSmem; }
+constexpr int smem_of() { return Cfg<D, BF16>::kSmemFused; }
 
 }  // namespace
 
@@ -903,12 +1096,12 @@ int decode_ctas_per_sm(int D, int kv_dtype) {
 }
 
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int D, int kv_dtype,
+                                const CUtensorMap& vmap, int D, int kv_dtype, bool fused,
                                 cudaStream_t stream) {
     switch (D) {
-        case 64: return dispatch_dtype<64>(p, kmap, vmap, kv_dtype, stream);
-        case 128: return dispatch_dtype<128>(p, kmap, vmap, kv_dtype, stream);
-        default: return dispatch_dtype<256>(p, kmap, vmap, kv_dtype, stream);
+        case 64: return dispatch_fused<64>(p, kmap, vmap, kv_dtype, fused, stream);
+        case 128: return dispatch_fused<128>(p, kmap, vmap, kv_dtype, fused, stream);
+        default: return dispatch_fused<256>(p, kmap, vmap, kv_dtype, fused, stream);
     }
 }
 

@@ -58,11 +58,18 @@ struct DecodeParams {
     int out_bf16;
     int scale_mode;
     int32_t* err;
+    // fused decode step only (null otherwise): the new token of every sequence,
+    // [B][Hkv][D] bf16, stored at position ctx - 1 by the kernel itself
+    const __nv_bfloat16* k_new;
+    const __nv_bfloat16* v_new;
+    uint8_t* k_cache;
+    uint8_t* v_cache;
 };
 
-// Launches the split kernel and the merge kernel.
+// Launches the split kernel and the merge kernel (fused: the split kernel also
+// stores k_new / v_new).
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int D, int kv_dtype,
+                                const CUtensorMap& vmap, int D, int kv_dtype, bool fused,
                                 cudaStream_t stream);
 
 // Chunked causal prefill on the tcgen05 FP8 tensor cores.  CTA (x, h, b) takes

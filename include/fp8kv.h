@@ -158,6 +158,41 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
                             int out_dtype, int32_t* err_flag, void* cuda_stream);
 
 /*
+ * fp8kv_decode_step -- a whole decode step of one attention layer in one
+ * call: fp8kv_kv_cache_write of every sequence's new token followed by
+ * fp8kv_paged_decode_attn, with the store done inside the attention kernel.
+ * [KVQ] "Per-Token-Head vs Per-Tensor 양자화" (the kernel computes the
+ * per-token-head scales when it stores the cache); [KO] opening paragraph.
+ *
+ *   k_new, v_new   bf16 [B][Hkv][D] (device or pinned host memory): the new
+ *                  token of sequence b, stored at position ctx - 1
+ *                  (ctx = context_lens[b]), i.e. in block
+ *                  block_table[b][(ctx-1) / 16] at offset (ctx-1) % 16, with
+ *                  exactly the codes and scales fp8kv_kv_cache_write would
+ *                  store there (bf16 cache: the values as they are).  A
+ *                  sequence with ctx 0 stores nothing and gets a zero row.
+ *   k_cache, v_cache, k_scale_cache, v_scale_cache  written at those slots.
+ *   Everything else as in fp8kv_paged_decode_attn; the attention sees the new
+ *   token.  A block id outside the cache skips the store and sets
+ *   FP8KV_ERR_BAD_INDEX in err_flag.
+ * Ordering (programmatic stream serialization): besides context_lens,
+ * block_table and k_scale / v_scale, the cache contents other than the slots
+ * this call writes must be complete before the preceding kernel of the stream
+ * starts -- the kernel streams the older pages while that kernel finishes;
+ * q, k_new and v_new are read, and anything is written, only after it has
+ * completed.  In a model the preceding kernel produces q / k_new / v_new and
+ * the cache was written by earlier steps, so this holds.
+ */
+int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, int kv_dtype, int scale_mode, const float* k_scale,
+                      const float* v_scale, float* k_scale_cache, float* v_scale_cache,
+                      const int32_t* block_table, int max_blocks_per_seq,
+                      const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                      int64_t num_blocks, float softmax_scale, int window, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* out, int out_dtype,
+                      int32_t* err_flag, void* cuda_stream);
+
+/*
  * fp8kv_prefill_attn -- chunked causal prefill in FP8 on the tcgen05 tensor
  * cores.  [KO] opening paragraph (FP8 e4m3 attention compute), "커널 및 퓨전
  * 최적화" (query quantization fused into the kernel), "정확도를 위한 2단계 누적"

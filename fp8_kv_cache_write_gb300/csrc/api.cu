@@ -117,8 +117,7 @@ struct Plan {
 // 16 tiles per CTA for the upper bound of the work (B * Hkv * visible pages);
 // an explicit count n asks for about n partitions per (seq, KV head) unit.
 // Workspace: one (m, l, O) slot per (warp, unit) pair a warp can touch, i.e.
-// 4 * num_splits + B * Hkv slots of G query heads, then the first / last worker
-// of every unit.
+// 4 * num_splits + B * Hkv slots of G query heads.
 int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out) {
     int maxvis = max_blocks;
     if (window > 0) {
@@ -143,8 +142,7 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     const int64_t G = Hkv > 0 ? Hq / Hkv : 1;
     const int64_t workers = n * kDecodeWarps;      // every warp is a worker
     out->workspace_bytes = static_cast<size_t>(workers + units) * G *
-                               (static_cast<size_t>(D) + 2) * sizeof(float) +
-                           static_cast<size_t>(units) * 2 * sizeof(int);
+                           (static_cast<size_t>(D) + 2) * sizeof(float);
     return FP8KV_OK;
 }
 
@@ -359,8 +357,6 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
         p.ws_o = ws;
         p.ws_m = ws + rows * D;
         p.ws_l = p.ws_m + rows;
-        p.ws_first = reinterpret_cast<int*>(p.ws_l + rows);
-        p.ws_last = p.ws_first + static_cast<size_t>(B) * Hkv;
     }
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;

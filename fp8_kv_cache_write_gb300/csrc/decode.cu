@@ -314,6 +314,22 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
 
     // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
     //      tiles; every warp is an independent worker (no block-wide barrier)
+    if (lane == 0) {                      // ring barriers (their fences overlap the loads below)
+        for (int s = 0; s < C::kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        mbar_init_fence();
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+    }
+    // the page table's lines reach L2 while the context lengths are read (the
+    // CTAs share the prefetch line by line)
+    if (warp == 0) {
+        const long long lines =
+            (static_cast<long long>(p.B) * p.max_blocks_per_seq * 4 + 127) / 128;
+        const uintptr_t base = reinterpret_cast<uintptr_t>(p.block_table) & ~uintptr_t{127};
+        for (long long ln = blockIdx.x + static_cast<long long>(gridDim.x) * lane; ln < lines;
+             ln += static_cast<long long>(gridDim.x) * 32)
+            prefetch_l2(reinterpret_cast<const void*>(base + ln * 128));
+    }
     // the first 32 context lengths are read once and kept in shared memory
     volatile int* ctx32 = reinterpret_cast<volatile int*>(smem + C::kOffCtx) + 32 * warp;
     long long W = 0;
@@ -339,16 +355,14 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     // [resume, end) of the share lives in shared memory (kept out of registers)
     volatile long long* share = reinterpret_cast<volatile long long*>(smem + C::kOffShare) + 2 * warp;
     if (lane == 0) {
-        share[0] = FP8KV_WORKER * W / n_workers;
-        share[1] = (FP8KV_WORKER + 1) * W / n_workers;
-    }
-    __syncwarp();
-
-    if (lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
-        mbar_init_fence();
-        prefetch_tmap(&kmap);
-        prefetch_tmap(&vmap);
+        // floor(w W / n) for w and w + 1 with one 64-bit division: W = q n + r,
+        // so w W / n = w q + w r / n, and w r < 2^24 (w, r < 4096)
+        const long long q = W / n_workers, r = W - q * n_workers;
+        const long long w = FP8KV_WORKER;
+        share[0] = w * q + static_cast<long long>(static_cast<unsigned>(w * r) /
+                                                  static_cast<unsigned>(n_workers));
+        share[1] = (w + 1) * q + static_cast<long long>(static_cast<unsigned>((w + 1) * r) /
+                                                        static_cast<unsigned>(n_workers));
     }
     __syncwarp();
 
@@ -550,12 +564,6 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                 }
             }
         }
-        // the workers that start and end the unit, for split_merge (a whole unit
-        // records first == last, so the merge leaves its output alone)
-        if (lane == 0) {
-            if (flags & 2) p.ws_first[unit] = static_cast<int>(FP8KV_WORKER);
-            if (flags & 4) p.ws_last[unit] = static_cast<int>(FP8KV_WORKER);
-        }
         if (whole) return;
         if (g == 0) {
             if (head0 < G) {
@@ -669,6 +677,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&bars[st]);
                 const uint32_t base = smem_addr(ring + st * C::kStageB);
+                const uint64_t pol = l2_evict_first();   // pages are read once
                 fence_proxy_async();
                 mbar_arrive_expect_tx(bar, tx);
 #pragma unroll
@@ -677,15 +686,17 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                     const int z = blk[k] * p.Hkv + h_i;
 #pragma unroll
                     for (int box = 0; box < C::kBoxes; ++box) {
-                        tma_load_3d(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0, z, bar);
-                        tma_load_3d(base + (PPI + k) * C::kTileB + box * 2048, &vmap, box * 128, 0,
-                                    z, bar);
+                        tma_load_3d_hint(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0,
+                                         z, bar, pol);
+                        tma_load_3d_hint(base + (PPI + k) * C::kTileB + box * 2048, &vmap,
+                                         box * 128, 0, z, bar, pol);
                     }
                     if constexpr (PER_TOKEN) {
                         const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
-                        bulk_load(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64, bar);
-                        bulk_load(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64,
-                                  bar);
+                        bulk_load_hint(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                                       bar, pol);
+                        bulk_load_hint(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage,
+                                       64, bar, pol);
                     }
                 }
             }
@@ -957,6 +968,34 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     const int unit = b * p.Hkv + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvis = vis_pages(p, b);           // context_lens: complete before the chain
+    // the workers whose shares meet the unit: the decode kernel split the W
+    // tiles of the launch as worker w <- [floor(w W / n), floor((w+1) W / n)),
+    // so tile t belongs to worker floor(((t+1) n - 1) / W)
+    long long first = 0, last = -1;
+    {
+        long long W = 0, base = 0;
+        int nb = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int bb = b0 + lane;
+            const long long w = bb < p.B ? static_cast<long long>(vis_pages(p, bb)) * p.Hkv : 0;
+            long long incl = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (b >= b0 && b < b0 + 32) base = W + __shfl_sync(0xffffffffu, incl - w, b - b0);
+            W += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        nb = nvis;
+        const long long workers = static_cast<long long>(p.num_splits) * kWarps;
+        const long long n = W < workers ? W : workers;
+        if (nb > 0 && n > 0) {
+            const long long t0 = base + static_cast<long long>(h) * nb, t1 = t0 + nb;
+            first = ((t0 + 1) * n - 1) / W;
+            last = (t1 * n - 1) / W;
+        }
+    }
     pdl_wait();                                 // the decode kernel's partials are visible
     // The next kernel may now start its set-up.  Not earlier: a dependent grid
     // launched while the decode grid still runs takes SM slots as they free up
@@ -967,20 +1006,17 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
             store_out<false>(p.out, p.out_bf16, static_cast<size_t>(row) * D + d, 0.f);
         return;
     }
-    // the unit's workers, recorded by them in this call (first == last: one
-    // worker covered the unit whole and wrote the output itself)
-    const int first = p.ws_first[unit], last = p.ws_last[unit];
-    const long long workers = static_cast<long long>(p.num_splits) * kWarps;
-    if (last <= first || first < 0 || last >= workers) return;
+    // first == last: one worker covered the unit whole and wrote the output
+    if (last <= first) return;
     float M = neg_inf(), L = 0.f, acc[kCols];
 #pragma unroll
     for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
     constexpr int kChunk = 8;
-    for (int w0 = first + warp; w0 <= last; w0 += nw * kChunk) {
+    for (long long w0 = first + warp; w0 <= last; w0 += nw * kChunk) {
         float mi[kChunk], li[kChunk], oi[kChunk][kCols];
 #pragma unroll
         for (int q = 0; q < kChunk; ++q) {
-            const int w = w0 + nw * q;
+            const long long w = w0 + nw * q;
             const bool ok = w <= last;
             const size_t sl = (static_cast<size_t>(ok ? w : first) + unit) * G + head;
             mi[q] = ok ? p.ws_m[sl] : neg_inf();

@@ -52,8 +52,6 @@ struct DecodeParams {
     float* ws_m;                 // [4*num_splits + B*Hkv][G] running max (log2 units)
     float* ws_l;                 // [4*num_splits + B*Hkv][G] softmax denominator
     float* ws_o;                 // [4*num_splits + B*Hkv][G][D] unnormalised output
-    int* ws_first;               // [B*Hkv] first worker of a split unit
-    int* ws_last;                // [B*Hkv] last worker of a split unit
     void* out;                   // [B][Hq][D]
     int out_bf16;
     int scale_mode;

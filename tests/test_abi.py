@@ -50,13 +50,12 @@ def test_status_strings(lib):
 
 def test_decode_plan_is_consistent(lib):
     # num_splits = CTAs of the balanced partition (4 worker warps each); one
-    # workspace slot of G query heads x (D + 2) floats per warp plus one per unit,
-    # then the first / last worker of every unit
+    # workspace slot of G query heads x (D + 2) floats per warp plus one per unit
     for B, Hq, Hkv, D, mbs, win in [(8, 32, 8, 128, 1375, 0), (1, 64, 8, 128, 8192, 0),
                                     (32, 64, 8, 64, 2048, 128), (1, 32, 8, 128, 64, 0)]:
         s, ws = fk.decode_plan(B, Hq, Hkv, D, mbs, win)
         assert 1 <= s <= 1024
-        assert ws == (4 * s + B * Hkv) * (Hq // Hkv) * (D + 2) * 4 + B * Hkv * 8
+        assert ws == (4 * s + B * Hkv) * (Hq // Hkv) * (D + 2) * 4
         for req in (1, 2, 7):
             s2, _ = fk.decode_plan(B, Hq, Hkv, D, mbs, win, req)
             assert 1 <= s2 <= min(1024, req * B * Hkv)

@@ -627,6 +627,23 @@ def _extra_prefill(fk, synth, dev, stream, emit):
                   "ms": ms, "tflops": flops / ms / 1e9})
         del kc, vc
         torch.cuda.empty_cache()
+    # the same chunk over a per-token-head e4m3 cache (scales computed at write time)
+    kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    ksc = torch.zeros(w.num_blocks, w.Hkv, 16, dtype=torch.float32, device=dev)
+    vsc = torch.zeros_like(ksc)
+    fk.kv_cache_write(w.k_all.to(dev), w.v_all.to(dev), w.all_slots.to(dev), kc, vc, kv_dtype=E4,
+                      scale_mode=fk.SCALE_PER_TOKEN_HEAD, k_scale_cache=ksc, v_scale_cache=vsc)
+    for two in (False, True):
+        fn = lambda i, two=two: fk.prefill_attn(
+            q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=E4,
+            scale_mode=fk.SCALE_PER_TOKEN_HEAD, k_scale_cache=ksc, v_scale_cache=vsc,
+            two_level=two, out=out)
+        ms = _time_graph(fn, 10, stream)
+        emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": "fp8 per-token-head",
+              "two_level": two, "ms": ms, "tflops": flops / ms / 1e9})
+    del kc, vc, ksc, vsc
+    torch.cuda.empty_cache()
 
 
 def _extra_write(fk, dev, stream, emit):

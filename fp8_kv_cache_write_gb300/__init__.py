@@ -74,7 +74,7 @@ def lib() -> ctypes.CDLL:
                                                       i32, i32, i32, i32, i64, f32, i32, i32, P,
                                                       i32, P, P]
         L.fp8kv_paged_decode_attn_noalloc.restype = i32
-        L.fp8kv_prefill_attn.argtypes = [P, P, i32, P, P, i32, i32, P, P, f32, f32, P, i32, P,
+        L.fp8kv_prefill_attn.argtypes = [P, P, i32, P, P, i32, i32, P, P, P, P, f32, f32, P, i32, P,
                                          i32, i32, i32, i32, i64, f32, i32, P, i32, P, P]
         L.fp8kv_prefill_attn.restype = i32
         L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
@@ -282,8 +282,9 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
 
 def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, context_lens,
                  *, kv_dtype=KV_E4M3, scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
-                 q_scale=1.0, prob_scale=1.0, softmax_scale=None, two_level=False, out=None,
-                 out_dtype=OUT_F32, err_flag=None, stream=None):
+                 k_scale_cache=None, v_scale_cache=None, q_scale=1.0, prob_scale=1.0,
+                 softmax_scale=None, two_level=False, out=None, out_dtype=OUT_F32, err_flag=None,
+                 stream=None):
     """Chunked causal FP8 prefill of q [Tq][Hq][D] (bf16) over the paged cache;
     returns out [Tq][Hq][D].  See fp8kv_prefill_attn."""
     _check(q, "q", torch.bfloat16)
@@ -292,8 +293,9 @@ def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, c
         _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
     _check(block_table, "block_table", torch.int32)
     _check(context_lens, "context_lens", torch.int32)
-    _check(k_scale, "k_scale", torch.float32)
-    _check(v_scale, "v_scale", torch.float32)
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale), ("k_scale_cache", k_scale_cache),
+                 ("v_scale_cache", v_scale_cache)):
+        _check(t, n, torch.float32)
     Tq, Hq, D = q.shape
     Hkv = k_cache.shape[1]
     if softmax_scale is None:
@@ -304,7 +306,8 @@ def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, c
     _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
     st = lib().fp8kv_prefill_attn(
         _ptr(q), _ptr(cu_seqlens_q), int(max_seqlen_q), _ptr(k_cache), _ptr(v_cache), kv_dtype,
-        scale_mode, _ptr(k_scale), _ptr(v_scale), float(q_scale), float(prob_scale),
+        scale_mode, _ptr(k_scale), _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache),
+        float(q_scale), float(prob_scale),
         _ptr(block_table), block_table.shape[1], _ptr(context_lens), cu_seqlens_q.numel() - 1,
         Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), 1 if two_level else 0, _ptr(out),
         out_dtype, _ptr(err_flag), _stream(stream))

@@ -412,7 +412,8 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
 
 int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
                        const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
-                       const float* k_scale, const float* v_scale, float q_scale,
+                       const float* k_scale, const float* v_scale, const float* k_scale_cache,
+                       const float* v_scale_cache, float q_scale,
                        float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
                        const int32_t* context_lens, int B, int Hq, int Hkv, int D,
                        int64_t num_blocks, float softmax_scale, int two_level, void* out,
@@ -429,9 +430,7 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
         !(prob_scale < 3.0e38f) || !(softmax_scale == softmax_scale))
         return FP8KV_ERR_INVALID;
     const int G = Hq / Hkv;
-    if ((kv_dtype == FP8KV_KV_E4M3 && scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD) ||
-        (D != 128 && D != 256) || G > 128 || (128 % G) != 0)
-        return FP8KV_ERR_UNSUPPORTED;
+    if ((D != 128 && D != 256) || G > 128 || (128 % G) != 0) return FP8KV_ERR_UNSUPPORTED;
     if (B == 0 || max_seqlen_q == 0) return FP8KV_OK;
     if (B > 65535 || Hkv > 65535 || max_blocks_per_seq < 1 || num_blocks < 1)
         return FP8KV_ERR_INVALID;
@@ -440,7 +439,11 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
         return FP8KV_ERR_UNSUPPORTED;
     if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_table || !context_lens || !out)
         return FP8KV_ERR_INVALID;
-    if (kv_dtype == FP8KV_KV_E4M3 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID;
+    const bool per_token = kv_dtype == FP8KV_KV_E4M3 && scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD;
+    if (kv_dtype == FP8KV_KV_E4M3 && !per_token && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID;
+    if (per_token && (!k_scale_cache || !v_scale_cache || !aligned(k_scale_cache, 16) ||
+                      !aligned(v_scale_cache, 16)))
+        return FP8KV_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return FP8KV_ERR_INVALID;
     CUtensorMap kmap, vmap;
@@ -464,6 +467,8 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     p.prob_scale = prob_scale;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.k_scale_cache = k_scale_cache;
+    p.v_scale_cache = v_scale_cache;
     p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;

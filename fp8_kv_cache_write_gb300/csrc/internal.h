@@ -85,6 +85,8 @@ struct PrefillParams {
     float q_scale, prob_scale;
     const float* k_scale;          // [1] or [Hkv]
     const float* v_scale;
+    const float* k_scale_cache;    // per token-head: [num_blocks][Hkv][16]
+    const float* v_scale_cache;
     int scale_mode;
     void* out;                     // [Tq][Hq][D]
     int out_bf16;

@@ -26,6 +26,13 @@
 //     rescales a row of O in TMEM only when the row max grows by more than 2^8.
 //     two-level on: every tile's P V lands in a fresh TMEM tile and the softmax
 //     threads add it into an fp32 accumulator on the CUDA cores.
+//   * per-token-head scales (PT): the K loader also copies each tile's K and V
+//     scale rows (64 bytes a page) into a 4-slot ring; the softmax multiplies
+//     logit column t by s_k(t) before the row max, and folds s_v(t) into the
+//     e4m3 weights relative to a running power-of-two bound E of the V scales
+//     seen so far, lifted by 2^5 under a lazy max of 2^3 so that they stay in
+//     e4m3's normal range; O is rescaled when E grows, like the lazy row max,
+//     and the row sums use the unfolded weights.
 //   * every mbarrier wait is bounded and watches a shared abort flag, so a stuck
 //     stage ends the kernel with FP8KV_ERR_TIMEOUT instead of hanging.
 #include <cuda_runtime.h>
@@ -40,6 +47,12 @@ namespace {
 
 constexpr int kRows = 128;          // MMA M: query rows of a CTA
 constexpr float kMaxInitP = -1.0e30f;
+// Per-token-head weights p s_v / E sit up to a factor max(s_v) / min(s_v) below
+// p; a lazy max of 2^3 (p <= 8) leaves room to lift them by 2^5 (<= 256 < 448),
+// which keeps almost every weight in e4m3's normal range (3 mantissa bits)
+// instead of its subnormal steps of 2^-9.
+constexpr float kLazyPT = 3.f;
+constexpr float kHeadPT = 32.f;
 
 template <int D, bool BF16>
 struct PCfg {
@@ -71,7 +84,11 @@ struct PCfg {
     static constexpr int kOffPMax = kOffOnes2;               // [2][kHalves][128] partial maxima
     static constexpr int kOffBar = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
     static constexpr int kNumBars = 20;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8; // tmem slot, abort flag
+    // per-token-head scales (e4m3 only): 4 slots of [k scales][v scales] of a
+    // tile (128 floats each), then the halves' V-scale maxima [2][2]
+    static constexpr int kOffScl = kOffBar + kNumBars * 8;
+    static constexpr int kSclBytes = BF16 ? 0 : 4 * 1024 + 16 * 4;
+    static constexpr int kOffMisc = kOffScl + kSclBytes;    // tmem slot, abort flag
     static constexpr int kSmem = 1024 + kOffMisc + 16;
 };
 
@@ -106,7 +123,16 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
-template <int D, bool TWO_LEVEL, bool BF16>
+// Smallest power of two >= x for x > 0 (normal floats), 0 for x <= 0.
+__device__ __forceinline__ float pow2_ceil(float x) {
+    if (!(x > 0.f)) return 0.f;
+    uint32_t u = __float_as_uint(x);
+    uint32_t e = u >> 23;
+    if (u & 0x7fffffu) ++e;
+    return __uint_as_float(e << 23);
+}
+
+template <int D, bool TWO_LEVEL, bool BF16, bool PT>
 __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -123,7 +149,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     // l of the quantized weights come from the tensor core too, as P times a
     // block of ones, into [kLCol, kLCol + 16).
     constexpr uint32_t kOCol = D <= 128 ? 128u : (TWO_LEVEL ? 256u : 128u);
-    constexpr bool kLMma = D == 256 && !TWO_LEVEL && !BF16;
+    constexpr bool kLMma = D == 256 && !TWO_LEVEL && !BF16 && !PT;
     constexpr uint32_t kLCol = kOCol + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -255,13 +281,25 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             if (j >= 2 && lane == 0)
                 go = wait_or_abort(bar(empty0 + st), ((j - 2) >> 1) & 1, abort_flag, p.err);
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), tile_bytes);
+            const uint32_t scl_bytes = PT && !is_v ? static_cast<uint32_t>(n_pages) * 128u : 0u;
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), tile_bytes + scl_bytes);
             __syncwarp();
             if (lane < n_pages) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_3d(dst + pn * (kKeys * 128) + lane * 2048, map, pn * 128, 0, z,
                                 bar(full0 + st));
+                if constexpr (PT) {
+                    // the tile's K and V scale rows, into slot j % 4 (the softmax of
+                    // tile j - 4 has finished with it: QK of j - 2 ran after it)
+                    if (!is_v) {
+                        const uint32_t sd = sbase + C::kOffScl + (j & 3) * 1024 + lane * 64;
+                        bulk_load(sd, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                                  bar(full0 + st));
+                        bulk_load(sd + 512, p.v_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                                  bar(full0 + st));
+                    }
+                }
             }
             __syncwarp();
             issued = j + 1;
@@ -393,11 +431,16 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
         // the bf16 cache has no scales and keeps Q and P in bf16
         float kconst = 1.f, vconst = 1.f, qs = 1.f, ps = 1.f;
         if constexpr (!BF16) {
-            kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
-            vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
+            if constexpr (!PT) {
+                kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
+                vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
+            }
             qs = p.q_scale;
             ps = p.prob_scale;
         }
+        // PT: running power-of-two bound of the V scales folded into the weights
+        float e_run = 0.f;
+        float* ebuf = reinterpret_cast<float*>(smem + C::kOffScl + 4 * 1024);   // [2][2]
         const float sc = qs * kconst * p.scale_log2;   // > 0: the max of raw S scales
         const float lps = log2f(ps);                   // p / prob_scale = 2^(s sc - m - lps)
         float m = kMaxInitP, l = 0.f;                  // l: this half's keys (summed at the end)
@@ -428,7 +471,27 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) mxp[i] = -__int_as_float(0x7f800000);
             const bool full = key0 + kKH - 1 <= pos_r;
-            if (full) {
+            // PT: this tile's scale rows (keys past ctx hold stale values: never read
+            // for a logit, excluded from the V-scale bound)
+            const float* ksl = reinterpret_cast<const float*>(smem + C::kOffScl + (j & 3) * 1024) +
+                               kh * kKH;
+            const float* vsl = ksl + 128;
+            if constexpr (PT) {
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < kKH; ++i) {
+                        s[i] = __uint_as_float(sb[i]) * (ksl[i] * sc);
+                        mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kKH; ++i) {
+                        s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) * (ksl[i] * sc)
+                                                 : -__int_as_float(0x7f800000);
+                        mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                    }
+                }
+            } else if (full) {
 #pragma unroll
                 for (int i = 0; i < kKH; ++i) {
                     s[i] = __uint_as_float(sb[i]);
@@ -443,6 +506,17 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             }
             float mx_raw = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            float vmax = 0.f;                   // PT: this half's largest V scale
+            if constexpr (PT) {
+                const int nval = ctx - key0;    // keys of this half with written scales
+                if (nval >= kKH) {
+#pragma unroll 16
+                    for (int i = 0; i < kKH; ++i) vmax = fmaxf(vmax, vsl[i]);
+                } else {
+                    for (int i = 0; i < nval; ++i) vmax = fmaxf(vmax, vsl[i]);
+                }
+                ebuf[st * 2 + kh] = vmax;       // every thread of the half: the same value
+            }
             if constexpr (kHalves == 2) {       // the row's max over both halves
                 pmax[(st * 2 + kh) * kRows + r] = mx_raw;
                 if (!pair_sync()) {
@@ -450,17 +524,26 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                     break;
                 }
                 mx_raw = fmaxf(mx_raw, pmax[(st * 2 + (kh ^ 1)) * kRows + r]);
+                if constexpr (PT) vmax = fmaxf(vmax, ebuf[st * 2 + (kh ^ 1)]);
             }
-            const float mx = mx_raw * sc;
+            const float mx = PT ? mx_raw : mx_raw * sc;
+            float beta = 1.f;                   // PT: O's factor when the V bound grows
+            if constexpr (PT) {
+                const float e_t = pow2_ceil(vmax);
+                if (e_t > e_run) {
+                    beta = e_run > 0.f ? e_run / e_t : 1.f;
+                    e_run = e_t;
+                }
+            }
             float alpha = 1.f;
-            if (mx > m + 8.f) {                 // lazy running max (the same in both halves)
+            if (mx > m + (PT ? kLazyPT : 8.f)) {   // lazy running max (the same in both halves)
                 alpha = ex2p(m - mx);
                 m = mx;
                 l *= alpha;
             }
             // a row whose max moved rescales its O row in TMEM (two-level off); the
             // tcgen05 loads are warp-wide, so the warp does it when any row needs it
-            if (!TWO_LEVEL && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (!TWO_LEVEL && j > 0 && __any_sync(0xffffffffu, alpha != 1.f || beta != 1.f)) {
                 // O (TMEM) must hold PV of tile j-1 before it is rescaled
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(bar(kPvDone0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
@@ -479,9 +562,11 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                                         (cch < kChunks ? kOCol + kh * kDH + cch * 32 : kLCol);
                     tmem_ld32(ta, rr);
                     tmem_wait_ld();
+                    // O takes alpha and beta; the tensor-core l (not PT) only alpha
+                    const float fo = cch < kChunks ? alpha * beta : alpha;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * fo);
                     tmem_st32(ta, rr);
                 }
                 tmem_wait_st();
@@ -497,10 +582,31 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             constexpr int kPerChunk = 16 / C::kElem;    // keys per 16-byte chunk
             constexpr int kMyChunks = 8 / kHalves;      // this half's chunks of the row
             const float moff = m + lps;
+            // PT: weight = p * s_v * kHeadPT / (E prob_scale), the unfolded p into l
+            const float vinv = PT && e_run > 0.f ? kHeadPT / (e_run * ps) : 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < kMyChunks; ++c8) {
                 const int cc = kh * kMyChunks + c8;
                 uint32_t w[4];
+                if constexpr (PT) {
+#pragma unroll
+                    for (int i = 0; i < kPerChunk / 2; ++i) {
+                        const int ia = c8 * kPerChunk + 2 * i, ib = ia + 1;
+                        const float pa = ex2p(s[ia] - m), pb = ex2p(s[ib] - m);
+                        l += pa + pb;
+                        // masked keys: p = 0 and a stale scale that must not enter
+                        const bool va = full || key0 + ia <= pos_r, vb = full || key0 + ib <= pos_r;
+                        const uint32_t code = e4m3x2_from_f32(va ? pa * vsl[ia] * vinv : 0.f,
+                                                              vb ? pb * vsl[ib] * vinv : 0.f);
+                        if (i & 1)
+                            w[i >> 1] |= code << 16;
+                        else
+                            w[i >> 1] = code;
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < kPerChunk / 2; ++i) {
                     const float pa = ex2p(fmaf(s[c8 * kPerChunk + 2 * i], sc, -moff));
@@ -566,7 +672,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float prev = j > 0 ? __uint_as_float(acc[i]) * alpha : 0.f;
+                        const float prev = j > 0 ? __uint_as_float(acc[i]) * (alpha * beta) : 0.f;
                         acc[i] = __float_as_uint(prev + __uint_as_float(pv[i]));
                     }
                     tmem_st32(tmem + lane_addr + kOCol + col, acc);
@@ -603,7 +709,8 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             }
         }
         if (ok) {
-            const float f = l > 0.f ? vconst * ps / l : 0.f;
+            // PT: l sums p itself (not p / prob_scale) and O carries kHeadPT / (E prob_scale)
+            const float f = l > 0.f ? (PT ? e_run * ps / kHeadPT : vconst * ps) / l : 0.f;
             const int head = r % G;
             for (int cch = 0; cch < kDH / 32; ++cch) {
                 const int col = kh * kDH + cch * 32;
@@ -639,10 +746,10 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     }
 }
 
-template <int D, bool TWO, bool BF16>
+template <int D, bool TWO, bool BF16, bool PT>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
-    auto kern = prefill_kernel<D, TWO, BF16>;
+    auto kern = prefill_kernel<D, TWO, BF16, PT>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -658,11 +765,20 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
     return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PT>
 cudaError_t launch_two(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        int two_level, int grid_x, cudaStream_t stream) {
-    return two_level ? launch_prefill_t<D, true, BF16>(p, kmap, vmap, grid_x, stream)
-                     : launch_prefill_t<D, false, BF16>(p, kmap, vmap, grid_x, stream);
+    return two_level ? launch_prefill_t<D, true, BF16, PT>(p, kmap, vmap, grid_x, stream)
+                     : launch_prefill_t<D, false, BF16, PT>(p, kmap, vmap, grid_x, stream);
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     bool bf, int two_level, int grid_x, cudaStream_t stream) {
+    if (bf) return launch_two<D, true, false>(p, kmap, vmap, two_level, grid_x, stream);
+    if (p.scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD)
+        return launch_two<D, false, true>(p, kmap, vmap, two_level, grid_x, stream);
+    return launch_two<D, false, false>(p, kmap, vmap, two_level, grid_x, stream);
 }
 
 }  // namespace
@@ -671,11 +787,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int D, int kv_dtype, int two_level,
                            int grid_x, cudaStream_t stream) {
     const bool bf = kv_dtype == FP8KV_KV_BF16;
-    if (D == 128)
-        return bf ? launch_two<128, true>(p, kmap, vmap, two_level, grid_x, stream)
-                  : launch_two<128, false>(p, kmap, vmap, two_level, grid_x, stream);
-    return bf ? launch_two<256, true>(p, kmap, vmap, two_level, grid_x, stream)
-              : launch_two<256, false>(p, kmap, vmap, two_level, grid_x, stream);
+    if (D == 128) return launch_d<128>(p, kmap, vmap, bf, two_level, grid_x, stream);
+    return launch_d<256>(p, kmap, vmap, bf, two_level, grid_x, stream);
 }
 
 }  // namespace fp8kv

@@ -204,7 +204,11 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
  *   max_seqlen_q   host upper bound of cu[b+1] - cu[b] (sizes the grid).
  *   k_cache, v_cache  e4m3 [num_blocks][Hkv][16][D] holding every key of the
  *                  sequence, the chunk's own keys included (written before).
- *   scale_mode     PER_TENSOR (k_scale[0], v_scale[0]) or PER_HEAD (k_scale[h]).
+ *   scale_mode     PER_TENSOR (k_scale[0], v_scale[0]), PER_HEAD (k_scale[h]) or
+ *                  PER_TOKEN_HEAD (k_scale_cache / v_scale_cache [num_blocks][Hkv][16],
+ *                  16-byte aligned, as fp8kv_kv_cache_write stored them; the V
+ *                  scales are folded into the e4m3 weights relative to a running
+ *                  power-of-two bound of the scales seen, see prefill.cu).
  *   q_scale, prob_scale  host floats > 0: Q and the softmax weights are stored
  *                  as e4m3(q / q_scale) and e4m3(p / prob_scale) for the MMAs.
  *   context_lens   int32 [B]: keys of sequence b, the chunk included; query i of
@@ -213,13 +217,15 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
  *                  accumulator on the CUDA cores; 0: the tensor core accumulates
  *                  across tiles (enough on Blackwell).
  *   out            [Tq][Hq][D] fp32 or bf16.
- * Supported: e4m3 cache, D in {128, 256}, Hq / Hkv dividing 128.  Other modes
- * return FP8KV_ERR_UNSUPPORTED.  With q_scale or prob_scale equal to 1.0 the
- * call succeeds and sets fp8kv_last_warning().
+ * Supported: e4m3 cache (every scale mode) and its bf16 twin (bf16 Q, P and
+ * cache, kind::f16; scales ignored), D in {128, 256}, Hq / Hkv dividing 128.
+ * Other shapes return FP8KV_ERR_UNSUPPORTED.  With q_scale or prob_scale equal
+ * to 1.0 an e4m3 call succeeds and sets fp8kv_last_warning().
  */
 int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
                        const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
-                       const float* k_scale, const float* v_scale, float q_scale,
+                       const float* k_scale, const float* v_scale, const float* k_scale_cache,
+                       const float* v_scale_cache, float q_scale,
                        float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
                        const int32_t* context_lens, int B, int Hq, int Hkv, int D,
                        int64_t num_blocks, float softmax_scale, int two_level, void* out,

@@ -22,39 +22,51 @@ PREFILL_TOL = 1e-2
 
 
 def _caches(w, scale_mode=0):
+    """The cache written by the library and by the oracle (compared bit for bit);
+    per-token-head mode also returns both sides' scale caches."""
     nb, Hkv, D = w.num_blocks, w.Hkv, w.D
     kc = torch.zeros(nb, Hkv, 16, D, dtype=torch.uint8, device="cuda")
     vc = torch.zeros_like(kc)
+    ksc = torch.zeros(nb, Hkv, 16, dtype=torch.float32, device="cuda")
+    vsc = torch.zeros_like(ksc)
     ks, vs = w.k_scale.cuda(), w.v_scale.cuda()
     fk.kv_cache_write(w.k_all.cuda(), w.v_all.cuda(), w.all_slots.cuda(), kc, vc, kv_dtype=0,
-                      scale_mode=scale_mode, k_scale=ks, v_scale=vs)
+                      scale_mode=scale_mode, k_scale=ks, v_scale=vs, k_scale_cache=ksc,
+                      v_scale_cache=vsc)
     okc = np.zeros((nb, Hkv, 16, D), np.uint8)
     ovc = np.zeros_like(okc)
+    oks = np.zeros((nb, Hkv, 16), np.float32)
+    ovs = np.zeros_like(oks)
     assert oracle.kv_cache_write(bits16(w.k_all), bits16(w.v_all), w.all_slots.numpy(), okc, ovc,
                                  kv_dtype=0, scale_mode=scale_mode, k_scale=w.k_scale.numpy(),
-                                 v_scale=w.v_scale.numpy()) == 0
+                                 v_scale=w.v_scale.numpy(), k_scale_cache=oks,
+                                 v_scale_cache=ovs) == 0
     assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
-    return (kc, vc, ks, vs), (okc, ovc)
+    if scale_mode == 2:
+        assert np.array_equal(ksc.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+        return (kc, vc, ks, vs, ksc, vsc), (okc, ovc, oks, ovs)
+    return (kc, vc, ks, vs, None, None), (okc, ovc, None, None)
 
 
 def _gpu(w, dev_c, scale_mode=0, two_level=False, **kw):
-    kc, vc, ks, vs = dev_c
+    kc, vc, ks, vs, ksc, vsc = dev_c
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = fk.prefill_attn(w.q.cuda(), w.cu_seqlens_q.cuda(), w.max_seqlen_q, kc, vc,
                           w.block_table.cuda(), w.context_lens.cuda(), kv_dtype=0,
-                          scale_mode=scale_mode, k_scale=ks, v_scale=vs, two_level=two_level,
-                          err_flag=err, **kw)
+                          scale_mode=scale_mode, k_scale=ks, v_scale=vs, k_scale_cache=ksc,
+                          v_scale_cache=vsc, two_level=two_level, err_flag=err, **kw)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, int(err.item())
     return out
 
 
 def _oracle(w, host_c, units, scale_mode=0):
-    okc, ovc = host_c
+    okc, ovc, oks, ovs = host_c
     st, ref = oracle.prefill_attn(bits16(w.q), w.cu_seqlens_q.numpy(), okc, ovc,
                                   w.block_table.numpy(), w.context_lens.numpy(), kv_dtype=0,
                                   scale_mode=scale_mode, k_scale=w.k_scale.numpy(),
-                                  v_scale=w.v_scale.numpy(), units=units, nthreads=16)
+                                  v_scale=w.v_scale.numpy(), k_scale_cache=oks,
+                                  v_scale_cache=ovs, units=units, nthreads=16)
     assert st == 0
     return ref
 
@@ -155,6 +167,92 @@ def test_prefill_per_head_scales():
     assert float(np.abs(got - ref).max()) <= PREFILL_TOL
 
 
+def _with_outliers(w, seed, frac=0.01, factor=20.0):
+    """1 % of the (KV head, channel) pairs of every token scaled x20 in K and V (the
+    outlier channels per-token-head scales are for), plus 5 % of the tokens'
+    values x8 so that the V scales of a tile differ by up to 8x."""
+    g = torch.Generator().manual_seed(seed)
+    Hkv, D = w.Hkv, w.D
+    n = max(1, int(np.ceil(frac * Hkv * D)))
+    idx = torch.randperm(Hkv * D, generator=g)[:n]
+    for t in (w.k_all, w.v_all):
+        for i in idx.tolist():
+            h, c = divmod(i, D)
+            t[:, h, c] = (t[:, h, c].float() * factor).to(torch.bfloat16)
+    loud = torch.randperm(w.v_all.shape[0], generator=g)[: w.v_all.shape[0] // 20]
+    w.v_all[loud] = (w.v_all[loud].float() * 8.0).to(torch.bfloat16)
+    return w
+
+
+def _loud_values(w, seed, frac=0.05, factor=8.0):
+    """5 % of the tokens' values x8: their per-token-head V scales are 8x the
+    others', so the running V-scale bound grows and most weights sit 8x under it."""
+    g = torch.Generator().manual_seed(seed)
+    loud = torch.randperm(w.v_all.shape[0], generator=g)[: int(w.v_all.shape[0] * frac)]
+    w.v_all[loud] = (w.v_all[loud].float() * factor).to(torch.bfloat16)
+    return w
+
+
+@pytest.mark.parametrize("two_level", [False, True])
+@pytest.mark.parametrize("D,Hq,Hkv", [(256, 8, 1), (128, 8, 2)])
+def test_prefill_per_token_head_long_context(two_level, D, Hq, Hkv):
+    # The error model above with the values' rms in place of 1 (the loud tokens
+    # raise it to ~2): rounding P to e4m3 is the only approximation, per row.
+    w = _loud_values(synth.prefill(seed=360 + D, ctx=(4100, 6001), chunk=(123, 300), Hq=Hq,
+                                   Hkv=Hkv, D=D), 361 + D)
+    dev_c, host_c = _caches(w, scale_mode=2)
+    out = _gpu(w, dev_c, scale_mode=2, two_level=two_level).cpu().numpy()
+    units = _rows(w, 5)
+    ref = _oracle(w, host_c, units, scale_mode=2)
+    got = np.stack([out[t, h] for t, h in units])
+    rms_v = float(np.sqrt((w.v_all.float().numpy() ** 2).mean()))
+    bound = np.array([max(PREFILL_TOL, rms_v * 8 * 0.036 * 1.4 * np.sqrt(np.e / _n_keys(w, t)))
+                      for t, _ in units])
+    err = np.abs(got - ref).max(axis=1)
+    assert np.all(err <= bound), float((err / bound).max())
+
+
+@pytest.mark.parametrize("two_level", [False, True])
+def test_prefill_per_token_head_short_context(two_level):
+    w = synth.prefill(seed=370, ctx=(700, 1301, 17), chunk=(123, 300, 17), Hq=8, Hkv=2, D=128)
+    dev_c, host_c = _caches(w, scale_mode=2)
+    out = _gpu(w, dev_c, scale_mode=2, two_level=two_level).cpu().numpy()
+    units = _rows(w, 2)
+    ref = _oracle(w, host_c, units, scale_mode=2)
+    got = np.stack([out[t, h] for t, h in units])
+    bound = np.array([_short_context_bound(_n_keys(w, t)) for t, _ in units])
+    err = np.abs(got - ref).max(axis=1)
+    assert np.all(err <= bound), float((err / bound).max())
+
+
+def test_prefill_per_token_head_two_level_agree():
+    w = _with_outliers(synth.prefill(seed=380, ctx=(3000,), chunk=(256,), Hq=8, Hkv=1, D=256),
+                       381)
+    dev_c, _ = _caches(w, scale_mode=2)
+    off = _gpu(w, dev_c, scale_mode=2, two_level=False)
+    on = _gpu(w, dev_c, scale_mode=2, two_level=True)
+    assert torch.isfinite(off).all() and torch.isfinite(on).all()
+    scale = max(1.0, float(off.abs().max()))
+    assert float((off - on).abs().max()) <= 1e-4 * scale
+
+
+def test_prefill_per_token_head_stale_scales_do_not_leak():
+    # scale slots past ctx on the last page hold NaN / inf: never read for a
+    # logit, never in the V-scale bound
+    w = synth.prefill(seed=390, ctx=(1000,), chunk=(40,), Hq=8, Hkv=1, D=256)
+    dev_c, _ = _caches(w, scale_mode=2)
+    clean = _gpu(w, dev_c, scale_mode=2).clone()
+    kc, vc, ks, vs, ksc, vsc = dev_c
+    last_blk = int(w.block_table[0, (1000 - 1) // 16])
+    ksc[last_blk, :, 1000 % 16:] = float("nan")
+    vsc[last_blk, :, 1000 % 16:] = float("inf")
+    kc[last_blk, :, 1000 % 16:] = 0x7F
+    vc[last_blk, :, 1000 % 16:] = 0x7F
+    dirty = _gpu(w, dev_c, scale_mode=2)
+    assert torch.isfinite(dirty).all()
+    assert torch.equal(clean, dirty)
+
+
 def test_prefill_config5_full_size_sampled():
     # 4096 new queries at positions 28672..32767 of a 32768-token e4m3 cache,
     # 8 query heads / 1 KV head, head_dim 256, per-tensor 1.0, both switch settings
@@ -174,11 +272,11 @@ def test_unwritten_tail_slots_do_not_leak():
     w = synth.prefill(seed=330, ctx=(1000,), chunk=(40,), Hq=8, Hkv=1, D=256)
     dev_c, _ = _caches(w)
     clean = _gpu(w, dev_c).clone()
-    kc, vc, ks, vs = dev_c
+    kc, vc, ks, vs, _, _ = dev_c
     last_blk = int(w.block_table[0, (1000 - 1) // 16])
     kc[last_blk, :, 1000 % 16:] = 0x7F
     vc[last_blk, :, 1000 % 16:] = 0x7F
-    dirty = _gpu(w, (kc, vc, ks, vs))
+    dirty = _gpu(w, (kc, vc, ks, vs, None, None))
     assert torch.isfinite(dirty).all()
     assert torch.equal(clean, dirty)
 

@@ -51,6 +51,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -154,6 +158,60 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 __device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
     return static_cast<uint16_t>(
         __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// e4m3 codes of IEEE fp32 quotients fp32(x / s) in two phases: a multiply by
+// r = __frcp_rn(s) for every value (no branches), then the IEEE divide for the
+// few pairs whose codes the multiply cannot certify.
+//
+// Why the multiply is exact where it is used: y = fp32(x * r) has relative error
+// below 2^-22 against x / s, so y is within 6 fp32 steps (adjacent bit patterns)
+// of Q = fp32(x / s), also across a binade boundary.  Rounding to e4m3 is
+// monotone in the value, so if the patterns 16 steps below and 16 steps above y
+// encode to the same code, Q, which lies between them, encodes to it too.
+// Zeros, infinities, NaN and magnitudes within 16 steps of zero make the two
+// ends differ (their patterns cross into the other sign or into NaN), as does a
+// quotient near an e4m3 rounding midpoint (about 1 % of pairs on bf16 data,
+// whose ratios often land on one exactly).  r must be finite and nonzero
+// (quotient_fast), else every pair takes the divide.
+//
+// Phase 1 for N values: codes into w (4 per word, value 0 in the low byte);
+// returns the mask of pairs (bit i = values 2i, 2i+1) that need phase 2.
+template <int N>
+__device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], float r, bool fast,
+                                                           uint32_t (&w)[N / 4]) {
+    uint32_t redo = 0u;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const uint32_t b0 = __float_as_uint(__fmul_rn(f[2 * i], r));
+        const uint32_t b1 = __float_as_uint(__fmul_rn(f[2 * i + 1], r));
+        const uint32_t lo = e4m3x2_from_f32(__uint_as_float(b0 - 16u), __uint_as_float(b1 - 16u));
+        const uint32_t hi = e4m3x2_from_f32(__uint_as_float(b0 + 16u), __uint_as_float(b1 + 16u));
+        if (i & 1)
+            w[i >> 1] |= lo << 16;
+        else
+            w[i >> 1] = lo;
+        redo |= static_cast<uint32_t>(lo != hi) << i;
+    }
+    return fast ? redo : (N >= 64 ? ~0u : (1u << (N / 2)) - 1u);
+}
+
+// Phase 2 for pair i: codes of fp32(x0 / s), fp32(x1 / s) by IEEE divides,
+// written over the pair's two bytes in w.
+template <int NW>
+__device__ __forceinline__ void e4m3_pair_by_divide(uint32_t (&w)[NW], int i, float x0, float x1,
+                                                    float s) {
+    const uint32_t c = e4m3x2_from_f32(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+    const int sh = (i & 1) * 16;
+#pragma unroll
+    for (int k = 0; k < NW; ++k)
+        if (k == (i >> 1)) w[k] = (w[k] & ~(0xffffu << sh)) | (c << sh);
+}
+
+// The per-row inputs of phase 1: r = __frcp_rn(s) and whether it may be used
+// (r finite and nonzero).
+__device__ __forceinline__ bool quotient_fast(float r) {
+    return r != 0.0f && (__float_as_uint(r) & 0x7f800000u) != 0x7f800000u;
 }
 
 // Two e4m3fn bytes (low byte first) -> f16x2, exact.

@@ -91,8 +91,11 @@ typedef enum { FP8KV_OUT_F32 = 0, FP8KV_OUT_BF16 = 1 } fp8kv_out_dtype;
  *                 k_scale_cache / v_scale_cache.  A zero scale writes code 0.
  *   k_scale, v_scale  fp32 device arrays of 1 or Hkv entries (ignored for
  *                 PER_TOKEN_HEAD and BF16).
- * The division is an IEEE fp32 divide and the encoding rounds to nearest even,
- * so codes and scales are bit-identical to a plain CPU restatement.
+ * Codes are those of the IEEE fp32 quotient (a multiply by fp32(1/scale) is used
+ * only where it provably gives the same codes) rounded to nearest even, so codes
+ * and scales are bit-identical to a plain CPU restatement.  Bulk writes
+ * (T * Hkv >= 8192 rows, k and v in device memory) stream K and V through
+ * shared memory with bulk copies; other writes use plain loads.
  */
 int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T,
                          int Hkv, int D, void* k_cache, void* v_cache, int64_t num_blocks,

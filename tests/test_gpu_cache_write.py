@@ -121,3 +121,90 @@ def test_encoder_with_scales_matches_oracle(scale):
     got = fk.quantize_e4m3(x.cuda(), scale).cpu().numpy()
     q = (x.numpy().astype(np.float32) / np.float32(scale)).astype(np.float32)
     assert np.array_equal(got, oracle.e4m3_encode(q))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hkv", [3, 8])
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
+def test_bulk_write_bit_exact(D, Hkv, kv_dtype, mode):
+    # Bulk writes (T * Hkv >= 8192 rows, device inputs) go through the
+    # shared-memory staged kernel: chunked rows, ragged last chunk, a head count
+    # that is not a power of two, padding slots, all-zero rows, a x20 outlier
+    # channel and bytes outside the written slots left untouched.
+    T = 3000 if Hkv == 3 else 1100
+    nb = T // 16 + 9
+    g = torch.Generator().manual_seed(40 + D + Hkv + 7 * mode + 11 * kv_dtype)
+    k = torch.randn(T, Hkv, D, generator=g)
+    v = torch.randn(T, Hkv, D, generator=g)
+    k[:, 0, 5] *= 20
+    v[:, Hkv - 1, D - 1] *= 20
+    k[17] = 0
+    v[T - 2, 0] = 0
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int64)
+    slots[3::97] = -1
+    dt = torch.uint8 if kv_dtype == 0 else torch.bfloat16
+    kc = torch.full((nb, Hkv, 16, D), 0x5A, dtype=torch.uint8, device="cuda").view(dt) \
+        if kv_dtype == 0 else torch.full((nb, Hkv, 16, D), 7.0, dtype=dt, device="cuda")
+    vc = kc.clone()
+    ks = torch.full((nb, Hkv, 16), -3.0, device="cuda")
+    vs = ks.clone()
+    ksc = vsc = None
+    if kv_dtype == 0 and mode == 0:
+        ksc, vsc = torch.tensor([0.37]), torch.tensor([3.0e-3])
+    elif kv_dtype == 0 and mode == 1:
+        ksc = torch.rand(Hkv, generator=g) * 0.05 + 1e-3
+        vsc = torch.rand(Hkv, generator=g) * 0.05 + 1e-3
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fk.kv_cache_write(k.cuda(), v.cuda(), slots.cuda(), kc, vc, kv_dtype=kv_dtype, scale_mode=mode,
+                      k_scale=None if ksc is None else ksc.cuda(),
+                      v_scale=None if vsc is None else vsc.cuda(),
+                      k_scale_cache=ks, v_scale_cache=vs, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    if kv_dtype == 0:
+        okc = np.full((nb, Hkv, 16, D), 0x5A, np.uint8)
+    else:
+        okc = np.full((nb, Hkv, 16, D), bits16(torch.tensor([7.0]).to(torch.bfloat16))[0],
+                      np.uint16)
+    ovc = okc.copy()
+    oks = np.full((nb, Hkv, 16), -3.0, np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_cache_write(bits16(k), bits16(v), slots.numpy(), okc, ovc,
+                                 kv_dtype=kv_dtype, scale_mode=mode,
+                                 k_scale=None if ksc is None else ksc.numpy(),
+                                 v_scale=None if vsc is None else vsc.numpy(),
+                                 k_scale_cache=oks, v_scale_cache=ovs) == 0
+    view = (lambda t: t.cpu().numpy()) if kv_dtype == 0 else \
+        (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert np.array_equal(view(kc), okc), "K cache bytes differ"
+    assert np.array_equal(view(vc), ovc), "V cache bytes differ"
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+
+
+def test_encoder_every_bf16_value_under_many_scales():
+    # Every finite bf16 value divided by 256 scales spread over the whole fp32
+    # range (tiny, subnormal, huge, negative, amax/448-shaped), through the
+    # writer's quantizer, against the oracle's encoder of numpy's IEEE fp32
+    # quotient.  NaN quotients are left out (their sign is not compared).
+    allbf = (np.arange(1 << 16, dtype=np.uint32) << 16).view(np.float32)
+    allbf = allbf[np.isfinite(allbf)]
+    rng = np.random.default_rng(9)
+    scales = np.concatenate([
+        np.float32([1.0, 448.0, 1.0 / 448, -0.37, 2.0 ** -149, 2.0 ** -130, 2.0 ** -127,
+                    2.0 ** 126, 3 * 2.0 ** 125, np.finfo(np.float32).max, 1e-30, 3.0e38]),
+        (np.abs(rng.standard_normal(180)) * 10.0 ** rng.uniform(-44, 38, 180)).astype(np.float32),
+        ((rng.integers(1, 0x7f80, 64, dtype=np.uint32) << 16).view(np.float32)
+         / np.float32(448)).astype(np.float32)])
+    xd = torch.from_numpy(allbf).cuda()
+    for s in scales:
+        s = np.float32(s)
+        if not np.isfinite(s) or s == 0:
+            continue
+        got = fk.quantize_e4m3(xd, float(s)).cpu().numpy()
+        with np.errstate(all="ignore"):
+            q = (allbf / s).astype(np.float32)
+        keep = ~np.isnan(q)
+        want = oracle.e4m3_encode(q)
+        assert np.array_equal(got[keep], want[keep]), f"scale {s!r}"

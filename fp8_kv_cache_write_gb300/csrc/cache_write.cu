@@ -12,10 +12,10 @@
 // Two kernels, both HBM-streaming (read 4*Hkv*D, write 2*Hkv*D (+8*Hkv scale)
 // bytes per token):
 //   * staged (bulk writes from device memory): K and V are contiguous
-//     [T*Hkv][D] arrays, so one producer lane bulk-copies 16 KiB chunks of each
-//     (cp.async.bulk, L2 evict-first) into a 2-stage shared-memory ring, and 8
+//     [T*Hkv][D] arrays, so one producer lane bulk-copies 12 KiB chunks of each
+//     (cp.async.bulk, L2 evict-first) into a 3-stage shared-memory ring, and 8
 //     consumer warps quantize rows out of shared memory.  The bytes in flight
-//     (3 CTAs x 2 stages of 32 KiB per SM) no longer depend on registers.
+//     (3 CTAs x 2 of their 3 stages of 24 KiB per SM) no longer depend on registers.
 //   * direct (small writes, e.g. one decode step, or inputs in pinned host
 //     memory): D/8 lanes own one row and keep the loads of 4 rows in flight.
 // Each lane quantizes in two phases: a branch-free multiply by fp32(1/s) whose
@@ -64,8 +64,8 @@ __device__ __forceinline__ void unpack8(uint4 x, float* f) {
 namespace staged {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
-constexpr int kStages = 2;
-constexpr int kTileBytes = 16384;                     // per tensor (K or V) per stage
+constexpr int kStages = 3;
+constexpr int kTileBytes = 12288;                     // per tensor (K or V) per stage
 constexpr int kSmemBytes = kStages * 2 * kTileBytes + 2 * kStages * 8;
 constexpr int kCtasPerSm = 3;
 // bulk writes only: below this many (token, head) rows the direct kernel runs
@@ -74,7 +74,7 @@ constexpr int64_t kMinRows = 8192;
 
 // CTA c takes chunks c, c + gridDim.x, ...; chunk i holds rows
 // [i * rows_per_chunk, min(rows, (i + 1) * rows_per_chunk)) of K and of V
-// (rows_per_chunk <= 16 KiB / (2 D)).  hkv_shift = log2(Hkv) when Hkv is a power
+// (rows_per_chunk <= 12 KiB / (2 D)).  hkv_shift = log2(Hkv) when Hkv is a power
 // of two, else -1.
 template <int D, int MODE, bool BF16>
 __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
@@ -192,21 +192,20 @@ __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
                     if (l == 0) (which ? p.v_scale_cache : p.k_scale_cache)[row] = s;
                 }
                 uint32_t w[4] = {0u, 0u, 0u, 0u};   // a zero scale writes code 0
-                if (s != 0.0f) {
-                    const float r = __frcp_rn(s);
-                    uint32_t redo = e4m3_codes_by_multiply(f, r, quotient_fast(r), w);
-                    while (redo) {                   // rare: reread the pair, divide
-                        const int i = __ffs(redo) - 1;
-                        redo &= redo - 1u;
-                        const uint32_t pr = *reinterpret_cast<const uint32_t*>(
-                            src + (i < 4 ? l * 16 + 4 * i : D + l * 16 + 4 * (i - 4)));
-                        e4m3_pair_by_divide(w, i, bf16_bits_to_float(pr & 0xffffu),
-                                            bf16_bits_to_float(pr >> 16), s);
-                    }
-                }
+                uint32_t redo = 0u;
+                if (s != 0.0f) redo = e4m3_codes_by_multiply(f, s, w);
                 uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache) + row * D;
                 *reinterpret_cast<uint2*>(dst + l * 8) = make_uint2(w[0], w[1]);
                 *reinterpret_cast<uint2*>(dst + D / 2 + l * 8) = make_uint2(w[2], w[3]);
+                while (redo) {                       // rare: reread the pair, divide, restore
+                    const int i = __ffs(redo) - 1;
+                    redo &= redo - 1u;
+                    const int e = i < 4 ? 2 * i : D / 2 + 2 * (i - 4);   // value index in the lane's run
+                    const uint32_t pr = *reinterpret_cast<const uint32_t*>(
+                        src + (i < 4 ? l * 16 + 4 * i : D + l * 16 + 4 * (i - 4)));
+                    *reinterpret_cast<uint16_t*>(dst + l * 8 + e) = e4m3x2_by_divide(
+                        bf16_bits_to_float(pr & 0xffffu), bf16_bits_to_float(pr >> 16), s);
+                }
             }
         }
         __syncwarp();
@@ -279,22 +278,18 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(WriteParams p) {
                     if (l == 0) (which ? p.v_scale_cache : p.k_scale_cache)[row] = s;
                 }
                 uint32_t w[2] = {0u, 0u};            // a zero scale writes code 0
-                if (s != 0.0f) {
-                    const float rcp = __frcp_rn(s);
-                    uint32_t redo = e4m3_codes_by_multiply(f, rcp, quotient_fast(rcp), w);
-                    const uint32_t xw[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-                    while (redo) {                   // rare: divide the pair
-                        const int i = __ffs(redo) - 1;
-                        redo &= redo - 1u;
-                        uint32_t pr = 0u;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) pr = k == i ? xw[k] : pr;
-                        e4m3_pair_by_divide(w, i, bf16_bits_to_float(pr & 0xffffu),
-                                            bf16_bits_to_float(pr >> 16), s);
-                    }
+                uint32_t redo = 0u;
+                if (s != 0.0f) redo = e4m3_codes_by_multiply(f, s, w);
+                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache) +
+                               row * D + l * 8;
+                *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                while (redo) {                       // rare: divide the pair, restore its codes
+                    const int i = __ffs(redo) - 1;
+                    redo &= redo - 1u;
+                    const uint32_t pr = i == 0 ? x[u].x : i == 1 ? x[u].y : i == 2 ? x[u].z : x[u].w;
+                    *reinterpret_cast<uint16_t*>(dst + 2 * i) = e4m3x2_by_divide(
+                        bf16_bits_to_float(pr & 0xffffu), bf16_bits_to_float(pr >> 16), s);
                 }
-                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
-                *reinterpret_cast<uint2*>(dst + row * D + l * 8) = make_uint2(w[0], w[1]);
             }
         }
     }
@@ -418,8 +413,6 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const float* __restr
                                                             float scale,
                                                             uint8_t* __restrict__ out,
                                                             int64_t n) {
-    const float r = __frcp_rn(scale);
-    const bool fast = quotient_fast(r);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 4;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < n;
          i += stride) {
@@ -435,12 +428,11 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const float* __restr
         }
         uint32_t w[1] = {0u};                // a zero scale writes code 0
         if (scale != 0.0f) {
-            uint32_t redo = e4m3_codes_by_multiply(f, r, fast, w);
-            while (redo) {
-                const int k = __ffs(redo) - 1;
-                redo &= redo - 1u;
-                e4m3_pair_by_divide(w, k, k ? f[2] : f[0], k ? f[3] : f[1], scale);
-            }
+            const uint32_t redo = e4m3_codes_by_multiply(f, scale, w);
+            if (redo & 1u) w[0] = (w[0] & 0xffff0000u) | e4m3x2_by_divide(f[0], f[1], scale);
+            if (redo & 2u)
+                w[0] = (w[0] & 0x0000ffffu) |
+                       (static_cast<uint32_t>(e4m3x2_by_divide(f[2], f[3], scale)) << 16);
         }
         if (i + 4 <= n && (reinterpret_cast<uintptr_t>(out + i) & 3u) == 0u) {
             *reinterpret_cast<uint32_t*>(out + i) = w[0];

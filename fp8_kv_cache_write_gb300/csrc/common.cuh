@@ -160,33 +160,66 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
         __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
-// e4m3 codes of IEEE fp32 quotients fp32(x / s) in two phases: a multiply by
-// r = __frcp_rn(s) for every value (no branches), then the IEEE divide for the
-// few pairs whose codes the multiply cannot certify.
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): value a in the low word.
+__device__ __forceinline__ uint64_t pack_f32x2(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Both products rounded to nearest even (IEEE fp32 multiplies, subnormals kept).
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// e4m3_rn_satfinite of both values of a pair (low value in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2_from_f32x2(uint64_t v) {
+    uint16_t d;
+    asm("{\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo;\n\t}"
+        : "=h"(d)
+        : "l"(v));
+    return d;
+}
+
+// e4m3 codes of IEEE fp32 quotients fp32(x / s) in two phases: multiplies by
+// two reciprocals for every value (no branches), then the IEEE divide for the
+// few pairs whose codes the multiplies cannot certify.
 //
-// Why the multiply is exact where it is used: y = fp32(x * r) has relative error
-// below 2^-22 against x / s, so y is within 6 fp32 steps (adjacent bit patterns)
-// of Q = fp32(x / s), also across a binade boundary.  Rounding to e4m3 is
-// monotone in the value, so if the patterns 16 steps below and 16 steps above y
-// encode to the same code, Q, which lies between them, encodes to it too.
-// Zeros, infinities, NaN and magnitudes within 16 steps of zero make the two
-// ends differ (their patterns cross into the other sign or into NaN), as does a
-// quotient near an e4m3 rounding midpoint (about 1 % of pairs on bf16 data,
-// whose ratios often land on one exactly).  r must be finite and nonzero
-// (quotient_fast), else every pair takes the divide.
+// Why the multiplies are exact where they are used: r = __fdividef(1, s) is
+// within 2 ulps of 1 / s for |s| in [2^-126, 2^126), so x * r is within 2^-21
+// (relative) of x / s.  With r_lo = fp32(r * (1 - 2^-19)) and
+// r_hi = fp32(r * (1 + 2^-19)), the products y_lo = fp32(x * r_lo) and
+// y_hi = fp32(x * r_hi) therefore lie on either side of Q = fp32(x / s): the
+// 2^-19 margins exceed that error plus the roundings.  Rounding to e4m3
+// (satfinite) is monotone in the value, so if y_lo and y_hi encode to the same
+// code, Q, which lies between them, encodes to it too.  This holds for zeros,
+// infinities, fp32 subnormals and overflowing products alike (they encode like
+// Q does); NaN inputs give NaN codes on both paths.  The codes differ when a
+// rounding midpoint of e4m3 lies between the two products (about 1 % of pairs
+// on bf16 data, whose ratios often land on one exactly); those pairs take the
+// divide.  Scales outside [2^-126, 2^126) send every pair to the divide.
 //
 // Phase 1 for N values: codes into w (4 per word, value 0 in the low byte);
 // returns the mask of pairs (bit i = values 2i, 2i+1) that need phase 2.
 template <int N>
-__device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], float r, bool fast,
+__device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], float s,
                                                            uint32_t (&w)[N / 4]) {
+    const uint32_t e = (__float_as_uint(s) >> 23) & 0xffu;
+    const bool fast = e >= 1u && e <= 252u;              // |s| in [2^-126, 2^126)
+    const float r = __fdividef(1.0f, s);
+    const float r_lo = __fmul_rn(r, 1.0f - 0x1p-19f);
+    const float r_hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+    const uint64_t rl = pack_f32x2(r_lo, r_lo), rh = pack_f32x2(r_hi, r_hi);
     uint32_t redo = 0u;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
-        const uint32_t b0 = __float_as_uint(__fmul_rn(f[2 * i], r));
-        const uint32_t b1 = __float_as_uint(__fmul_rn(f[2 * i + 1], r));
-        const uint32_t lo = e4m3x2_from_f32(__uint_as_float(b0 - 16u), __uint_as_float(b1 - 16u));
-        const uint32_t hi = e4m3x2_from_f32(__uint_as_float(b0 + 16u), __uint_as_float(b1 + 16u));
+        const uint64_t x2 = pack_f32x2(f[2 * i], f[2 * i + 1]);
+        const uint32_t lo = e4m3x2_from_f32x2(mul_f32x2(x2, rl));
+        const uint32_t hi = e4m3x2_from_f32x2(mul_f32x2(x2, rh));
         if (i & 1)
             w[i >> 1] |= lo << 16;
         else
@@ -196,22 +229,12 @@ __device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], 
     return fast ? redo : (N >= 64 ? ~0u : (1u << (N / 2)) - 1u);
 }
 
-// Phase 2 for pair i: codes of fp32(x0 / s), fp32(x1 / s) by IEEE divides,
-// written over the pair's two bytes in w.
-template <int NW>
-__device__ __forceinline__ void e4m3_pair_by_divide(uint32_t (&w)[NW], int i, float x0, float x1,
-                                                    float s) {
-    const uint32_t c = e4m3x2_from_f32(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-    const int sh = (i & 1) * 16;
-#pragma unroll
-    for (int k = 0; k < NW; ++k)
-        if (k == (i >> 1)) w[k] = (w[k] & ~(0xffffu << sh)) | (c << sh);
-}
-
-// The per-row inputs of phase 1: r = __frcp_rn(s) and whether it may be used
-// (r finite and nonzero).
-__device__ __forceinline__ bool quotient_fast(float r) {
-    return r != 0.0f && (__float_as_uint(r) & 0x7f800000u) != 0x7f800000u;
+// Phase 2 for one pair: codes of fp32(x0 / s), fp32(x1 / s) by IEEE divides.
+// Callers store it over the pair's two bytes after storing phase 1's codes (no
+// register array is indexed by the pair number, which would move it to local
+// memory).
+__device__ __forceinline__ uint16_t e4m3x2_by_divide(float x0, float x1, float s) {
+    return e4m3x2_from_f32(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
 // Two e4m3fn bytes (low byte first) -> f16x2, exact.

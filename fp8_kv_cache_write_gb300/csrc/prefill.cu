@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     const int G = p.G, TPT = kRows / G;                 // query tokens per tile
     const int b = blockIdx.z, h = blockIdx.y;
     const int q0 = p.cu_seqlens_q[b], nq = p.cu_seqlens_q[b + 1] - q0;
-    const int tok0 = blockIdx.x * TPT;
+    // tiles go out last-first: later query tiles see more keys (causal), so the
+    // heaviest CTAs take the first wave and the lightest fill the partial last one
+    const int tok0 = (gridDim.x - 1 - blockIdx.x) * TPT;
     if (tok0 >= nq) return;
     int ctx = p.context_lens[b];
     if (ctx > p.max_blocks_per_seq * kPage) {

@@ -208,3 +208,35 @@ def test_encoder_every_bf16_value_under_many_scales():
         keep = ~np.isnan(q)
         want = oracle.e4m3_encode(q)
         assert np.array_equal(got[keep], want[keep]), f"scale {s!r}"
+
+
+def test_bulk_write_from_pinned_host_memory():
+    # A bulk write whose K / V live in pinned host memory takes the plain-load
+    # kernel (read over the host link) and must give the same bytes as from
+    # device memory and as the oracle.
+    T, Hkv, D = 4096, 8, 128
+    nb = T // 16 + 3
+    g = torch.Generator().manual_seed(77)
+    k = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int64)
+    outs = []
+    for kin, vin in ((k.pin_memory(), v.pin_memory()), (k.cuda(), v.cuda())):
+        kc = torch.zeros(nb, Hkv, 16, D, dtype=torch.uint8, device="cuda")
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(nb, Hkv, 16, device="cuda")
+        vs = torch.zeros_like(ks)
+        fk.kv_cache_write(kin, vin, slots.cuda(), kc, vc, kv_dtype=0, scale_mode=2,
+                          k_scale_cache=ks, v_scale_cache=vs)
+        torch.cuda.synchronize()
+        outs.append([t.cpu().numpy() for t in (kc, vc, ks, vs)])
+    okc = np.zeros((nb, Hkv, 16, D), np.uint8)
+    ovc = okc.copy()
+    oks = np.zeros((nb, Hkv, 16), np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_cache_write(bits16(k), bits16(v), slots.numpy(), okc, ovc, kv_dtype=0,
+                                 scale_mode=2, k_scale_cache=oks, v_scale_cache=ovs) == 0
+    for got in outs:
+        assert np.array_equal(got[0], okc) and np.array_equal(got[1], ovc)
+        assert np.array_equal(got[2].view(np.uint32), oks.view(np.uint32))
+        assert np.array_equal(got[3].view(np.uint32), ovs.view(np.uint32))

@@ -644,6 +644,23 @@ def _extra_prefill(fk, synth, dev, stream, emit):
               "two_level": two, "ms": ms, "tflops": flops / ms / 1e9})
     del kc, vc, ksc, vsc
     torch.cuda.empty_cache()
+    # the other geometry: the 4096-query chunk after a complete 32768-token prefix
+    w2 = synth.prefill(seed=1015, ctx=(36864,), chunk=(4096,), device=dev)
+    q2, cu2 = w2.q.to(dev), w2.cu_seqlens_q.to(dev)
+    bt2, cl2 = w2.block_table.to(dev), w2.context_lens.to(dev)
+    c2 = int(w2.context_lens[0]) - int(w2.cu_seqlens_q[1])
+    flops2 = 4.0 * w2.D * w2.Hq * sum(c2 + i + 1 for i in range(int(w2.cu_seqlens_q[1])))
+    kc = torch.zeros(w2.num_blocks, w2.Hkv, 16, w2.D, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    fk.kv_cache_write(w2.k_all.to(dev), w2.v_all.to(dev), w2.all_slots.to(dev), kc, vc,
+                      kv_dtype=E4, scale_mode=0, k_scale=one, v_scale=one)
+    fn = lambda i: fk.prefill_attn(q2, cu2, w2.max_seqlen_q, kc, vc, bt2, cl2, kv_dtype=E4,
+                                   k_scale=one, v_scale=one, two_level=False, out=out)
+    ms = _time_graph(fn, 10, stream)
+    emit({"extra": "prefill_chunk4096_after_prefix32768_d256", "kv": "fp8", "two_level": False,
+          "ms": ms, "tflops": flops2 / ms / 1e9})
+    del kc, vc
+    torch.cuda.empty_cache()
 
 
 def _extra_write(fk, dev, stream, emit):

@@ -267,6 +267,18 @@ def test_prefill_config5_full_size_sampled():
         assert err <= PREFILL_TOL, (two_level, err)
 
 
+def test_prefill_after_full_prefix_sampled():
+    # the other reading of the chunked-prefill workload: 4096 new queries after a
+    # complete 32768-token prefix (positions 32768..36863 of a 36864-token cache)
+    w = synth.prefill(seed=1015, ctx=(36864,), chunk=(4096,))
+    dev_c, host_c = _caches(w)
+    units = [(t, h) for t in list(range(0, 4096, 257)) + [4095] for h in range(8)]
+    ref = _oracle(w, host_c, units)
+    out = _gpu(w, dev_c).cpu().numpy()
+    got = np.stack([out[t, h] for t, h in units])
+    assert float(np.abs(got - ref).max()) <= PREFILL_TOL
+
+
 def test_unwritten_tail_slots_do_not_leak():
     # the last page of the sequence holds NaN codes past ctx
     w = synth.prefill(seed=330, ctx=(1000,), chunk=(40,), Hq=8, Hkv=1, D=256)

@@ -528,7 +528,9 @@ def run_extras(args, dev):
 
     want = lambda name: args.extras in ("all", name)
 
-    # (1) inter-token latency against context: B=8, 32/8 heads, D=128, decode only
+    # (1) inter-token latency against context, decode only, 32/8 heads, D=128:
+    # B=8 at 2k..32k, and the single-request sweep B=1 at 1k..128k with fp8
+    # per-token-head, fp8 per-tensor and bf16, fitted as t = a + b * ctx
     for ctx in (2048, 4096, 8192, 16384, 32768) if want("itl") else ():
         w = synth.decode_workload(2000 + ctx, [ctx] * 8, 32, 8, 128, 2, device=dev)
         row = {"extra": "itl_vs_context", "B": 8, "context": ctx}
@@ -544,6 +546,35 @@ def run_extras(args, dev):
         row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
         emit(row)
         del w
+    if want("itl"):
+        variants = (("fp8_per_token_head", E4, 2), ("fp8_per_tensor", E4, 0), ("bf16", BF, 0))
+        pts = {name: [] for name, _, _ in variants}
+        for ctx in (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072):
+            row = {"extra": "itl_single_request", "B": 1, "context": ctx}
+            for name, kv, mode in variants:
+                w = synth.decode_workload(3000 + ctx, [ctx], 32, 8, 128, mode, device=dev)
+                d_b, _ = step_bytes(w, 1 if kv == E4 else 2, mode == 2)
+                caches = _caches_for(fk, w, kv, mode, dev, _copies_for(d_b))
+                ms = _time_graph(_decode_caller(fk, w, kv, mode, caches, dev), 64, stream)
+                row[name + "_us"] = ms * 1e3
+                pts[name].append((ctx, ms * 1e3))
+                del caches, w
+                torch.cuda.empty_cache()
+            emit(row)
+        fit = {"extra": "itl_single_request_fit", "B": 1, "model": "t_us = a + b * ctx"}
+        for name, _, _ in variants:
+            x = [c for c, _ in pts[name]]
+            y = [t for _, t in pts[name]]
+            n, mx, my = len(x), sum(x) / len(x), sum(y) / len(y)
+            b = sum((xi - mx) * (yi - my) for xi, yi in zip(x, y)) / sum((xi - mx) ** 2 for xi in x)
+            fit[name] = {"a_us": my - b * mx, "b_us_per_token": b}
+        bb = fit["bf16"]["b_us_per_token"]
+        for name in ("fp8_per_token_head", "fp8_per_tensor"):
+            f = fit[name]
+            f["slope_vs_bf16"] = f["b_us_per_token"] / bb
+            db = bb - f["b_us_per_token"]
+            f["break_even_ctx"] = (f["a_us"] - fit["bf16"]["a_us"]) / db if db > 0 else None
+        emit(fit)
 
     # (2)-(5) the 131072-token needle, the hybrid model, prefill, the bulk write
     if want("needle"):

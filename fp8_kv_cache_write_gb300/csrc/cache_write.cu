@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
                 while (redo) {                       // rare: reread the pair, divide, restore
                     const int i = __ffs(redo) - 1;
                     redo &= redo - 1u;
-                    const int e = i < 4 ? 2 * i : D / 2 + 2 * (i - 4);   // value index in the lane's run
+                    // byte offset of the pair's two codes from dst + 8 l
+                    const int e = i < 4 ? 2 * i : D / 2 + 2 * (i - 4);
                     const uint32_t pr = *reinterpret_cast<const uint32_t*>(
                         src + (i < 4 ? l * 16 + 4 * i : D + l * 16 + 4 * (i - 4)));
                     *reinterpret_cast<uint16_t*>(dst + l * 8 + e) = e4m3x2_by_divide(

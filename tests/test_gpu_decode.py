@@ -246,3 +246,30 @@ def test_graph_replays_match_eager_calls():
         torch.cuda.synchronize()
         assert torch.equal(got, fresh)
         assert int(err.item()) == 0
+
+
+def _large_batch_lens(seed, B, hi=1500):
+    """Ragged context lengths for more than 32 sequences: the set-up scans the
+    batch 32 sequences at a time, so empty, single-token and page-exact
+    sequences are placed past the first block too."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(0, hi, (B,), generator=g).tolist()
+    lens[3], lens[32], lens[-1] = 0, 1, 16
+    if B > 40:
+        lens[40] = 0
+    return lens
+
+
+@pytest.mark.parametrize("B", [33, 70])
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 2), (1, 0)])
+def test_decode_batches_beyond_32(B, kv_dtype, mode):
+    w = synth.decode_workload(60 + B, _large_batch_lens(60 + B, B), 8, 2, 64, mode,
+                              outlier_frac=0.01)
+    e, _, _ = _check(w, kv_dtype)
+    assert e <= DECODE_TOL, e
+
+
+def test_window_batch_beyond_32():
+    w = synth.decode_workload(61, _large_batch_lens(61, 45), 8, 2, 64, 0, window=128)
+    e, _, _ = _check(w, 1)
+    assert e <= DECODE_TOL, e

@@ -154,3 +154,21 @@ def test_graph_replays_match_eager():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 2), (1, 0)])
+def test_step_batch_beyond_32(kv_dtype, mode):
+    # 40 sequences: the set-up and the merge scan the batch 32 at a time
+    g = torch.Generator().manual_seed(47)
+    lens = torch.randint(1, 1200, (40,), generator=g).tolist()
+    lens[5], lens[32], lens[39] = 0, 1, 16
+    w = synth.decode_workload(47, lens, 16, 2, 128, mode)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gc = _history_only(w, kv_dtype, err=err)
+    out = _step(w, gc, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    oc = oracle_cache(w, kv_dtype)
+    assert_same_cache(gc, oc)
+    e = float(np.abs(out.cpu().numpy().reshape(-1, w.D) - oracle_decode(w, oc)).max())
+    assert e <= DECODE_TOL, e

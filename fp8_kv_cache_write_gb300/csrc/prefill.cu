@@ -510,13 +510,13 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             float vmax = 0.f;                   // PT: this half's largest V scale
             if constexpr (PT) {
-                const int nval = ctx - key0;    // keys of this half with written scales
-                if (nval >= kKH) {
-#pragma unroll 16
-                    for (int i = 0; i < kKH; ++i) vmax = fmaxf(vmax, vsl[i]);
-                } else {
-                    for (int i = 0; i < nval; ++i) vmax = fmaxf(vmax, vsl[i]);
-                }
+                // every lane of the warp works on this half: the lanes share the
+                // keys with written scales and meet in a shuffle reduction
+                const int nval = min(ctx - key0, kKH);
+                for (int i = lane; i < nval; i += 32) vmax = fmaxf(vmax, vsl[i]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
                 ebuf[st * 2 + kh] = vmax;       // every thread of the half: the same value
             }
             if constexpr (kHalves == 2) {       // the row's max over both halves

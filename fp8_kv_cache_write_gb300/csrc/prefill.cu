@@ -89,7 +89,12 @@ struct PCfg {
     static constexpr int kOffScl = kOffBar + kNumBars * 8;
     static constexpr int kSclBytes = BF16 ? 0 : 4 * 1024 + 16 * 4;
     static constexpr int kOffMisc = kOffScl + kSclBytes;    // tmem slot, abort flag
-    static constexpr int kSmem = 1024 + kOffMisc + 16;
+    // per-token-head scales: each softmax warp's column factors of the current
+    // tile, [64] for the logits (k scale x logit scale), [64] for the weights
+    // (v scale / bound)
+    static constexpr int kOffPtf = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr int kPtfBytes = BF16 ? 0 : kSoftWarps * 128 * 4;
+    static constexpr int kSmem = 1024 + kOffPtf + kPtfBytes;
 };
 
 // barrier indices
@@ -478,17 +483,24 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             const float* ksl = reinterpret_cast<const float*>(smem + C::kOffScl + (j & 3) * 1024) +
                                kh * kKH;
             const float* vsl = ksl + 128;
+            // PT: this warp's column factors (every lane of the warp works on this half)
+            float* ptf = reinterpret_cast<float*>(smem + C::kOffPtf) + warp * 128;
             if constexpr (PT) {
+                static_assert(kKH == 64, "per-token-head tiles: 64 keys a half");
+                __syncwarp();                   // the previous tile's factors are read
+                ptf[lane] = ksl[lane] * sc;
+                ptf[lane + 32] = ksl[lane + 32] * sc;
+                __syncwarp();
                 if (full) {
 #pragma unroll
                     for (int i = 0; i < kKH; ++i) {
-                        s[i] = __uint_as_float(sb[i]) * (ksl[i] * sc);
+                        s[i] = __uint_as_float(sb[i]) * ptf[i];
                         mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < kKH; ++i) {
-                        s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) * (ksl[i] * sc)
+                        s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) * ptf[i]
                                                  : -__int_as_float(0x7f800000);
                         mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
                     }
@@ -586,6 +598,12 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             const float moff = m + lps;
             // PT: weight = p * s_v * kHeadPT / (E prob_scale), the unfolded p into l
             const float vinv = PT && e_run > 0.f ? kHeadPT / (e_run * ps) : 0.f;
+            if constexpr (PT) {
+                __syncwarp();                   // the previous tile's factors are read
+                ptf[64 + lane] = vsl[lane] * vinv;
+                ptf[96 + lane] = vsl[lane + 32] * vinv;
+                __syncwarp();
+            }
 #pragma unroll
             for (int c8 = 0; c8 < kMyChunks; ++c8) {
                 const int cc = kh * kMyChunks + c8;
@@ -598,8 +616,8 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                         l += pa + pb;
                         // masked keys: p = 0 and a stale scale that must not enter
                         const bool va = full || key0 + ia <= pos_r, vb = full || key0 + ib <= pos_r;
-                        const uint32_t code = e4m3x2_from_f32(va ? pa * vsl[ia] * vinv : 0.f,
-                                                              vb ? pb * vsl[ib] * vinv : 0.f);
+                        const uint32_t code = e4m3x2_from_f32(va ? pa * ptf[64 + ia] : 0.f,
+                                                              vb ? pb * ptf[64 + ib] : 0.f);
                         if (i & 1)
                             w[i >> 1] |= code << 16;
                         else

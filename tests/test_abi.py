@@ -107,3 +107,27 @@ def test_quantize_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), 5, _null()) == -1
     assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), 0, _null()) == 0
     assert lib.fp8kv_quantize_e4m3(_null(), 1.0, _null(), -1, _null()) == -1
+
+
+def test_prefill_rejects_bad_arguments_without_a_gpu(lib):
+    N = _null()
+
+    def call(B=1, Hq=8, Hkv=1, D=256, dtype=0, mode=0, q_scale=1.0, prob_scale=1.0,
+             two_level=0, out_dtype=0, max_q=128):
+        return lib.fp8kv_prefill_attn(N, N, max_q, N, N, dtype, mode, N, N, N, N, q_scale,
+                                      prob_scale, N, 4, N, B, Hq, Hkv, D, 10, 0.0625, two_level,
+                                      N, out_dtype, N, N)
+
+    assert call() == -1                 # null pointers
+    assert call(Hq=9, Hkv=2) == -1      # Hq % Hkv
+    assert call(Hq=9) == -2             # a group of 9 does not tile 128 MMA rows
+    assert call(D=64) == -2             # prefill tiles: D 128 or 256
+    assert call(dtype=2) == -1
+    assert call(mode=3) == -1
+    assert call(out_dtype=2) == -1
+    assert call(two_level=2) == -1
+    assert call(q_scale=0.0) == -1
+    assert call(prob_scale=-1.0) == -1
+    assert call(max_q=-1) == -1
+    assert call(B=0) == 0               # nothing to do, nothing launched
+    assert call(max_q=0) == 0

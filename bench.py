@@ -695,30 +695,35 @@ def _extra_prefill(fk, synth, dev, stream, emit):
 
 
 def _extra_write(fk, dev, stream, emit):
-    # bulk cache write: 32768 tokens x 8 KV heads x 128, per-token-head e4m3
+    # bulk cache write, 8 KV heads x 128, per-token-head e4m3: 32768 tokens, and the
+    # whole 158367-token history of the Llama-3.1-8B-shaped decode workload
     E4 = fk.KV_E4M3
-    T, H, D = 32768, 8, 128
-    gen = torch.Generator(device=dev).manual_seed(6)
-    sets = []
-    for _ in range(2):
-        k = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
-        v = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
-        sets.append((k, v))
-    # prefill-style slots: 16 consecutive tokens per page, pages in shuffled order
-    nb = T // 16 + 16
-    pages = torch.randperm(nb, generator=gen, device=dev)[:T // 16].to(torch.int64)
-    slots = (pages[:, None] * 16 + torch.arange(16, device=dev)).reshape(-1)
-    kc = torch.zeros(nb, H, 16, D, dtype=torch.uint8, device=dev)
-    vc = torch.zeros_like(kc)
-    ks = torch.zeros(nb, H, 16, dtype=torch.float32, device=dev)
-    vs = torch.zeros_like(ks)
-    fn = lambda i: fk.kv_cache_write(sets[i % 2][0], sets[i % 2][1], slots, kc, vc,
-                                     kv_dtype=E4, scale_mode=2, k_scale_cache=ks,
-                                     v_scale_cache=vs)
-    ms = _time_graph(fn, 20, stream)
-    nbytes = T * H * (2 * D * 2 + 2 * D + 8) + T * 8
-    emit({"extra": "bulk_cache_write", "tokens": T, "Hkv": H, "D": D, "us": ms * 1e3,
-          "gbs": nbytes / ms / 1e6})
+    H, D = 8, 128
+    for T in (32768, 158367):
+        gen = torch.Generator(device=dev).manual_seed(6)
+        sets = []
+        for _ in range(2):
+            k = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
+            v = torch.randn(T, H, D, generator=gen, device=dev).to(torch.bfloat16)
+            sets.append((k, v))
+        # prefill-style slots: 16 consecutive tokens per page, pages in shuffled order
+        npages = (T + 15) // 16
+        nb = npages + 16
+        pages = torch.randperm(nb, generator=gen, device=dev)[:npages].to(torch.int64)
+        slots = (pages[:, None] * 16 + torch.arange(16, device=dev)).reshape(-1)[:T].contiguous()
+        kc = torch.zeros(nb, H, 16, D, dtype=torch.uint8, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(nb, H, 16, dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        fn = lambda i: fk.kv_cache_write(sets[i % 2][0], sets[i % 2][1], slots, kc, vc,
+                                         kv_dtype=E4, scale_mode=2, k_scale_cache=ks,
+                                         v_scale_cache=vs)
+        ms = _time_graph(fn, 20, stream)
+        nbytes = T * H * (2 * D * 2 + 2 * D + 8) + T * 8
+        emit({"extra": "bulk_cache_write", "tokens": T, "Hkv": H, "D": D, "us": ms * 1e3,
+              "gbs": nbytes / ms / 1e6})
+        del sets, kc, vc, ks, vs
+        torch.cuda.empty_cache()
 
 
 def main():

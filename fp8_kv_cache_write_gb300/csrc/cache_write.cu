@@ -365,18 +365,24 @@ static cudaError_t launch_write_staged(const WriteParams& p, cudaStream_t stream
 }
 
 // The staged kernel reads K and V with bulk copies; it runs for bulk writes
-// whose inputs are device memory (pinned host inputs take the direct kernel,
-// whose plain loads read them over the host link).
+// whose inputs are device memory of the current GPU (pinned host inputs take the
+// direct kernel, whose plain loads read them over the host link).
 static bool use_staged(const WriteParams& p) {
     if (p.T * p.Hkv < staged::kMinRows) return false;
     RelaxedCapture relaxed;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
     for (const void* ptr : {static_cast<const void*>(p.k), static_cast<const void*>(p.v)}) {
         cudaPointerAttributes a{};
         if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        if (a.type != cudaMemoryTypeDevice) return false;
+        // device memory of this GPU only (peer or managed memory takes the plain loads)
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
     }
     return true;
 }

@@ -169,3 +169,57 @@ def test_outlier_channels_keep_small_values_resolvable(D):
     y = xv / ksc[0, 0, :8, None]
     bound = (_half_quantum(y) + np.abs(y) * 2.0 ** -23) * ksc[0, 0, :8, None]
     assert np.all(np.abs(dq - xv) <= bound * (1 + 1e-12))
+
+
+def _torch_e4m3(y):
+    """e4m3fn codes by torch's own cast (round to nearest even); valid for |y| <= 464,
+    where torch and satfinite agree."""
+    t = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_per_token_head_is_the_ieee_quotient():
+    # "Per-Token-Head vs Per-Tensor 양자화": scale = amax / 448 and code = e4m3 of
+    # x / scale.  Both are single IEEE fp32 divisions (numpy's float32 '/' is one),
+    # so the stored scale and every code must equal them bit for bit.  Rows with
+    # x20 outlier channels make scales far from powers of two, where x * fp32(1/s)
+    # and fp32(amax * fp32(1/448)) differ from the quotients: the test requires
+    # that such values occur, so an oracle that multiplies by a reciprocal fails.
+    T, Hkv, D, nb = 256, 4, 128, 64
+    g = torch.Generator().manual_seed(77)
+    k = torch.randn(T, Hkv, D, generator=g)
+    v = torch.randn(T, Hkv, D, generator=g) * 3.0
+    idx = torch.randperm(Hkv * D, generator=g)[: int(np.ceil(0.01 * Hkv * D))]
+    for x in (k, v):
+        for i in idx.tolist():
+            h, c = divmod(i, D)
+            x[:, h, c] *= 20.0
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    slots = np.random.default_rng(5).permutation(nb * PAGE)[:T].astype(np.int64)
+    kc, vc = _empty(nb, Hkv, D), _empty(nb, Hkv, D)
+    ksc = np.full((nb, Hkv, PAGE), -7.0, np.float32)
+    vsc = np.full((nb, Hkv, PAGE), -7.0, np.float32)
+    assert oracle.kv_cache_write(bits16(k), bits16(v), slots, kc, vc, kv_dtype=0, scale_mode=2,
+                                 k_scale_cache=ksc, v_scale_cache=vsc) == 0
+    recip_scale_differs = recip_code_differs = 0
+    for x, cache, sc in ((k, kc, ksc), (v, vc, vsc)):
+        xf = bf16_value(bits16(x)).astype(np.float32)        # exact: bf16 -> fp32
+        blk, off = np.divmod(slots, PAGE)
+        got_s = sc[blk, :, off]                              # [T][Hkv]
+        got_c = cache[blk, :, off]                           # [T][Hkv][D]
+        amax = np.abs(xf).max(axis=2)
+        want_s = amax / np.float32(448.0)
+        assert want_s.dtype == np.float32
+        assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32))
+        recip_scale_differs += int(np.count_nonzero(
+            (amax * (np.float32(1.0) / np.float32(448.0))).view(np.uint32)
+            != want_s.view(np.uint32)))
+        y = xf / want_s[:, :, None]                          # IEEE fp32 quotients
+        assert y.dtype == np.float32 and np.abs(y).max() <= 464.0
+        want_c = _torch_e4m3(y)
+        assert np.array_equal(got_c, want_c)
+        assert np.array_equal(got_c, oracle.e4m3_encode(y))
+        y_recip = xf * (np.float32(1.0) / want_s)[:, :, None]
+        recip_code_differs += int(np.count_nonzero(_torch_e4m3(y_recip) != want_c))
+    assert recip_scale_differs > 0
+    assert recip_code_differs > 0

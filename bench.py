@@ -267,17 +267,20 @@ def run_ours(args, dev, w, world, rank):
             kc, vc, ks, vs = caches[i % args.rotations]
             fk.paged_decode_attn(q_in, kc, vc, bt, cl_in, kv_dtype=kv_dtype, scale_mode=mode,
                                  k_scale_cache=ks, v_scale_cache=vs, workspace=ws, out=out,
-                                 num_splits=args.splits, err_flag=err)
+                                 num_splits=args.splits, flags=args.decode_flags, err_flag=err)
 
         def split_step(i):
             write(i)
             decode(i)
 
-        def step(i, q_in=q, k_in=kn, v_in=vn, cl_in=cl, out_t=out):
+        def step(i, q_in=q, k_in=kn, v_in=vn, cl_in=cl, out_t=out, flags=args.decode_flags):
             kc, vc, ks, vs = caches[i % args.rotations]
             fk.decode_step(q_in, k_in, v_in, kc, vc, bt, cl_in, kv_dtype=kv_dtype,
                            scale_mode=mode, k_scale_cache=ks, v_scale_cache=vs, workspace=ws,
-                           out=out_t, num_splits=args.splits, err_flag=err)
+                           out=out_t, num_splits=args.splits, flags=flags, err_flag=err)
+
+        def step_wait_first(i):
+            step(i, flags=0)
 
         with torch.cuda.stream(cap):
             for i in range(args.warmup):             # eager warm-up (also first-call setup)
@@ -287,10 +290,12 @@ def run_ours(args, dev, w, world, rank):
         graphs = _capture_steps(step, K, per_graph, cap)
         sgraph = _capture_steps(split_step, K, per_graph, cap)
         dgraph = _capture_steps(decode, K, per_graph, cap)
+        wgraph = _capture_steps(step_wait_first, K, per_graph, cap)
         for _ in range(max(1, args.warmup // per_graph)):
             graphs[0].replay()
             sgraph[0].replay()
             dgraph[0].replay()
+            wgraph[0].replay()
         torch.cuda.synchronize(dev)
 
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -320,9 +325,16 @@ def run_ours(args, dev, w, world, rank):
             t1.record(cap)
         torch.cuda.synchronize(dev)
         split_ms = t0.elapsed_time(t1) / K
+        with torch.cuda.stream(cap):
+            t0.record(cap)
+            _replay_steps(wgraph, K, cap)
+            t1.record(cap)
+        torch.cuda.synchronize(dev)
+        wait_first_ms = t0.elapsed_time(t1) / K
         gbs, tok_s, tmax = aggregate(d_b + w_b, w.B, secs, K)
         results[name] = {"gbs": gbs, "tokens_per_s": tok_s, "ms_per_step": tmax / K * 1e3,
-                         "decode_ms": dec_ms, "split_step_ms": split_ms, "num_splits": splits,
+                         "decode_ms": dec_ms, "split_step_ms": split_ms,
+                         "wait_first_step_ms": wait_first_ms, "num_splits": splits,
                          "clocks": clocks, "secs": tmax}
         if int(err.item()) != 0:
             raise RuntimeError(f"device error flag {int(err.item())} during the {name} run")
@@ -365,7 +377,7 @@ def run_ours(args, dev, w, world, rank):
                                      "host memory (kernel loads/stores over the host link); steps "
                                      "replayed as CUDA graphs"}
             del egraphs
-        del graphs, sgraph, dgraph, caches
+        del graphs, sgraph, dgraph, wgraph, caches
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
     return results, dec_bytes, launches_per_step
@@ -739,6 +751,10 @@ def main():
     ap.add_argument("--rotations", type=int, default=ROTATIONS,
                     help="cache copies rotated between steps (each larger than L2)")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planner)")
+    ap.add_argument("--decode-flags", type=int, default=2,
+                    help="decode launch-overlap flags (0 = wait for the preceding kernel "
+                         "first; 2 = early set-up and page streaming: the step's tables and "
+                         "older pages are written before the preceding kernel starts)")
     ap.add_argument("--extras", nargs="?", const="all", default=None,
                     choices=["all", "itl", "needle", "hybrid", "prefill", "write"],
                     help="time the other workloads (context sweep, needle, hybrid, prefill, "
@@ -786,6 +802,7 @@ def main():
             print(json.dumps({"only": args.only, "splits": r["num_splits"],
                               "step_gbs": r["gbs"], "ms_per_step": r["ms_per_step"],
                               "decode_ms": r["decode_ms"], "split_step_ms": r["split_step_ms"],
+                              "wait_first_step_ms": r["wait_first_step_ms"],
                               "decode_gbs": dec_bytes[args.only] / r["decode_ms"] / 1e6,
                               "tokens_per_s": r["tokens_per_s"], "clocks": r["clocks"]}),
                   flush=True)
@@ -808,7 +825,9 @@ def main():
                            "parallelism": f"replicas x{world}",
                            "l2": f"{args.rotations} rotating cache copies, each larger than L2",
                            "num_splits": fp8["num_splits"],
+                           "decode_flags": args.decode_flags,
                            "timing": "CUDA graphs of whole steps replayed back to back"},
+                "wait_first_ms_per_step": fp8["wait_first_step_ms"],
                 "pct_of_peak": fp8["gbs"] / peak,
                 "tokens_per_s": fp8["tokens_per_s"],
                 "bf16_twin": {"value": bf16["gbs"], "unit": "GB/s",

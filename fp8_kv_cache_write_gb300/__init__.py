@@ -22,6 +22,8 @@ PAGE_SIZE = 16
 KV_E4M3, KV_BF16 = 0, 1
 SCALE_PER_TENSOR, SCALE_PER_HEAD, SCALE_PER_TOKEN_HEAD = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
+# decode flags (include/fp8kv.h): what may run before the preceding kernel ends
+DECODE_EARLY_SETUP, DECODE_EARLY_PAGES = 1, 2
 
 STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -3: "FP8KV_ERR_WORKSPACE", -4: "FP8KV_ERR_CUDA", -5: "FP8KV_ERR_TIMEOUT",
@@ -58,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                 ctypes.c_size_t)
+        u32 = ctypes.c_uint
         L.fp8kv_kv_cache_write.argtypes = [P, P, P, i64, i32, i32, P, P, i64, i32, i32, P, P, P,
                                            P, P, P]
         L.fp8kv_kv_cache_write.restype = i32
@@ -65,10 +68,11 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(i32), ctypes.POINTER(sz)]
         L.fp8kv_decode_plan.restype = i32
         L.fp8kv_paged_decode_attn.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
-                                              i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
+                                              i32, i32, i64, f32, i32, i32, P, sz, P, i32, u32, P,
+                                              P]
         L.fp8kv_paged_decode_attn.restype = i32
         L.fp8kv_decode_step.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, i32, P, i32, i32,
-                                        i32, i32, i64, f32, i32, i32, P, sz, P, i32, P, P]
+                                        i32, i32, i64, f32, i32, i32, P, sz, P, i32, u32, P, P]
         L.fp8kv_decode_step.restype = i32
         L.fp8kv_paged_decode_attn_noalloc.argtypes = [P, P, P, i32, i32, P, P, P, P, P, i32, P,
                                                       i32, i32, i32, i32, i64, f32, i32, i32, P,
@@ -162,10 +166,11 @@ def decode_plan(B, Hq, Hkv, D, max_blocks_per_seq, window=0, num_splits=0):
 def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtype,
                       scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
                       k_scale_cache=None, v_scale_cache=None, softmax_scale=None, window=0,
-                      num_splits=0, workspace=None, out=None, out_dtype=OUT_F32, err_flag=None,
-                      stream=None):
+                      num_splits=0, workspace=None, out=None, out_dtype=OUT_F32, flags=0,
+                      err_flag=None, stream=None):
     """Decode attention of q [B][Hq][D] (bf16) over the paged cache; returns out
-    [B][Hq][D] (fp32 or bf16).  See fp8kv_paged_decode_attn."""
+    [B][Hq][D] (fp32 or bf16).  flags: 0 or DECODE_EARLY_SETUP / DECODE_EARLY_PAGES.
+    See fp8kv_paged_decode_attn."""
     _check(q, "q", torch.bfloat16, pinned_ok=True)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check(t, n, torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16)
@@ -194,7 +199,7 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
         _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), int(window),
         int(num_splits), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
-        out_dtype, _ptr(err_flag), _stream(stream))
+        out_dtype, int(flags), _ptr(err_flag), _stream(stream))
     _raise(st, "paged_decode_attn")
     return out
 
@@ -202,7 +207,7 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, context_lens, *, kv_dtyp
 def decode_step(q, k_new, v_new, k_cache, v_cache, block_table, context_lens, *, kv_dtype,
                 scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None, k_scale_cache=None,
                 v_scale_cache=None, softmax_scale=None, window=0, num_splits=0, workspace=None,
-                out=None, out_dtype=OUT_F32, err_flag=None, stream=None):
+                out=None, out_dtype=OUT_F32, flags=0, err_flag=None, stream=None):
     """One decode step in one call: stores the new token k_new / v_new [B][Hkv][D]
     (bf16) of every sequence at position context_lens[b] - 1 of its page table
     (quantized as kv_cache_write does), then attends q [B][Hq][D] over all its
@@ -239,7 +244,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, block_table, context_lens, *,
         _ptr(block_table), mbs, _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0],
         float(softmax_scale), int(window), int(num_splits), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(out),
-        out_dtype, _ptr(err_flag), _stream(stream))
+        out_dtype, int(flags), _ptr(err_flag), _stream(stream))
     _raise(st, "decode_step")
     return out
 
@@ -272,10 +277,17 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
         _ptr(context_lens), B, Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), int(window),
         int(num_splits), _ptr(out), out_dtype, _ptr(err_flag), _stream(stream))
     if st == -3:
+        if num_splits == 0:
+            raise Fp8kvError(st, f"paged_decode_attn_noalloc: one split slot per (sequence, KV "
+                                 f"head) already needs B*Hq*(D+2)*4 = {B * Hq * (D + 2) * 4} "
+                                 f"bytes, more than the static array's "
+                                 f"{NOALLOC_DECODE_SCRATCH_BYTES}; use paged_decode_attn with "
+                                 f"a workspace")
         _, need = decode_plan(B, Hq, Hkv, D, mbs, window, num_splits)
         raise Fp8kvError(st, f"paged_decode_attn_noalloc: the split plan needs {need} bytes of "
                              f"scratch but the static array holds "
-                             f"{NOALLOC_DECODE_SCRATCH_BYTES}; pass fewer num_splits")
+                             f"{NOALLOC_DECODE_SCRATCH_BYTES}; pass fewer num_splits (or 0) or "
+                             f"use paged_decode_attn with a workspace")
     _raise(st, "paged_decode_attn_noalloc")
     return out
 

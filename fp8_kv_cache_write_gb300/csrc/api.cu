@@ -13,6 +13,56 @@
 #include "../../include/fp8kv.h"
 #include "internal.h"
 
+namespace fp8kv {
+
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrent>(a);
+            get_id = reinterpret_cast<GetId>(b);
+        } else {
+            cudaGetLastError();
+        }
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id + 1;
+}
+
+cudaError_t opt_in_smem(const void* func, int bytes, unsigned long long (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long id = current_context_id();
+    if (dev >= 0 && dev < 64 && id != 0 && done[dev] == id) return cudaSuccess;
+    // a setting, not a stream operation: allowed while another thread captures
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = current_context_id();
+    return cudaSuccess;
+}
+
+}  // namespace fp8kv
+
 namespace {
 
 using namespace fp8kv;
@@ -115,10 +165,12 @@ struct Plan {
 // Decode planner.  The launch's (seq, KV head, page) tiles are split evenly over
 // the 4 warps of `num_splits` CTAs.  Automatic: one wave of resident CTAs, but no fewer than
 // 16 tiles per CTA for the upper bound of the work (B * Hkv * visible pages);
-// an explicit count n asks for about n partitions per (seq, KV head) unit.
+// an explicit count n asks for about n partitions per (seq, KV head) unit;
+// max_ctas > 0 caps the CTA count.
 // Workspace: one (m, l, O) slot per (warp, unit) pair a warp can touch, i.e.
 // 4 * num_splits + B * Hkv slots of G query heads.
-int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out) {
+int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out,
+         int64_t max_ctas = 0) {
     int maxvis = max_blocks;
     if (window > 0) {
         const int wp = (window + FP8KV_PAGE_SIZE - 1) / FP8KV_PAGE_SIZE + 1;
@@ -137,6 +189,7 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     }
     if (n > work) n = work;
     if (n > 1024) n = 1024;
+    if (max_ctas > 0 && n > max_ctas) n = max_ctas;
     if (n < 1) n = 1;
     out->num_splits = static_cast<int>(n);
     const int64_t G = Hkv > 0 ? Hq / Hkv : 1;
@@ -280,10 +333,12 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
                  const int32_t* block_table, int max_blocks_per_seq, const int32_t* context_lens,
                  int B, int Hq, int Hkv, int D, int64_t num_blocks, float softmax_scale,
                  int window, int num_splits, void* workspace, size_t workspace_bytes, void* out,
-                 int out_dtype, int32_t* err_flag, void* cuda_stream) {
+                 int out_dtype, unsigned flags, int32_t* err_flag, void* cuda_stream,
+                 int64_t max_ctas = 0) {
     const bool fused = k_new != nullptr || v_new != nullptr;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || window < 0 || num_splits < 0 ||
-        max_blocks_per_seq < 0 || num_blocks < 0)
+        max_blocks_per_seq < 0 || num_blocks < 0 ||
+        (flags & ~(FP8KV_DECODE_EARLY_SETUP | FP8KV_DECODE_EARLY_PAGES)) != 0)
         return FP8KV_ERR_INVALID;
     if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
     if (Hq / Hkv > 8) return FP8KV_ERR_UNSUPPORTED;
@@ -324,7 +379,7 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
         }
     }
     Plan pl;
-    plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &pl);
+    plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &pl, max_ctas);
     if (!workspace || workspace_bytes < pl.workspace_bytes) return FP8KV_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
@@ -361,6 +416,7 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
     p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
+    p.flags = flags;
     p.err = err_flag;
     if (fused) {
         p.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -375,6 +431,35 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
 
 }  // namespace
 
+namespace fp8kv {
+
+int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_cache,
+                              int kv_dtype, int scale_mode, const float* k_scale,
+                              const float* v_scale, const float* k_scale_cache,
+                              const float* v_scale_cache, const int32_t* block_table,
+                              int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
+                              int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
+                              int num_splits, void* scratch, size_t scratch_bytes, void* out,
+                              int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    g_warning.clear();
+    int64_t max_ctas = 0;
+    if (num_splits == 0 && Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 && valid_d(D)) {
+        // slots that fit, less the one per unit, over the 4 worker warps of a CTA
+        const int64_t slot_bytes = static_cast<int64_t>(Hq / Hkv) * (D + 2) * sizeof(float);
+        const int64_t spare = static_cast<int64_t>(scratch_bytes) / slot_bytes -
+                              static_cast<int64_t>(B) * Hkv;
+        max_ctas = spare / kDecodeWarps;
+        if (max_ctas < 1) return FP8KV_ERR_WORKSPACE;
+    }
+    return paged_decode(q, nullptr, nullptr, k_cache, v_cache, kv_dtype, scale_mode, k_scale,
+                        v_scale, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
+                        context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, window,
+                        num_splits, scratch, scratch_bytes, out, out_dtype, 0u, err_flag,
+                        cuda_stream, max_ctas);
+}
+
+}  // namespace fp8kv
+
 extern "C" {
 
 int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -384,12 +469,12 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
                             int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
                             int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
                             int num_splits, void* workspace, size_t workspace_bytes, void* out,
-                            int out_dtype, int32_t* err_flag, void* cuda_stream) {
+                            int out_dtype, unsigned flags, int32_t* err_flag, void* cuda_stream) {
     g_warning.clear();
     return paged_decode(q, nullptr, nullptr, k_cache, v_cache, kv_dtype, scale_mode, k_scale,
                         v_scale, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
                         context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, window,
-                        num_splits, workspace, workspace_bytes, out, out_dtype, err_flag,
+                        num_splits, workspace, workspace_bytes, out, out_dtype, flags, err_flag,
                         cuda_stream);
 }
 
@@ -400,13 +485,13 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
                       const int32_t* context_lens, int B, int Hq, int Hkv, int D,
                       int64_t num_blocks, float softmax_scale, int window, int num_splits,
                       void* workspace, size_t workspace_bytes, void* out, int out_dtype,
-                      int32_t* err_flag, void* cuda_stream) {
+                      unsigned flags, int32_t* err_flag, void* cuda_stream) {
     g_warning.clear();
     if (!k_new || !v_new) return FP8KV_ERR_INVALID;
     return paged_decode(q, k_new, v_new, k_cache, v_cache, kv_dtype, scale_mode, k_scale,
                         v_scale, k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
                         context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, window,
-                        num_splits, workspace, workspace_bytes, out, out_dtype, err_flag,
+                        num_splits, workspace, workspace_bytes, out, out_dtype, flags, err_flag,
                         cuda_stream);
 }
 

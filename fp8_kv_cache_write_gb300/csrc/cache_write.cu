@@ -338,16 +338,9 @@ static cudaError_t launch_write_staged(const WriteParams& p, cudaStream_t stream
     using namespace staged;
     constexpr int64_t kMaxRows = kTileBytes / (D * 2);
     auto kern = kv_cache_write_staged_kernel<D, MODE, BF16>;
-    static bool attr_done[64] = {};          // large dynamic shared memory, once per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static unsigned long long attr_done[64] = {};   // large dynamic shared memory, once per context
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        RelaxedCapture relaxed;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
     // equal chunk counts per CTA: as many chunk rounds as full-size chunks need,
     // then the chunk size that spreads the rows evenly over them
     const int64_t rows = p.T * p.Hkv;

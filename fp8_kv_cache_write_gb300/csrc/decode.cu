@@ -297,12 +297,16 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     const int g = lane >> 2, c = lane & 3;
     const int G = p.G;
     pdl_trigger();                        // split_merge may launch while this runs
-    // The set-up below -- shares, segments, page-table rows -- reads only
-    // context_lens, block_table and the constant scales, which must be complete
-    // before the preceding kernel of the stream starts; it overlaps that kernel's
-    // tail.  The wait for it comes before the first cache load or workspace write
-    // (FUSED: before the first read of q, k_new or v_new and the first write; the
-    // cache pages, complete before the preceding kernel started, stream first).
+    // Ordering against the preceding kernel of the stream (programmatic launch):
+    // by default the kernel waits for it before reading any global memory.  With
+    // FP8KV_DECODE_EARLY_SETUP the set-up below -- shares, segments, page-table
+    // rows, which read only context_lens, block_table and the constant scales --
+    // overlaps that kernel's tail (the caller guarantees those are complete
+    // before it starts); with FP8KV_DECODE_EARLY_PAGES the first cache pages
+    // stream before the wait too.  q, k_new, v_new and the workspace are read,
+    // and anything is written, only after the wait.
+    const bool early_setup = (p.flags & (FP8KV_DECODE_EARLY_SETUP | FP8KV_DECODE_EARLY_PAGES)) != 0;
+    const bool early_pages = (p.flags & FP8KV_DECODE_EARLY_PAGES) != 0;
 
     uint8_t* ring = smem + warp * C::kWarpSmem;
     uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
@@ -320,6 +324,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
     }
+    if (!early_setup) pdl_wait();         // the preceding kernel's writes are visible
     // the page table's lines reach L2 while the context lengths are read (the
     // CTAs share the prefetch line by line)
     if (warp == 0) {
@@ -708,9 +713,9 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int si = 0; si < nseg; ++si)
             total_groups += (seg[kSegInts * si + 3] - seg[kSegInts * si + 2] + PPI - 1) / PPI;
         const int pre = total_groups < C::kStages ? total_groups : C::kStages;
-        if constexpr (!FUSED) pdl_wait();   // the preceding kernel's results are visible
+        if (!early_pages) pdl_wait();       // the preceding kernel's results are visible
         for (int q = 0; q < pre; ++q) issue_next();
-        if constexpr (FUSED) pdl_wait();
+        if (early_pages) pdl_wait();
 
         int consumed = 0;
         for (int si = 0; si < nseg && !timed_out; ++si) {
@@ -967,7 +972,11 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     const int G = p.G, h = hq / G, head = hq % G;
     const int unit = b * p.Hkv + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nvis = vis_pages(p, b);           // context_lens: complete before the chain
+    // context_lens are read before the wait only when the caller allows it (the
+    // decode kernel lets this one start early; it has waited for its own
+    // predecessor, so after this wait everything before it is visible too)
+    if ((p.flags & (FP8KV_DECODE_EARLY_SETUP | FP8KV_DECODE_EARLY_PAGES)) == 0) pdl_wait();
+    const int nvis = vis_pages(p, b);
     // the workers whose shares meet the unit: the decode kernel split the W
     // tiles of the launch as worker w <- [floor(w W / n), floor((w+1) W / n)),
     // so tile t belongs to worker floor(((t+1) n - 1) / W)
@@ -1062,16 +1071,10 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     using C = Cfg<D, BF16>;
     constexpr int kSmemBytes = FUSED ? C::kSmemFused : C::kSmem;
     auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED>;
-    // opt in to the large dynamic shared-memory size once per device
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // opt in to the large dynamic shared-memory size once per context
+    static unsigned long long attr_done[64] = {};
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmemBytes, attr_done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
     // both kernels may start before their predecessor in the stream ends (they
     // wait for its results in-kernel): launch latency and set-up overlap
     cudaLaunchAttribute attr[1];

@@ -16,10 +16,15 @@
 //     overlap on the GPU (different streams, or different host threads) race;
 //     serialize them, e.g. on one stream;
 //   * the first call on each device looks up the array's device address (with
-//     that device current); make that first call before any stream capture;
-//   * a call whose split plan (fp8kv_decode_plan) needs more bytes than the
-//     array holds is rejected with FP8KV_ERR_WORKSPACE and launches nothing;
-//     fewer splits (num_splits) or the allocating entry point are the remedies.
+//     that device current), and so does the first call after the device's
+//     context was recreated (cudaDeviceReset); make those calls outside stream
+//     capture;
+//   * with num_splits 0 the automatic plan is lowered to the largest CTA count
+//     whose partials fit the array; a call that cannot fit even one CTA (the
+//     B * Hq * (D + 2) * 4 bytes of one slot per unit alone exceed the array),
+//     or whose explicit num_splits plan does not fit, is rejected with
+//     FP8KV_ERR_WORKSPACE and launches nothing: the allocating entry point is
+//     the remedy.
 // The partials need no initial value: every split the merge reads is written by
 // the same call first, so nothing is cleared between calls.
 #include <cuda_runtime.h>
@@ -27,6 +32,7 @@
 #include <mutex>
 
 #include "../../include/fp8kv.h"
+#include "internal.h"
 
 namespace {
 
@@ -35,27 +41,35 @@ constexpr size_t kScratchBytes = FP8KV_NOALLOC_DECODE_SCRATCH_BYTES;
 // The split partials' home on every device (fp32, 256-byte aligned).
 static __device__ __align__(256) float g_decode_scratch[kScratchBytes / sizeof(float)];
 
-// Device address of g_decode_scratch on the current device, looked up once
-// per device.  In host code the symbol is only a host-side stand-in, never a
-// device address, so kernels always receive the looked-up pointer.
+// Device address of g_decode_scratch in the current context, looked up once per
+// device and again whenever that device's context is a new one (after
+// cudaDeviceReset the old address is gone).  In host code the symbol is only a
+// host-side stand-in, never a device address, so kernels always receive the
+// looked-up pointer.
 int scratch_on_current_device(void** out) {
+    struct Entry {
+        unsigned long long ctx;
+        void* addr;
+    };
     static std::mutex mu;
-    static void* addr[64] = {};
+    static Entry cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return FP8KV_ERR_CUDA;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    const unsigned long long ctx = fp8kv::current_context_id();
+    if (cache[dev].addr == nullptr || ctx == 0 || cache[dev].ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
             return FP8KV_ERR_CUDA;
         }
-        addr[dev] = p;
+        // the lookup makes the context current if it was not yet
+        cache[dev] = Entry{fp8kv::current_context_id(), p};
     }
-    *out = addr[dev];
+    *out = cache[dev].addr;
     return FP8KV_OK;
 }
 
@@ -76,17 +90,17 @@ int fp8kv_paged_decode_attn_noalloc(const void* q, const void* k_cache, const vo
     int st = fp8kv_decode_plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &splits,
                                &need);
     if (st != FP8KV_OK) return st;
-    if (need > kScratchBytes) return FP8KV_ERR_WORKSPACE;
+    if (num_splits > 0 && need > kScratchBytes) return FP8KV_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (need > 0) {
+    if (B > 0) {
         st = scratch_on_current_device(&scratch);
         if (st != FP8KV_OK) return st;
     }
-    return fp8kv_paged_decode_attn(q, k_cache, v_cache, kv_dtype, scale_mode, k_scale, v_scale,
-                                   k_scale_cache, v_scale_cache, block_table, max_blocks_per_seq,
-                                   context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale,
-                                   window, num_splits, scratch, need > 0 ? kScratchBytes : 0,
-                                   out, out_dtype, err_flag, cuda_stream);
+    return fp8kv::paged_decode_attn_fitting(
+        q, k_cache, v_cache, kv_dtype, scale_mode, k_scale, v_scale, k_scale_cache,
+        v_scale_cache, block_table, max_blocks_per_seq, context_lens, B, Hq, Hkv, D, num_blocks,
+        softmax_scale, window, num_splits, scratch, kScratchBytes, out, out_dtype, err_flag,
+        cuda_stream);
 }
 
 }  // extern "C"

@@ -55,6 +55,7 @@ struct DecodeParams {
     void* out;                   // [B][Hq][D]
     int out_bf16;
     int scale_mode;
+    unsigned flags;              // FP8KV_DECODE_EARLY_* (what may run before the wait)
     int32_t* err;
     // fused decode step only (null otherwise): the new token of every sequence,
     // [B][Hkv][D] bf16, stored at position ctx - 1 by the kernel itself
@@ -96,6 +97,29 @@ struct PrefillParams {
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int D, int kv_dtype, int two_level,
                            int grid_x, cudaStream_t stream);
+
+// Identifier of the calling thread's current CUDA context, unique over the
+// process's lifetime (a context recreated after cudaDeviceReset gets a new one);
+// 0 when there is no current context or the driver cannot say.
+unsigned long long current_context_id();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func` when the current
+// context has not had it yet: done[dev] keeps the id of the context it was set in.
+cudaError_t opt_in_smem(const void* func, int bytes, unsigned long long (&done)[64]);
+
+// fp8kv_paged_decode_attn with the split partials in `scratch` (scratch_bytes
+// long).  num_splits 0: the automatic plan, with the CTA count lowered until
+// its partials fit (FP8KV_ERR_WORKSPACE if not even one CTA fits, i.e. the
+// B * Hq * (D + 2) * 4 bytes of one slot per unit alone exceed it); num_splits
+// > 0: that plan, FP8KV_ERR_WORKSPACE if it does not fit.
+int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_cache,
+                              int kv_dtype, int scale_mode, const float* k_scale,
+                              const float* v_scale, const float* k_scale_cache,
+                              const float* v_scale_cache, const int32_t* block_table,
+                              int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
+                              int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
+                              int num_splits, void* scratch, size_t scratch_bytes, void* out,
+                              int out_dtype, int32_t* err_flag, void* cuda_stream);
 
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;

@@ -770,16 +770,10 @@ template <int D, bool TWO, bool BF16, bool PT>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
     auto kern = prefill_kernel<D, TWO, BF16, PT>;
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static unsigned long long attr_done[64] = {};
+    cudaError_t e =
+        opt_in_smem(reinterpret_cast<const void*>(kern), PCfg<D, BF16>::kSmem, attr_done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PCfg<D, BF16>::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
     dim3 grid(grid_x, p.Hkv, p.B);
     kern<<<grid, PCfg<D, BF16>::kThreads, PCfg<D, BF16>::kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();

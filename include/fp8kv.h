@@ -142,15 +142,25 @@ int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int
  *   workspace      scratch of at least the planned bytes, 16-byte aligned; its
  *                  contents need no initialisation.  Calls that share one
  *                  workspace must not overlap on the GPU.
- * Ordering: the kernels launch with programmatic stream serialization.  The
- * set-up (shares of the work, page-table rows) reads context_lens, block_table
- * and k_scale / v_scale while the preceding kernel of the stream is still
- * finishing, so those must be complete before that kernel starts (written by a
- * copy, or by any earlier kernel); q, the caches and the workspace are accessed
- * only after the preceding kernel has completed.
  *   out            [B][Hq][D] fp32 or bf16 (out_dtype).
+ *   flags          0 or FP8KV_DECODE_EARLY_SETUP / FP8KV_DECODE_EARLY_PAGES
+ *                  (below); any other bit is FP8KV_ERR_INVALID.
+ * Ordering: the kernels launch with programmatic stream serialization, so they
+ * may be resident while the preceding kernel of the stream finishes.  With
+ * flags 0 they read nothing before that kernel has completed: any kernel may
+ * produce any input.  The flags let the start overlap that kernel's tail when
+ * the caller knows which inputs it does not write.
  * Output: softmax(z) V over the visible keys, accumulated in fp32.
  */
+/* context_lens, block_table and k_scale / v_scale are complete before the
+ * preceding kernel of the stream starts (written by a copy or an earlier
+ * kernel): the work partition and the page-table reads start before it ends. */
+#define FP8KV_DECODE_EARLY_SETUP 1u
+/* EARLY_SETUP, and the cache pages the call reads (every slot but those
+ * fp8kv_decode_step itself writes) are complete before the preceding kernel
+ * starts too: the first pages stream before it ends.  True in a decode loop
+ * whose older pages were written by earlier steps. */
+#define FP8KV_DECODE_EARLY_PAGES 2u
 int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                             int kv_dtype, int scale_mode, const float* k_scale,
                             const float* v_scale, const float* k_scale_cache,
@@ -158,7 +168,7 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
                             int max_blocks_per_seq, const int32_t* context_lens, int B, int Hq,
                             int Hkv, int D, int64_t num_blocks, float softmax_scale, int window,
                             int num_splits, void* workspace, size_t workspace_bytes, void* out,
-                            int out_dtype, int32_t* err_flag, void* cuda_stream);
+                            int out_dtype, unsigned flags, int32_t* err_flag, void* cuda_stream);
 
 /*
  * fp8kv_decode_step -- a whole decode step of one attention layer in one
@@ -178,13 +188,11 @@ int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_ca
  *   Everything else as in fp8kv_paged_decode_attn; the attention sees the new
  *   token.  A block id outside the cache skips the store and sets
  *   FP8KV_ERR_BAD_INDEX in err_flag.
- * Ordering (programmatic stream serialization): besides context_lens,
- * block_table and k_scale / v_scale, the cache contents other than the slots
- * this call writes must be complete before the preceding kernel of the stream
- * starts -- the kernel streams the older pages while that kernel finishes;
- * q, k_new and v_new are read, and anything is written, only after it has
- * completed.  In a model the preceding kernel produces q / k_new / v_new and
- * the cache was written by earlier steps, so this holds.
+ * Ordering: as fp8kv_paged_decode_attn, flags included.  q, k_new and v_new
+ * are read, and anything is written, only after the preceding kernel has
+ * completed, whatever the flags.  In a decode loop whose tables were copied in
+ * before the step and whose older pages were written by earlier steps,
+ * FP8KV_DECODE_EARLY_PAGES holds.
  */
 int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
                       void* v_cache, int kv_dtype, int scale_mode, const float* k_scale,
@@ -193,7 +201,7 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
                       const int32_t* context_lens, int B, int Hq, int Hkv, int D,
                       int64_t num_blocks, float softmax_scale, int window, int num_splits,
                       void* workspace, size_t workspace_bytes, void* out, int out_dtype,
-                      int32_t* err_flag, void* cuda_stream);
+                      unsigned flags, int32_t* err_flag, void* cuda_stream);
 
 /*
  * fp8kv_prefill_attn -- chunked causal prefill in FP8 on the tcgen05 tensor
@@ -252,17 +260,22 @@ int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
  * allocator to get a workspace from), and serving loops that cannot call
  * cudaMalloc / cudaFree because those synchronize the device.
  *
- * Arguments are those of fp8kv_paged_decode_attn without workspace: the split
+ * Arguments are those of fp8kv_paged_decode_attn without workspace and flags
+ * (it always waits for the preceding kernel first, as flags 0 does): the split
  * partials live in a static device array of FP8KV_NOALLOC_DECODE_SCRATCH_BYTES
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  The caller still passes q, the caches, the tables and `out`.
- *   - A call whose plan (fp8kv_decode_plan) needs more scratch than the array
- *     holds returns FP8KV_ERR_WORKSPACE and launches nothing; request fewer
- *     splits or use fp8kv_paged_decode_attn.
+ *   - num_splits 0: the automatic plan, lowered to the largest CTA count whose
+ *     partials fit the array.  If not even one CTA fits (one slot per
+ *     (sequence, KV head) unit alone, B * Hq * (D + 2) * 4 bytes, exceeds the
+ *     array), or an explicit num_splits plan (fp8kv_decode_plan) needs more
+ *     than the array holds, the call returns FP8KV_ERR_WORKSPACE and launches
+ *     nothing; use fp8kv_paged_decode_attn with a workspace then.
  *   - All calls on a device share the array: calls whose kernels overlap on the
  *     GPU (other streams, other host threads) race.  Serialize them.
  *   - The first call on each device looks the array's address up with that
- *     device current; make that first call before any stream capture.
+ *     device current, and so does the first call after that device's context
+ *     was recreated (cudaDeviceReset); make those calls outside stream capture.
  *   - The array needs no initialisation and keeps the last call's partials.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */

@@ -34,6 +34,10 @@ def test_binding_constants_match_the_header():
         m = re.search(r"#define\s+" + name + r"\s+\((\d+)u << (\d+)\)", text)
         return int(m.group(1)) << int(m.group(2))
     assert define("FP8KV_NOALLOC_DECODE_SCRATCH_BYTES") == fk.NOALLOC_DECODE_SCRATCH_BYTES
+    def flag(name):
+        return int(re.search(r"#define\s+" + name + r"\s+(\d+)u", text).group(1))
+    assert flag("FP8KV_DECODE_EARLY_SETUP") == fk.DECODE_EARLY_SETUP
+    assert flag("FP8KV_DECODE_EARLY_PAGES") == fk.DECODE_EARLY_PAGES
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -88,9 +92,11 @@ def test_write_rejects_bad_arguments_without_a_gpu(lib):
 def test_decode_rejects_bad_arguments_without_a_gpu(lib):
     N = _null()
 
-    def call(B=2, Hq=8, Hkv=2, D=128, dtype=0, mode=0, out_dtype=0, window=0, splits=0):
+    def call(B=2, Hq=8, Hkv=2, D=128, dtype=0, mode=0, out_dtype=0, window=0, splits=0,
+             flags=0):
         return lib.fp8kv_paged_decode_attn(N, N, N, dtype, mode, N, N, N, N, N, 4, N, B, Hq, Hkv,
-                                           D, 10, 0.1, window, splits, N, 0, N, out_dtype, N, N)
+                                           D, 10, 0.1, window, splits, N, 0, N, out_dtype, flags,
+                                           N, N)
 
     assert call() == -1            # null pointers
     assert call(Hq=9) == -1        # Hq % Hkv
@@ -100,7 +106,9 @@ def test_decode_rejects_bad_arguments_without_a_gpu(lib):
     assert call(mode=7) == -1
     assert call(out_dtype=3) == -1
     assert call(window=-1) == -1
+    assert call(flags=4) == -1     # unknown flag bit
     assert call(B=0) == 0
+    assert call(B=0, flags=fk.DECODE_EARLY_SETUP | fk.DECODE_EARLY_PAGES) == 0
 
 
 def test_quantize_rejects_bad_arguments_without_a_gpu(lib):

@@ -174,7 +174,7 @@ def test_workspace_too_small_is_rejected():
     st = lib.fp8kv_paged_decode_attn(P(q), P(gc["k"]), P(gc["v"]), 0, 0, P(gc["k_scale"]),
                                      P(gc["v_scale"]), None, None, P(bt), bt.shape[1], P(cl), 1,
                                      8, 2, 128, w.num_blocks, 0.08, 0, 4, P(ws),
-                                     ws.numel() * 4, P(out), 0, None, None)
+                                     ws.numel() * 4, P(out), 0, 0, None, None)
     assert st == -3
 
 

@@ -85,3 +85,35 @@ def test_noalloc_rejects_plans_larger_than_the_static_array():
             torch.zeros(64, dtype=torch.int32, device="cuda"), kv_dtype=0, scale_mode=0,
             k_scale=one, v_scale=one, num_splits=64,
             out=torch.empty(64, 64, 256, device="cuda"))
+
+
+def test_noalloc_automatic_plan_is_lowered_to_fit_the_array():
+    # 32 sequences x 64 query heads at head_dim 128: the regular automatic plan
+    # (one wave of CTAs) needs more partial slots than the static array holds,
+    # so the entry point uses fewer CTAs instead of rejecting the call.
+    w = synth.decode_workload(33, [1900 + 7 * i for i in range(32)], 64, 8, 128,
+                              fk.SCALE_PER_TOKEN_HEAD)
+    _, need = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, w.block_table.shape[1])
+    assert need > fk.NOALLOC_DECODE_SCRATCH_BYTES
+    c = gpu_fill(w, fk.KV_E4M3)
+    want = gpu_decode(w, c).cpu().numpy()
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+    for _ in range(2):
+        got = _noalloc_call(w, c, out).cpu().numpy()
+        np.testing.assert_allclose(got, want, rtol=RTOL, atol=ATOL)
+
+
+def test_noalloc_rejects_a_batch_whose_unit_slots_alone_exceed_the_array():
+    # B * Hq * (D + 2) * 4 bytes (one slot per sequence and query head) above the
+    # array: no CTA count fits; the binding names the term and the alternative.
+    B, Hq, Hkv, D = 256, 64, 8, 128
+    assert B * Hq * (D + 2) * 4 > fk.NOALLOC_DECODE_SCRATCH_BYTES
+    one = torch.ones(1, device="cuda")
+    with pytest.raises(fk.Fp8kvError, match="workspace"):
+        fk.paged_decode_attn_noalloc(
+            torch.zeros(B, Hq, D, dtype=torch.bfloat16, device="cuda"),
+            torch.zeros(64, Hkv, 16, D, dtype=torch.uint8, device="cuda"),
+            torch.zeros(64, Hkv, 16, D, dtype=torch.uint8, device="cuda"),
+            torch.zeros(B, 4, dtype=torch.int32, device="cuda"),
+            torch.zeros(B, dtype=torch.int32, device="cuda"), kv_dtype=0, scale_mode=0,
+            k_scale=one, v_scale=one, out=torch.empty(B, Hq, D, device="cuda"))

@@ -661,13 +661,17 @@ def _extra_prefill(fk, synth, dev, stream, emit):
         vc = torch.zeros_like(kc)
         fk.kv_cache_write(w.k_all.to(dev), w.v_all.to(dev), w.all_slots.to(dev), kc, vc,
                           kv_dtype=kv, scale_mode=0, k_scale=one, v_scale=one)
-        for two in (False, True):
-            fn = lambda i, kc=kc, vc=vc, kv=kv, two=two: fk.prefill_attn(
+        # split operands ("always") cost two MMAs per contraction; "auto" takes
+        # single operands here (every row sees >= 28673 keys)
+        variants = [(False, "auto"), (True, "auto")] + (
+            [(False, "always"), (True, "always")] if kv == E4 else [])
+        for two, split in variants:
+            fn = lambda i, kc=kc, vc=vc, kv=kv, two=two, split=split: fk.prefill_attn(
                 q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=kv, k_scale=one, v_scale=one,
-                two_level=two, out=out)
+                two_level=two, split=split, out=out)
             ms = _time_graph(fn, 10, stream)
             emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": name, "two_level": two,
-                  "ms": ms, "tflops": flops / ms / 1e9})
+                  "split": split, "ms": ms, "tflops": flops / ms / 1e9})
         del kc, vc
         torch.cuda.empty_cache()
     # the same chunk over a per-token-head e4m3 cache (scales computed at write time)
@@ -677,14 +681,14 @@ def _extra_prefill(fk, synth, dev, stream, emit):
     vsc = torch.zeros_like(ksc)
     fk.kv_cache_write(w.k_all.to(dev), w.v_all.to(dev), w.all_slots.to(dev), kc, vc, kv_dtype=E4,
                       scale_mode=fk.SCALE_PER_TOKEN_HEAD, k_scale_cache=ksc, v_scale_cache=vsc)
-    for two in (False, True):
-        fn = lambda i, two=two: fk.prefill_attn(
+    for two, split in ((False, "auto"), (True, "auto"), (False, "always")):
+        fn = lambda i, two=two, split=split: fk.prefill_attn(
             q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=E4,
             scale_mode=fk.SCALE_PER_TOKEN_HEAD, k_scale_cache=ksc, v_scale_cache=vsc,
-            two_level=two, out=out)
+            two_level=two, split=split, out=out)
         ms = _time_graph(fn, 10, stream)
         emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": "fp8 per-token-head",
-              "two_level": two, "ms": ms, "tflops": flops / ms / 1e9})
+              "two_level": two, "split": split, "ms": ms, "tflops": flops / ms / 1e9})
     del kc, vc, ksc, vsc
     torch.cuda.empty_cache()
     # the other geometry: the 4096-query chunk after a complete 32768-token prefix

@@ -24,6 +24,8 @@ SCALE_PER_TENSOR, SCALE_PER_HEAD, SCALE_PER_TOKEN_HEAD = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
 # decode flags (include/fp8kv.h): what may run before the preceding kernel ends
 DECODE_EARLY_SETUP, DECODE_EARLY_PAGES = 1, 2
+# prefill flags: two-level accumulation, operand precision of the e4m3 path
+PREFILL_TWO_LEVEL, PREFILL_SPLIT_ALWAYS, PREFILL_SPLIT_NEVER = 1, 2, 4
 
 STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -3: "FP8KV_ERR_WORKSPACE", -4: "FP8KV_ERR_CUDA", -5: "FP8KV_ERR_TIMEOUT",
@@ -295,10 +297,15 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
 def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, context_lens,
                  *, kv_dtype=KV_E4M3, scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
                  k_scale_cache=None, v_scale_cache=None, q_scale=1.0, prob_scale=1.0,
-                 softmax_scale=None, two_level=False, out=None, out_dtype=OUT_F32, err_flag=None,
-                 stream=None):
+                 softmax_scale=None, two_level=False, split="auto", out=None, out_dtype=OUT_F32,
+                 err_flag=None, stream=None):
     """Chunked causal FP8 prefill of q [Tq][Hq][D] (bf16) over the paged cache;
-    returns out [Tq][Hq][D].  See fp8kv_prefill_attn."""
+    returns out [Tq][Hq][D].  split: "auto" (split e4m3 operands for blocks of
+    rows under 8192 keys), "always" or "never".  See fp8kv_prefill_attn."""
+    if split not in ("auto", "always", "never"):
+        raise ValueError("split: 'auto', 'always' or 'never'")
+    flags = (PREFILL_TWO_LEVEL if two_level else 0) | {
+        "auto": 0, "always": PREFILL_SPLIT_ALWAYS, "never": PREFILL_SPLIT_NEVER}[split]
     _check(q, "q", torch.bfloat16)
     _check(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
@@ -321,7 +328,7 @@ def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, c
         scale_mode, _ptr(k_scale), _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache),
         float(q_scale), float(prob_scale),
         _ptr(block_table), block_table.shape[1], _ptr(context_lens), cu_seqlens_q.numel() - 1,
-        Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), 1 if two_level else 0, _ptr(out),
+        Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), flags, _ptr(out),
         out_dtype, _ptr(err_flag), _stream(stream))
     _raise(st, "prefill_attn")
     return out

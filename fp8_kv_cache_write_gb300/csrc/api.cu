@@ -501,12 +501,16 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
                        const float* v_scale_cache, float q_scale,
                        float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
                        const int32_t* context_lens, int B, int Hq, int Hkv, int D,
-                       int64_t num_blocks, float softmax_scale, int two_level, void* out,
+                       int64_t num_blocks, float softmax_scale, int flags, void* out,
                        int out_dtype, int32_t* err_flag, void* cuda_stream) {
     g_warning.clear();
+    constexpr int kKnown =
+        FP8KV_PREFILL_TWO_LEVEL | FP8KV_PREFILL_SPLIT_ALWAYS | FP8KV_PREFILL_SPLIT_NEVER;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen_q < 0 ||
-        max_blocks_per_seq < 0 || num_blocks < 0 || (two_level != 0 && two_level != 1))
+        max_blocks_per_seq < 0 || num_blocks < 0 || (flags & ~kKnown) != 0 ||
+        ((flags & FP8KV_PREFILL_SPLIT_ALWAYS) && (flags & FP8KV_PREFILL_SPLIT_NEVER)))
         return FP8KV_ERR_INVALID;
+    const int two_level = flags & FP8KV_PREFILL_TWO_LEVEL;
     if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
     if (scale_mode < FP8KV_SCALE_PER_TENSOR || scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD)
         return FP8KV_ERR_INVALID;
@@ -555,6 +559,7 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     p.k_scale_cache = k_scale_cache;
     p.v_scale_cache = v_scale_cache;
     p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
+    p.split = flags & (FP8KV_PREFILL_SPLIT_ALWAYS | FP8KV_PREFILL_SPLIT_NEVER);
     p.out = out;
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
     p.err = err_flag;

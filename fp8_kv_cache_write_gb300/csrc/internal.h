@@ -89,6 +89,7 @@ struct PrefillParams {
     const float* k_scale_cache;    // per token-head: [num_blocks][Hkv][16]
     const float* v_scale_cache;
     int scale_mode;
+    int split;                     // 0 automatic, else FP8KV_PREFILL_SPLIT_ALWAYS / _NEVER
     void* out;                     // [Tq][Hq][D]
     int out_bf16;
     int32_t* err;

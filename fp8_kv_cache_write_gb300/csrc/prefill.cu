@@ -10,29 +10,44 @@
 // pos_i = ctx_b - n_b + i and every query head of a KV head,
 //     q8 = e4m3(q / q_scale),  s_t = q8 . code_k(t) * q_scale * s_k * softmax_scale,
 //     p8_t = e4m3(exp(s_t - m) / prob_scale),  o = sum_t p8_t code_v(t) / sum_t p8_t
-// over keys t = 0 .. pos_i (times s_v * prob_scale), fp32 accumulation.
+// over keys t = 0 .. pos_i (times s_v), fp32 accumulation.
+//
+// Two operand precisions, chosen per CTA:
+//   * single: Q and P are one e4m3 term each, as above (the pages' FP8
+//     attention).  Its rounding (3 mantissa bits) averages out over long rows:
+//     used where every row of the CTA sees at least kSplitKeys keys.
+//   * split: Q and P enter the MMAs as two e4m3 terms each, hi = e4m3(x) and
+//     lo = e4m3(x - hi), both accumulated into the same fp32 tensor-memory sum
+//     (about 8 significant bits per operand).  Q is first scaled per row by a
+//     power of two (max |q| in [128, 256)) and the weights are lifted by 2^8 under
+//     a running max that moves every half binade, so that both stay in e4m3's
+//     normal range; the logits and the output undo these exact powers of two.
+//     Used for rows with fewer keys (or on request), where single terms would
+//     miss the accuracy target.
 //
 // Design (GB300):
 //   * one CTA per (tile of 128 / G query tokens x the G query heads of a KV
-//     head) = 128 MMA rows; 6 warps: warps 0-3 own one row each per thread
-//     (softmax, P quantization, rescale, epilogue), warp 4 issues TMA, warp 5
-//     allocates tensor memory and issues the MMAs from one thread.
-//   * per KV tile of 128 keys (8 pages): S = Q8 K^T (kind::f8f6f4, M 128, N 128,
-//     K = D in steps of 32) into TMEM; softmax reads S with tcgen05.ld, writes
-//     P8 (e4m3) to shared memory; O += P8 V (M 128, N = D, K = 128 keys) with V
-//     read MN-major straight from the cache tile.  Q8, K and P8 are K-major.
-//     All tiles use the 128-byte swizzle that TMA writes.
+//     head) = 128 MMA rows; softmax warps own one row each per thread (softmax,
+//     P quantization, rescale, epilogue), two loader warps issue TMA (K tiles,
+//     V tiles), one warp allocates tensor memory and issues the MMAs from one
+//     thread.
+//   * per KV tile (128 keys single, 64 keys split): S = Q8 K^T (kind::f8f6f4, M
+//     128, N = keys, K = D in steps of 32) into TMEM; softmax reads S with
+//     tcgen05.ld, writes P8 (e4m3) to shared memory; O += P8 V (M 128, N = D,
+//     K = keys) with V read MN-major straight from the cache tile.  Q8, K and
+//     P8 are K-major; a P row is always 128 bytes (split: 64 hi then 64 lo
+//     weights, which the PV k-steps pair with the same 64 value rows).  All
+//     tiles use the 128-byte swizzle that TMA writes.
 //   * two-level off: O accumulates in TMEM across tiles; the lazy running max
-//     rescales a row of O in TMEM only when the row max grows by more than 2^8.
-//     two-level on: every tile's P V lands in a fresh TMEM tile and the softmax
-//     threads add it into an fp32 accumulator on the CUDA cores.
+//     rescales a row of O in TMEM only when the row max moves.  two-level on:
+//     every tile's P V lands in a fresh TMEM tile and the softmax threads add it
+//     into an fp32 accumulator on the CUDA cores.
 //   * per-token-head scales (PT): the K loader also copies each tile's K and V
 //     scale rows (64 bytes a page) into a 4-slot ring; the softmax multiplies
 //     logit column t by s_k(t) before the row max, and folds s_v(t) into the
 //     e4m3 weights relative to a running power-of-two bound E of the V scales
-//     seen so far, lifted by 2^5 under a lazy max of 2^3 so that they stay in
-//     e4m3's normal range; O is rescaled when E grows, like the lazy row max,
-//     and the row sums use the unfolded weights.
+//     seen so far; O is rescaled when E grows, like the lazy row max, and the
+//     row sums use the unfolded weights.
 //   * every mbarrier wait is bounded and watches a shared abort flag, so a stuck
 //     stage ends the kernel with FP8KV_ERR_TIMEOUT instead of hanging.
 #include <cuda_runtime.h>
@@ -47,31 +62,41 @@ namespace {
 
 constexpr int kRows = 128;          // MMA M: query rows of a CTA
 constexpr float kMaxInitP = -1.0e30f;
-// Per-token-head weights p s_v / E sit up to a factor max(s_v) / min(s_v) below
-// p; a lazy max of 2^3 (p <= 8) leaves room to lift them by 2^5 (<= 256 < 448),
-// which keeps almost every weight in e4m3's normal range (3 mantissa bits)
-// instead of its subnormal steps of 2^-9.
-constexpr float kLazyPT = 3.f;
-constexpr float kHeadPT = 32.f;
+// Rows that see at least this many keys take single e4m3 operands.
+constexpr int kSplitKeys = 8192;
 
-template <int D, bool BF16>
+// Softmax reference and weight lift.  Weights are p * lift with p = 2^(s - m)
+// <= 2^lazy (the running max m moves only when a tile exceeds it by more than
+// `lazy` binades); lift * 2^lazy stays below e4m3's largest value 448.
+//   single, per-tensor / per-head: lazy 8, lift 1 / prob_scale (the pages' P8)
+//   single, per-token-head: lazy 3, lift 2^5 s_v / E (the V scales fold in)
+//   split (both): lazy 1/2, lift 2^8 (x s_v / E): small weights stay normal
+template <bool SPLIT, bool PT>
+struct Soft {
+    static constexpr float kLazy = SPLIT ? 0.5f : (PT ? 3.f : 8.f);
+    static constexpr float kLift = SPLIT ? 256.f : (PT ? 32.f : 1.f);
+};
+
+template <int D, bool BF16, bool SPLIT>
 struct PCfg {
-    // e4m3 tiles hold 128 keys (8 pages), bf16 tiles 64 keys (4 pages) so that
-    // D = 256 still fits in shared memory; every MMA k-step is 32 bytes wide
+    // e4m3 tiles hold 128 keys (8 pages), bf16 and split tiles 64 keys (4 pages):
+    // every P row is 128 bytes (bf16: 64 weights; split: 64 hi + 64 lo weights)
     static constexpr int kElem = BF16 ? 2 : 1;
-    static constexpr int kKeys = BF16 ? 64 : 128;
+    static constexpr int kKeys = (BF16 || SPLIT) ? 64 : 128;
     static constexpr int kRowB = D * kElem;                 // bytes of a Q / K / V row
     // tensor memory: S (or the two-level P V tile) from column 0, O from the
     // kernel's kOCol; D 128 takes 256 columns so two co-resident CTAs never wait
     // on each other
     static constexpr uint32_t kTmemCols = D <= 128 ? 256u : 512u;
     static constexpr int kPanels = kRowB / 128;             // 128-byte panels of a row
-    static constexpr int kQBytes = kRows * kRowB;           // Q tile
+    static constexpr int kQTerms = SPLIT ? 2 : 1;           // Q tiles (hi, lo)
+    static constexpr int kQBytes = kRows * kRowB;           // one Q tile
     static constexpr int kKVBytes = kKeys * kRowB;          // one K (or V) tile
-    static constexpr int kPBytes = kRows * kKeys * kElem;   // one P tile (128-byte rows)
+    static constexpr int kPBytes = kRows * 128;             // one P tile (128-byte rows)
+    static constexpr int kPVSteps = kKeys * kElem / 32;     // PV k-steps of one term
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kQBytes;          // [stage][K | V]
-    static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes; // [2] P8 tiles
+    static constexpr int kOffKV = kOffQ + kQTerms * kQBytes;  // [stage][K | V]
+    static constexpr int kOffP = kOffKV + 2 * 2 * kKVBytes;   // [2] P tiles
     // e4m3 only: 16 x 128-byte rows of 1.0 (the bf16 D 256 tiles leave no room)
     static constexpr int kOffOnes = kOffP + 2 * kPBytes;
     static constexpr int kOffOnes2 = kOffOnes + (BF16 ? 0 : 16 * 128);
@@ -82,7 +107,10 @@ struct PCfg {
     static constexpr int kSoftWarps = 4 * kHalves;
     static constexpr int kThreads = 32 * (kSoftWarps + 3);   // + K loader, MMA, V loader
     static constexpr int kOffPMax = kOffOnes2;               // [2][kHalves][128] partial maxima
-    static constexpr int kOffBar = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
+    // split: per row, 2^-e of the row's Q scaling, then the halves' |q| maxima [2][128]
+    static constexpr int kOffRow = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
+    static constexpr int kRowBytes = SPLIT ? 3 * kRows * 4 : 0;
+    static constexpr int kOffBar = kOffRow + kRowBytes;
     static constexpr int kNumBars = 20;
     // per-token-head scales (e4m3 only): 4 slots of [k scales][v scales] of a
     // tile (128 floats each), then the halves' V-scale maxima [2][2]
@@ -95,7 +123,17 @@ struct PCfg {
     static constexpr int kOffPtf = (kOffMisc + 16 + 15) / 16 * 16;
     static constexpr int kPtfBytes = BF16 ? 0 : kSoftWarps * 128 * 4;
     static constexpr int kSmem = 1024 + kOffPtf + kPtfBytes;
+    static_assert(kKeys / kHalves % 32 == 0, "a half tile is a whole number of 32-key loads");
 };
+
+// Dynamic shared memory of the kernel: the larger of its two operand layouts.
+template <int D, bool BF16>
+constexpr int prefill_smem() {
+    return BF16 ? PCfg<D, true, false>::kSmem
+                : (PCfg<D, false, false>::kSmem > PCfg<D, false, true>::kSmem
+                       ? PCfg<D, false, false>::kSmem
+                       : PCfg<D, false, true>::kSmem);
+}
 
 // barrier indices
 // K and V stages fill and free separately: a K slot is free as soon as its QK
@@ -137,11 +175,44 @@ __device__ __forceinline__ float pow2_ceil(float x) {
     return __uint_as_float(e << 23);
 }
 
-template <int D, bool TWO_LEVEL, bool BF16, bool PT>
-__global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-    using C = PCfg<D, BF16>;
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) {
+    return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
+// Named barrier of the softmax warps only (the loader and MMA warps run on).
+__device__ __forceinline__ void soft_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Two fp32 values -> their e4m3 codes (hi) and the codes of what hi misses (lo),
+// low value in the low byte; *sum += the four decoded values when asked.
+__device__ __forceinline__ void e4m3x2_split(float a, float b, uint32_t& hi, uint32_t& lo,
+                                             float* sum) {
+    hi = e4m3x2_from_f32(a, b);
+    const float2 h = unpack_f16x2(f16x2_from_e4m3x2(hi));   // exact
+    lo = e4m3x2_from_f32(a - h.x, b - h.y);                 // exact differences
+    if (sum != nullptr) {
+        const float2 q = unpack_f16x2(f16x2_from_e4m3x2(lo));
+        *sum += (h.x + h.y) + (q.x + q.y);
+    }
+}
+
+// Where a CTA sits: sequence b, KV head h, its query tokens and key range.
+struct CtaGeo {
+    int b, h;
+    int q0, nq;          // the sequence's first q row and chunk length
+    int tok0;            // this CTA's first query token (in the chunk)
+    int ctx, pos_base;   // keys of the sequence; position of the chunk's first query
+    int n_tiles;         // key tiles the CTA's last row reaches
+};
+
+template <int D, bool TWO_LEVEL, bool BF16, bool PT, bool SPLIT>
+__device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                             const PrefillParams& p, uint8_t* smem,
+                                             const CtaGeo& cg) {
+    using C = PCfg<D, BF16, SPLIT>;
+    using S = Soft<SPLIT, PT>;
     constexpr int kKeys = C::kKeys;
     constexpr int kHalves = C::kHalves;
     constexpr int kSoft = 32 * C::kSoftWarps;          // softmax threads
@@ -149,39 +220,18 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     // of a tile held the pipeline back
     constexpr int kTmaWarp = C::kSoftWarps, kMmaWarp = C::kSoftWarps + 1,
                   kVWarp = C::kSoftWarps + 2;
-    // TMEM columns: S [0, 128); O from kOCol (two-level on: the P V tile takes
+    // TMEM columns: S [0, kKeys); O from kOCol (two-level on: the P V tile takes
     // [0, D) and O [kOCol, kOCol + D)).  e4m3, D 256, two-level off: the row sums
     // l of the quantized weights come from the tensor core too, as P times a
     // block of ones, into [kLCol, kLCol + 16).
     constexpr uint32_t kOCol = D <= 128 ? 128u : (TWO_LEVEL ? 256u : 128u);
     constexpr bool kLMma = D == 256 && !TWO_LEVEL && !BF16 && !PT;
     constexpr uint32_t kLCol = kOCol + D;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = p.G, TPT = kRows / G;                 // query tokens per tile
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int q0 = p.cu_seqlens_q[b], nq = p.cu_seqlens_q[b + 1] - q0;
-    // tiles go out last-first: later query tiles see more keys (causal), so the
-    // heaviest CTAs take the first wave and the lightest fill the partial last one
-    const int tok0 = (gridDim.x - 1 - blockIdx.x) * TPT;
-    if (tok0 >= nq) return;
-    int ctx = p.context_lens[b];
-    if (ctx > p.max_blocks_per_seq * kPage) {
-        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-        ctx = p.max_blocks_per_seq * kPage;
-    }
-    const int pos_base = ctx - nq;                      // position of the chunk's first query
-    const int n_tok = min(TPT, nq - tok0);
-    const int pos_max = pos_base + tok0 + n_tok - 1;
-    const int pos_min = pos_base + tok0;
-    if (pos_min < 0) {                                  // chunk longer than the context
-        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-        return;
-    }
-    const int n_tiles = pos_max / kKeys + 1;
+    const int G = p.G;
+    const int b = cg.b, h = cg.h, q0 = cg.q0, nq = cg.nq, tok0 = cg.tok0;
+    const int ctx = cg.ctx, pos_base = cg.pos_base, n_tiles = cg.n_tiles;
     const int ctx_pages = (ctx + kPage - 1) / kPage;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -205,20 +255,53 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
-    // ---- Q tile (K-major, 128-byte swizzle): e4m3(q / q_scale), or q itself (bf16)
+    // ---- Q tile(s) (K-major, 128-byte swizzle)
+    //   single: e4m3(q / q_scale); bf16: q itself;
+    //   split:  hi = e4m3(q 2^e_r), lo = e4m3(q 2^e_r - hi), with 2^e_r putting the
+    //           row's max |q| into [128, 256) (exact scaling; 2^-e_r goes to the logits)
+    float* rowinfo = reinterpret_cast<float*>(smem + C::kOffRow);   // split: [3][128]
     if (warp < C::kSoftWarps) {
         const int r = tid & (kRows - 1);
         const int half = tid / kRows;                   // which chunks of the row
         const int tk = tok0 + r / G, head = r % G;
         uint8_t* qtile = smem + C::kOffQ;
         constexpr int kChunks = C::kRowB / 16 / kHalves;
+        const __nv_bfloat16* qrow =
+            p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D;
+        float qmul = 1.f;                               // split: 2^e_r
+        if constexpr (SPLIT) {
+            float amax = 0.f;
+            if (tk < nq) {
+#pragma unroll 4
+                for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(qrow + c * 16);
+                    const uint4 bq = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
+                    const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_float(in[i] & 0xffffu)));
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_float(in[i] >> 16)));
+                    }
+                }
+            }
+            rowinfo[kRows + half * kRows + r] = amax;
+            soft_sync(kSoft);
+            amax = fmaxf(rowinfo[kRows + r], rowinfo[2 * kRows + r]);
+            int e = 0;
+            if (amax > 0.f) {
+                int ex;
+                frexpf(amax, &ex);                      // amax in [2^(ex-1), 2^ex)
+                e = 8 - ex;
+                e = e > 120 ? 120 : (e < -120 ? -120 : e);
+            }
+            qmul = exp2i(e);
+            if (half == 0) rowinfo[r] = exp2i(-e);
+        }
 #pragma unroll 4
         for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {   // 16-byte chunks
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            uint32_t w[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
             if (tk < nq) {
-                const __nv_bfloat16* src =
-                    p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D +
-                    c * (16 / C::kElem);
+                const __nv_bfloat16* src = qrow + c * (16 / C::kElem);
                 if constexpr (BF16) {
                     const uint4 a = *reinterpret_cast<const uint4*>(src);
                     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
@@ -228,16 +311,28 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                     const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float lo = __fdiv_rn(bf16_bits_to_float(in[i] & 0xffffu), p.q_scale);
-                        const float hi = __fdiv_rn(bf16_bits_to_float(in[i] >> 16), p.q_scale);
-                        w[i >> 1] |= static_cast<uint32_t>(e4m3x2_from_f32(lo, hi))
-                                     << (16 * (i & 1));
+                        const float x0 = bf16_bits_to_float(in[i] & 0xffffu);
+                        const float x1 = bf16_bits_to_float(in[i] >> 16);
+                        if constexpr (SPLIT) {
+                            uint32_t hi, lo;
+                            e4m3x2_split(x0 * qmul, x1 * qmul, hi, lo, nullptr);
+                            w[i >> 1] |= hi << (16 * (i & 1));
+                            wl[i >> 1] |= lo << (16 * (i & 1));
+                        } else {
+                            const float lo = __fdiv_rn(x0, p.q_scale);
+                            const float hi = __fdiv_rn(x1, p.q_scale);
+                            w[i >> 1] |= static_cast<uint32_t>(e4m3x2_from_f32(lo, hi))
+                                         << (16 * (i & 1));
+                        }
                     }
                 }
             }
             const int panel = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(qtile + panel * (kRows * 128) + r * 128 +
-                                      ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            const int off = panel * (kRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(qtile + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            if constexpr (SPLIT)
+                *reinterpret_cast<uint4*>(qtile + C::kQBytes + off) =
+                    make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
         if constexpr (kLMma) {                          // 16 rows of 128 bytes of 1.0
             const uint32_t one = 0x38383838u;
@@ -331,17 +426,21 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 else
                     mma_f8f6f4(d, a, bdsc, id, acc);
             };
-            const uint32_t tS = tmem;                           // S: columns [0, 128)
+            const uint32_t tS = tmem;                           // S: columns [0, kKeys)
             const uint32_t tO = tmem + (TWO_LEVEL ? 0u : kOCol); // PV target
             auto issue_qk = [&](int j) {
                 const uint32_t kbase = sbase + C::kOffKV + (j & 1) * 2 * C::kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < C::kRowB / 32; ++kk) {    // 32-byte k-steps over D
                     const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-                    const uint64_t ad = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * (kKeys * 128) +
                                                             (kk & 3) * 32, 16, 1024);
-                    mma(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int t = 0; t < C::kQTerms; ++t) {       // split: Q hi, then Q lo
+                        const uint64_t ad =
+                            smem_desc_sw128(sbase + C::kOffQ + t * C::kQBytes + off, 16, 1024);
+                        mma(tS, ad, bd, idesc_qk, (kk > 0 || t > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(bar(kSFull));
                 mma_commit(bar(kKEmpty0 + (j & 1)));
@@ -349,12 +448,15 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             auto issue_pv = [&](int j) {
                 const uint32_t vbase = sbase + C::kOffKV + (j & 1) * 2 * C::kKVBytes + C::kKVBytes;
                 const uint32_t pbase = sbase + C::kOffP + (j & 1) * C::kPBytes;
+                // 32-byte k-steps over the 128-byte P rows; split: steps kPVSteps..
+                // hold the lo weights of the same keys
 #pragma unroll
-                for (int kk = 0; kk < kKeys * C::kElem / 32; ++kk) {   // 32-byte k-steps over keys
+                for (int kk = 0; kk < 128 / 32; ++kk) {
+                    const int vk = kk % C::kPVSteps;
                     const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
                     // V: MN-major; 8-key groups 1024 B apart, 128-byte D panels
                     // kKeys * 128 B apart; one k-step = 32 / elem keys
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * (32 / C::kElem) * 128,
+                    const uint64_t bd = smem_desc_sw128(vbase + vk * (32 / C::kElem) * 128,
                                                         kKeys * 128, 1024);
                     const uint32_t acc = TWO_LEVEL ? (kk > 0 ? 1u : 0u)
                                                    : ((j > 0 || kk > 0) ? 1u : 0u);
@@ -442,14 +544,25 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 kconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.k_scale[h] : p.k_scale[0];
                 vconst = p.scale_mode == FP8KV_SCALE_PER_HEAD ? p.v_scale[h] : p.v_scale[0];
             }
-            qs = p.q_scale;
-            ps = p.prob_scale;
+            // split: Q is scaled per row and the weights by 2^8 instead; q_scale
+            // and prob_scale would cancel exactly and are not used
+            if constexpr (!SPLIT) {
+                qs = p.q_scale;
+                ps = p.prob_scale;
+            }
         }
+        // the row's logit factor: raw S times sc is s in base-2 units.  PT: the
+        // column factors carry scol, the row factor rowf = 2^-e_r (split) or 1.
+        const float rowf = SPLIT ? rowinfo[r] : 1.f;
+        const float scol = qs * kconst * p.scale_log2;
+        const float sc = scol * rowf;
+        const float rf = PT ? rowf : sc;               // raw (PT: column-scaled) S -> s
+        // weights p * lift: single non-PT e4m3(p / prob_scale); PT p s_v lift / E
+        const float lift = BF16 ? 1.f : S::kLift / ps;
+        const float llift = log2f(lift);
         // PT: running power-of-two bound of the V scales folded into the weights
         float e_run = 0.f;
         float* ebuf = reinterpret_cast<float*>(smem + C::kOffScl + 4 * 1024);   // [2][2]
-        const float sc = qs * kconst * p.scale_log2;   // > 0: the max of raw S scales
-        const float lps = log2f(ps);                   // p / prob_scale = 2^(s sc - m - lps)
         float m = kMaxInitP, l = 0.f;                  // l: this half's keys (summed at the end)
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -471,7 +584,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             mbar_arrive(bar(kSEmpty));
 
             // causal mask on the raw logits (keys past ctx always masked), the row
-            // max of raw S, then base-2 logits s * sc - m inside one FFMA below
+            // max of raw S, then base-2 logits s * rf - m inside one FFMA below
             const int key0 = j * kKeys + kh * kKH;
             float s[kKH];
             float mxp[8];                       // 8 independent partial maxima
@@ -486,10 +599,9 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             // PT: this warp's column factors (every lane of the warp works on this half)
             float* ptf = reinterpret_cast<float*>(smem + C::kOffPtf) + warp * 128;
             if constexpr (PT) {
-                static_assert(kKH == 64, "per-token-head tiles: 64 keys a half");
                 __syncwarp();                   // the previous tile's factors are read
-                ptf[lane] = ksl[lane] * sc;
-                ptf[lane + 32] = ksl[lane + 32] * sc;
+#pragma unroll
+                for (int i = lane; i < kKH; i += 32) ptf[i] = ksl[i] * scol;
                 __syncwarp();
                 if (full) {
 #pragma unroll
@@ -540,7 +652,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 mx_raw = fmaxf(mx_raw, pmax[(st * 2 + (kh ^ 1)) * kRows + r]);
                 if constexpr (PT) vmax = fmaxf(vmax, ebuf[st * 2 + (kh ^ 1)]);
             }
-            const float mx = PT ? mx_raw : mx_raw * sc;
+            const float mx = mx_raw * rf;
             float beta = 1.f;                   // PT: O's factor when the V bound grows
             if constexpr (PT) {
                 const float e_t = pow2_ceil(vmax);
@@ -550,7 +662,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 }
             }
             float alpha = 1.f;
-            if (mx > m + (PT ? kLazyPT : 8.f)) {   // lazy running max (the same in both halves)
+            if (mx > m + S::kLazy) {            // lazy running max (the same in both halves)
                 alpha = ex2p(m - mx);
                 m = mx;
                 l *= alpha;
@@ -594,58 +706,61 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             }
             uint8_t* prow = smem + C::kOffP + st * C::kPBytes + r * 128;
             constexpr int kPerChunk = 16 / C::kElem;    // keys per 16-byte chunk
-            constexpr int kMyChunks = 8 / kHalves;      // this half's chunks of the row
-            const float moff = m + lps;
-            // PT: weight = p * s_v * kHeadPT / (E prob_scale), the unfolded p into l
-            const float vinv = PT && e_run > 0.f ? kHeadPT / (e_run * ps) : 0.f;
+            constexpr int kMyChunks = kKH / kPerChunk;  // this half's chunks of the row
+            // PT: weight = p * s_v * lift / E, the unfolded p into l
+            const float vinv = PT && e_run > 0.f ? lift / e_run : 0.f;
             if constexpr (PT) {
                 __syncwarp();                   // the previous tile's factors are read
-                ptf[64 + lane] = vsl[lane] * vinv;
-                ptf[96 + lane] = vsl[lane + 32] * vinv;
+#pragma unroll
+                for (int i = lane; i < kKH; i += 32) ptf[64 + i] = vsl[i] * vinv;
                 __syncwarp();
             }
+            // not PT: weight = 2^(s rf - m) * lift, one FFMA and an ex2
+            const float moff = m - llift;
 #pragma unroll
             for (int c8 = 0; c8 < kMyChunks; ++c8) {
                 const int cc = kh * kMyChunks + c8;
-                uint32_t w[4];
-                if constexpr (PT) {
+                uint32_t w[4], wl[4];
 #pragma unroll
-                    for (int i = 0; i < kPerChunk / 2; ++i) {
-                        const int ia = c8 * kPerChunk + 2 * i, ib = ia + 1;
-                        const float pa = ex2p(s[ia] - m), pb = ex2p(s[ib] - m);
+                for (int i = 0; i < kPerChunk / 2; ++i) {
+                    const int ia = c8 * kPerChunk + 2 * i, ib = ia + 1;
+                    float wa, wb;
+                    if constexpr (PT) {
+                        const float pa = ex2p(fmaf(s[ia], rf, -m)), pb = ex2p(fmaf(s[ib], rf, -m));
                         l += pa + pb;
                         // masked keys: p = 0 and a stale scale that must not enter
                         const bool va = full || key0 + ia <= pos_r, vb = full || key0 + ib <= pos_r;
-                        const uint32_t code = e4m3x2_from_f32(va ? pa * ptf[64 + ia] : 0.f,
-                                                              vb ? pb * ptf[64 + ib] : 0.f);
-                        if (i & 1)
-                            w[i >> 1] |= code << 16;
-                        else
-                            w[i >> 1] = code;
+                        wa = va ? pa * ptf[64 + ia] : 0.f;
+                        wb = vb ? pb * ptf[64 + ib] : 0.f;
+                    } else {
+                        wa = ex2p(fmaf(s[ia], rf, -moff));
+                        wb = ex2p(fmaf(s[ib], rf, -moff));
                     }
-                    *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                    continue;
-                }
-#pragma unroll
-                for (int i = 0; i < kPerChunk / 2; ++i) {
-                    const float pa = ex2p(fmaf(s[c8 * kPerChunk + 2 * i], sc, -moff));
-                    const float pb = ex2p(fmaf(s[c8 * kPerChunk + 2 * i + 1], sc, -moff));
-                    // the denominator sums the same rounded weights the MMA uses
-                    // (on the tensor core for D 256, e4m3, two-level off)
+                    // the denominator (not PT) sums the same rounded weights the MMA
+                    // uses (on the tensor core for D 256, e4m3, two-level off)
                     if constexpr (BF16) {
-                        w[i] = pack_bf16x2(pa, pb);
+                        w[i] = pack_bf16x2(wa, wb);
                         if constexpr (!kLMma) {
                             const float2 q2 = unpack_bf16x2(w[i]);
                             l += q2.x + q2.y;
                         }
+                    } else if constexpr (SPLIT) {
+                        uint32_t hi, lo;
+                        e4m3x2_split(wa, wb, hi, lo, (PT || kLMma) ? nullptr : &l);
+                        if (i & 1) {
+                            w[i >> 1] |= hi << 16;
+                            wl[i >> 1] |= lo << 16;
+                        } else {
+                            w[i >> 1] = hi;
+                            wl[i >> 1] = lo;
+                        }
                     } else {
-                        const uint32_t code = e4m3x2_from_f32(pa, pb);
+                        const uint32_t code = e4m3x2_from_f32(wa, wb);
                         if (i & 1)
                             w[i >> 1] |= code << 16;
                         else
                             w[i >> 1] = code;
-                        if constexpr (!kLMma) {
+                        if constexpr (!kLMma && !PT) {
                             const float2 q2 = unpack_f16x2(f16x2_from_e4m3x2(code));
                             l += q2.x + q2.y;
                         }
@@ -653,6 +768,9 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 }
                 *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
+                if constexpr (SPLIT)            // the lo weights: chunks 4..7 of the row
+                    *reinterpret_cast<uint4*>(prow + (((cc + 4) ^ (r & 7)) << 4)) =
+                        make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
             // value rows past ctx in the last tile hold unwritten cache slots (any
             // bytes, NaN codes included): zero them so 0 * v stays 0
@@ -702,7 +820,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
                 mbar_arrive(bar(kPvtFree));
             }
         }
-        // ---- epilogue: out = O * (v_scale * prob_scale) / l
+        // ---- epilogue: out = O * v_scale / l (PT: O * E / (lift l))
         if (ok) {
             const int last = n_tiles - 1;
             if (!TWO_LEVEL &&
@@ -729,8 +847,9 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
             }
         }
         if (ok) {
-            // PT: l sums p itself (not p / prob_scale) and O carries kHeadPT / (E prob_scale)
-            const float f = l > 0.f ? (PT ? e_run * ps / kHeadPT : vconst * ps) / l : 0.f;
+            // not PT: l sums the weights the MMA used, so O / l is the weighted mean
+            // of the value codes; PT: l sums p itself and O carries lift / E
+            const float f = l > 0.f ? (PT ? e_run / lift : vconst) / l : 0.f;
             const int head = r % G;
             for (int cch = 0; cch < kDH / 32; ++cch) {
                 const int col = kh * kDH + cch * 32;
@@ -766,16 +885,65 @@ __global__ void __launch_bounds__(PCfg<D, BF16>::kThreads, 1)
     }
 }
 
+template <int D, bool TWO_LEVEL, bool BF16, bool PT>
+__global__ void __launch_bounds__(PCfg<D, BF16, false>::kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x;
+    CtaGeo cg;
+    cg.b = blockIdx.z;
+    cg.h = blockIdx.y;
+    cg.q0 = p.cu_seqlens_q[cg.b];
+    cg.nq = p.cu_seqlens_q[cg.b + 1] - cg.q0;
+    const int TPT = kRows / p.G;                        // query tokens per tile
+    // tiles go out last-first: later query tiles see more keys (causal), so the
+    // heaviest CTAs take the first wave and the lightest fill the partial last one
+    cg.tok0 = (gridDim.x - 1 - blockIdx.x) * TPT;
+    if (cg.tok0 >= cg.nq) return;
+    int ctx = p.context_lens[cg.b];
+    if (ctx > p.max_blocks_per_seq * kPage) {
+        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+        ctx = p.max_blocks_per_seq * kPage;
+    }
+    cg.ctx = ctx;
+    cg.pos_base = ctx - cg.nq;                          // position of the chunk's first query
+    const int n_tok = min(TPT, cg.nq - cg.tok0);
+    const int pos_max = cg.pos_base + cg.tok0 + n_tok - 1;
+    const int pos_min = cg.pos_base + cg.tok0;
+    if (pos_min < 0) {                                  // chunk longer than the context
+        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
+        return;
+    }
+    if constexpr (BF16) {
+        cg.n_tiles = pos_max / PCfg<D, true, false>::kKeys + 1;
+        prefill_body<D, TWO_LEVEL, true, PT, false>(kmap, vmap, p, smem, cg);
+    } else {
+        // split operands where a row of the CTA sees fewer than kSplitKeys keys
+        const bool split = p.split == FP8KV_PREFILL_SPLIT_ALWAYS ||
+                           (p.split == 0 && pos_min + 1 < kSplitKeys);
+        if (split) {
+            cg.n_tiles = pos_max / PCfg<D, false, true>::kKeys + 1;
+            prefill_body<D, TWO_LEVEL, false, PT, true>(kmap, vmap, p, smem, cg);
+        } else {
+            cg.n_tiles = pos_max / PCfg<D, false, false>::kKeys + 1;
+            prefill_body<D, TWO_LEVEL, false, PT, false>(kmap, vmap, p, smem, cg);
+        }
+    }
+}
+
 template <int D, bool TWO, bool BF16, bool PT>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
     auto kern = prefill_kernel<D, TWO, BF16, PT>;
+    constexpr int kSmem = prefill_smem<D, BF16>();
     static unsigned long long attr_done[64] = {};
-    cudaError_t e =
-        opt_in_smem(reinterpret_cast<const void*>(kern), PCfg<D, BF16>::kSmem, attr_done);
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmem, attr_done);
     if (e != cudaSuccess) return e;
     dim3 grid(grid_x, p.Hkv, p.B);
-    kern<<<grid, PCfg<D, BF16>::kThreads, PCfg<D, BF16>::kSmem, stream>>>(kmap, vmap, p);
+    kern<<<grid, PCfg<D, BF16, false>::kThreads, kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 

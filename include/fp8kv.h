@@ -221,25 +221,38 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
  *                  scales are folded into the e4m3 weights relative to a running
  *                  power-of-two bound of the scales seen, see prefill.cu).
  *   q_scale, prob_scale  host floats > 0: Q and the softmax weights are stored
- *                  as e4m3(q / q_scale) and e4m3(p / prob_scale) for the MMAs.
+ *                  as e4m3(q / q_scale) and e4m3(p / prob_scale) for the MMAs
+ *                  (single operands; see flags).
  *   context_lens   int32 [B]: keys of sequence b, the chunk included; query i of
  *                  the chunk sits at position ctx - n_b + i and sees keys 0..that.
- *   two_level      1: each KV tile's P V is added into a separate fp32
- *                  accumulator on the CUDA cores; 0: the tensor core accumulates
- *                  across tiles (enough on Blackwell).
+ *   flags          FP8KV_PREFILL_TWO_LEVEL: each KV tile's P V is added into a
+ *                  separate fp32 accumulator on the CUDA cores (else the tensor
+ *                  core accumulates across tiles, enough on Blackwell).
+ *                  Operand precision of the e4m3 cache: by default a block of
+ *                  query rows whose rows all see at least 8192 keys takes single
+ *                  e4m3 Q and P (the rounding averages out over long rows); other
+ *                  blocks take split operands, Q and P each as two e4m3 terms
+ *                  (hi and the e4m3 of what hi misses, ~8 significant bits, after
+ *                  exact power-of-two scaling that replaces q_scale and
+ *                  prob_scale), which meets max-abs 1e-2 on N(0,1) data at any
+ *                  length.  FP8KV_PREFILL_SPLIT_ALWAYS / _NEVER force one of
+ *                  them; setting both is FP8KV_ERR_INVALID, as is any other bit.
  *   out            [Tq][Hq][D] fp32 or bf16.
  * Supported: e4m3 cache (every scale mode) and its bf16 twin (bf16 Q, P and
  * cache, kind::f16; scales ignored), D in {128, 256}, Hq / Hkv dividing 128.
  * Other shapes return FP8KV_ERR_UNSUPPORTED.  With q_scale or prob_scale equal
  * to 1.0 an e4m3 call succeeds and sets fp8kv_last_warning().
  */
+#define FP8KV_PREFILL_TWO_LEVEL 1
+#define FP8KV_PREFILL_SPLIT_ALWAYS 2
+#define FP8KV_PREFILL_SPLIT_NEVER 4
 int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
                        const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
                        const float* k_scale, const float* v_scale, const float* k_scale_cache,
                        const float* v_scale_cache, float q_scale,
                        float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
                        const int32_t* context_lens, int B, int Hq, int Hkv, int D,
-                       int64_t num_blocks, float softmax_scale, int two_level, void* out,
+                       int64_t num_blocks, float softmax_scale, int flags, void* out,
                        int out_dtype, int32_t* err_flag, void* cuda_stream);
 
 /*

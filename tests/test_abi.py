@@ -38,6 +38,9 @@ def test_binding_constants_match_the_header():
         return int(re.search(r"#define\s+" + name + r"\s+(\d+)u", text).group(1))
     assert flag("FP8KV_DECODE_EARLY_SETUP") == fk.DECODE_EARLY_SETUP
     assert flag("FP8KV_DECODE_EARLY_PAGES") == fk.DECODE_EARLY_PAGES
+    for name in ("TWO_LEVEL", "SPLIT_ALWAYS", "SPLIT_NEVER"):
+        m = re.search(r"#define\s+FP8KV_PREFILL_" + name + r"\s+(\d+)", text)
+        assert int(m.group(1)) == getattr(fk, "PREFILL_" + name)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -133,7 +136,8 @@ def test_prefill_rejects_bad_arguments_without_a_gpu(lib):
     assert call(dtype=2) == -1
     assert call(mode=3) == -1
     assert call(out_dtype=2) == -1
-    assert call(two_level=2) == -1
+    assert call(two_level=8) == -1      # unknown flag bit
+    assert call(two_level=6) == -1      # split always and never
     assert call(q_scale=0.0) == -1
     assert call(prob_scale=-1.0) == -1
     assert call(max_q=-1) == -1

@@ -108,15 +108,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map over a paged cache [num_blocks * Hkv][16][row_bytes] (bytes):
-// boxes of 16 rows x 128 bytes with 128-byte swizzle (64-byte rows are viewed
-// as 8 rows of 128 bytes, two tokens each).  Encodings are cached per thread.
+// boxes of 16 rows x 128 bytes with 128-byte swizzle.  64-byte rows are viewed
+// as 8 rows of 128 bytes, two tokens each (decode), or copied as 16 rows of 64
+// bytes with the 64-byte swizzle (prefill's MMA operands, sw64).  Encodings are
+// cached per thread.
 struct MapKey {
     const void* base;
     int row_bytes;
     int64_t nbh;
+    bool sw64;
 };
 
-bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out) {
+bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
+                 bool sw64 = false) {
+    sw64 = sw64 && row_bytes == 64;
     struct Entry {
         MapKey key;
         CUtensorMap map;
@@ -125,7 +130,8 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out)
     thread_local Entry cache[8] = {};
     thread_local int next = 0;
     for (auto& e : cache)
-        if (e.used && e.key.base == base && e.key.row_bytes == row_bytes && e.key.nbh == nbh) {
+        if (e.used && e.key.base == base && e.key.row_bytes == row_bytes && e.key.nbh == nbh &&
+            e.key.sw64 == sw64) {
             *out = e.map;
             return true;
         }
@@ -135,7 +141,11 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out)
     cuuint64_t strides[2];
     cuuint32_t box[3];
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (row_bytes == 64) {
+    if (sw64) {
+        dims[0] = 64; dims[1] = 16; dims[2] = static_cast<cuuint64_t>(nbh);
+        strides[0] = 64; strides[1] = 1024;
+        box[0] = 64; box[1] = 16; box[2] = 1;
+    } else if (row_bytes == 64) {
         dims[0] = 128; dims[1] = 8; dims[2] = static_cast<cuuint64_t>(nbh);
         strides[0] = 128; strides[1] = 1024;
         box[0] = 128; box[1] = 8; box[2] = 1;
@@ -148,10 +158,11 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out)
     }
     CUtensorMap m;
     CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
-    cache[next] = Entry{MapKey{base, row_bytes, nbh}, m, true};
+    cache[next] = Entry{MapKey{base, row_bytes, nbh, sw64}, m, true};
     next = (next + 1) % 8;
     *out = m;
     return true;
@@ -183,7 +194,8 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     if (req > 0) {
         n = static_cast<int64_t>(req) * units;
     } else {
-        n = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0);
+        n = static_cast<int64_t>(sm_count()) *
+            decode_ctas_per_sm(D, 0, Hkv > 0 ? Hq / Hkv : 1);
         const int64_t by_work = (work + 15) / 16;
         if (by_work < n) n = by_work;
     }
@@ -341,7 +353,7 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
         (flags & ~(FP8KV_DECODE_EARLY_SETUP | FP8KV_DECODE_EARLY_PAGES)) != 0)
         return FP8KV_ERR_INVALID;
     if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
-    if (Hq / Hkv > 8) return FP8KV_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16) return FP8KV_ERR_UNSUPPORTED;
     if (kv_dtype != FP8KV_KV_E4M3 && kv_dtype != FP8KV_KV_BF16) return FP8KV_ERR_INVALID;
     if (kv_dtype == FP8KV_KV_E4M3 && (scale_mode < FP8KV_SCALE_PER_TENSOR ||
                                       scale_mode > FP8KV_SCALE_PER_TOKEN_HEAD))
@@ -519,7 +531,7 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
         !(prob_scale < 3.0e38f) || !(softmax_scale == softmax_scale))
         return FP8KV_ERR_INVALID;
     const int G = Hq / Hkv;
-    if ((D != 128 && D != 256) || G > 128 || (128 % G) != 0) return FP8KV_ERR_UNSUPPORTED;
+    if (!valid_d(D) || G > 128 || (128 % G) != 0) return FP8KV_ERR_UNSUPPORTED;
     if (B == 0 || max_seqlen_q == 0) return FP8KV_OK;
     if (B > 65535 || Hkv > 65535 || max_blocks_per_seq < 1 || num_blocks < 1)
         return FP8KV_ERR_INVALID;
@@ -538,7 +550,8 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     CUtensorMap kmap, vmap;
     const int64_t nbh = num_blocks * Hkv;
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
-    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap) || !make_kv_map(v_cache, row_bytes, nbh, &vmap))
+    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap, true) ||
+        !make_kv_map(v_cache, row_bytes, nbh, &vmap, true))
         return FP8KV_ERR_CUDA;
     PrefillParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);

@@ -50,7 +50,7 @@ constexpr int kWarps = kDecodeWarps;
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 constexpr float kMaxInit = -1.0e30f;   // running-max start: finite, below any real logit
 
-template <int D, bool BF16>
+template <int D, bool BF16, int NT = 1>
 struct Cfg {
     static constexpr int kElem = BF16 ? 2 : 1;
     static constexpr int kRowB = D * kElem;           // bytes of one token row
@@ -76,10 +76,14 @@ struct Cfg {
     static constexpr int kOffSegs = kOffBars + kWarps * kStages * 8;
     static constexpr int kOffShare = kOffSegs + kWarps * kMaxSeg * kSegInts * 4;  // [warp][resume, end]
     static constexpr int kOffCtx = kOffShare + kWarps * 16;    // [warp][32] context lengths
-    static constexpr int kSmem = 1024 + kOffCtx + kWarps * 128;
+    // NT = 2 (more than 8 query heads per KV head): each warp's query fragments of
+    // both 8-head groups, [group][k-step][lane] (8 bytes each), in shared memory
+    static constexpr int kOffQsm = kOffCtx + kWarps * 128;
+    static constexpr int kQsmBytes = NT > 1 ? kWarps * NT * kKSteps * 32 * 8 : 0;
+    static constexpr int kSmem = 1024 + kOffQsm + kQsmBytes;
     // fused step only, after the above: per warp the new token's K row, V row
     // (as stored in the cache) and its two per-token-head scales
-    static constexpr int kOffNew = kOffCtx + kWarps * 128;
+    static constexpr int kOffNew = kOffQsm + kQsmBytes;
     static constexpr int kNewB = (2 * kRowB + 8 + 15) / 16 * 16;
     static constexpr int kSmemFused = kSmem + kWarps * kNewB;
     static_assert(kSegs * kKPerSeg == kKSteps, "k-step split");
@@ -277,15 +281,19 @@ __device__ __noinline__ bool store_new_token_row(const int32_t* bt_row, int64_t 
     return ok;
 }
 
-// D <= 128 keeps 3 CTAs (12 warps) resident per SM: 168 registers at most.
+// CTAs resident per SM: 3 (12 warps, 168 registers at most) for D <= 128 with
+// one 8-head group, else 2.
+template <int D, int NT>
+constexpr int decode_min_ctas() { return D <= 128 && NT == 1 ? 3 : 2; }
+
 // FUSED: a decode step -- the kernel also stores every sequence's new token
-// (k_new / v_new at position ctx - 1) and starts streaming the older pages
-// before the preceding kernel has finished.
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED>
-__global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
+// (k_new / v_new at position ctx - 1).  NT: 8-head groups per KV head (1 for
+// G <= 8, 2 for G <= 16); the groups share every K and V conversion.
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
+__global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, NT>())
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-    using C = Cfg<D, BF16>;
+    using C = Cfg<D, BF16, NT>;
     constexpr int PPI = C::kPPI;
     constexpr int kMaxSeg = C::kMaxSeg;
     constexpr int kSegInts = C::kSegInts;
@@ -438,12 +446,18 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         return k;
     };
 
-    uint32_t qb[C::kKSteps][2];
-    float hs0 = 0.f, hs1 = 0.f;
-    // ---- query fragments (B operand of S^T = K Q^T): head g, elements d0..d0+3
+    // ---- query fragments (B operand of S^T = K Q^T): head 8 nt + g of the group,
+    //      elements d0..d0+3; in registers for one group, in shared memory for two
+    uint32_t qb[NT == 1 ? C::kKSteps : 1][2];
+    uint2* qsm = reinterpret_cast<uint2*>(smem + C::kOffQsm) + warp * NT * C::kKSteps * 32;
+    float hs[NT][2];                        // log2-domain logit multipliers, heads 2c, 2c+1
     auto load_q = [&](int b, int h, float kconst) {
-    const int hq_g = h * G + g;
-    float qscale;                           // log2-domain logit multiplier of head g
+    if constexpr (NT > 1) __syncwarp();     // the previous segment's fragments are read
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+    const int hl = nt * 8 + g;              // head within the group
+    const int hq_g = h * G + hl;
+    float qscale = 0.f;                     // log2-domain logit multiplier of head hl
     {
         const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(b) * p.Hq + hq_g) * D;
         uint2 raw[C::kKSteps];
@@ -451,14 +465,12 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
         for (int ks = 0; ks < C::kKSteps; ++ks) {
             const int s = ks / C::kKPerSeg, jj = ks % C::kKPerSeg;
             const int d0 = s * (64 / C::kElem) + c * (16 / C::kElem) + 4 * jj;
-            raw[ks] = g < G ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
+            raw[ks] = hl < G ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
         }
+        uint2 frag[C::kKSteps];
         if constexpr (BF16) {
 #pragma unroll
-            for (int ks = 0; ks < C::kKSteps; ++ks) {
-                qb[ks][0] = raw[ks].x;
-                qb[ks][1] = raw[ks].y;
-            }
+            for (int ks = 0; ks < C::kKSteps; ++ks) frag[ks] = raw[ks];
             qscale = p.scale_log2;
         } else {
             float amax = 0.f;
@@ -481,16 +493,34 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
             const float f = ldexpf(1.f, e);
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
-                qb[ks][0] = pack_f16x2(bf16_bits_to_float(raw[ks].x & 0xffffu) * f,
-                                       bf16_bits_to_float(raw[ks].x >> 16) * f);
-                qb[ks][1] = pack_f16x2(bf16_bits_to_float(raw[ks].y & 0xffffu) * f,
-                                       bf16_bits_to_float(raw[ks].y >> 16) * f);
+                frag[ks].x = pack_f16x2(bf16_bits_to_float(raw[ks].x & 0xffffu) * f,
+                                        bf16_bits_to_float(raw[ks].x >> 16) * f);
+                frag[ks].y = pack_f16x2(bf16_bits_to_float(raw[ks].y & 0xffffu) * f,
+                                        bf16_bits_to_float(raw[ks].y >> 16) * f);
             }
             qscale = p.scale_log2 * kconst / f;
         }
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            if constexpr (NT == 1) {
+                qb[ks][0] = frag[ks].x;
+                qb[ks][1] = frag[ks].y;
+            } else {
+                qsm[(nt * C::kKSteps + ks) * 32 + lane] = frag[ks];
+            }
+        }
     }
-    hs0 = __shfl_sync(0xffffffffu, qscale, (2 * c) * 4);
-    hs1 = __shfl_sync(0xffffffffu, qscale, (2 * c + 1) * 4);
+    hs[nt][0] = __shfl_sync(0xffffffffu, qscale, (2 * c) * 4);
+    hs[nt][1] = __shfl_sync(0xffffffffu, qscale, (2 * c + 1) * 4);
+    }
+    if constexpr (NT > 1) __syncwarp();     // the fragments are visible to the warp
+    };
+    // B fragment of k-step ks for group nt
+    auto qfrag = [&](int nt, int ks) -> uint2 {
+        if constexpr (NT == 1)
+            return make_uint2(qb[ks][0], qb[ks][1]);
+        else
+            return qsm[(nt * C::kKSteps + ks) * 32 + lane];
     };
 
     // The PV weights w = p * s_v enter the MMA as hi + lo halves (f16 for the
@@ -500,14 +530,18 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     // (divided by 16 at the end, exactly).
     constexpr float kWScale = BF16 ? 1.f : 16.f;
     constexpr float kLazy = BF16 ? 8.f : 4.f;          // log2 headroom of the lazy max
-    float o[C::kMTiles][4];
-    float m0, m1, l0, l1;
+    float o[NT][C::kMTiles][4];
+    float mst[NT][2], lst[NT][2];           // running max and sum, heads 2c and 2c + 1
     auto reset_state = [&]() {
 #pragma unroll
-        for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        // running max starts finite so that a fully masked group gives ex2(-inf) = 0
-        m0 = m1 = kMaxInit;
-        l0 = l1 = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int i = 0; i < C::kMTiles; ++i)
+                o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+            // running max starts finite so that a fully masked group gives ex2(-inf) = 0
+            mst[nt][0] = mst[nt][1] = kMaxInit;
+            lst[nt][0] = lst[nt][1] = 0.f;
+        }
     };
 
     // per-thread shared-memory offsets inside a page tile (fixed for the kernel)
@@ -536,48 +570,54 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
     // (m, l, unnormalised O) goes to workspace slot worker + unit.
     auto finish_segment = [&](int si) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                lst[nt][0] += __shfl_xor_sync(0xffffffffu, lst[nt][0], off);
+                lst[nt][1] += __shfl_xor_sync(0xffffffffu, lst[nt][1], off);
+            }
         }
         const int ub = seg[kSegInts * si + 0], uh = seg[kSegInts * si + 1];
         const int flags = seg[kSegInts * si + 4];
         const bool whole = flags == 6;           // starts and ends the unit
         const float vconst = __int_as_float(seg[kSegInts * si + 8]) / kWScale;
-        const int head0 = 2 * c, head1 = 2 * c + 1;
         const int dbase = perm8(g) * (D / 8);
         const size_t unit = static_cast<size_t>(ub) * p.Hkv + uh;
         const size_t slot = static_cast<size_t>(FP8KV_WORKER) + unit;
-        const float f0 = whole ? (l0 > 0.f ? vconst / l0 : 0.f) : vconst;
-        const float f1 = whole ? (l1 > 0.f ? vconst / l1 : 0.f) : vconst;
 #pragma unroll
-        for (int i = 0; i < C::kMTiles; ++i) {
-            const int d = dbase + 2 * i;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int head0 = nt * 8 + 2 * c, head1 = head0 + 1;
+            const float l0 = lst[nt][0], l1 = lst[nt][1];
+            const float f0 = whole ? (l0 > 0.f ? vconst / l0 : 0.f) : vconst;
+            const float f1 = whole ? (l1 > 0.f ? vconst / l1 : 0.f) : vconst;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int head = hh ? head1 : head0;
-                if (head >= G) continue;
-                const float f = hh ? f1 : f0;
-                const float va = o[i][hh] * f, vb = o[i][2 + hh] * f;
-                if (whole) {
-                    const size_t row = static_cast<size_t>(ub) * p.Hq + uh * G + head;
-                    store_out<BF16>(p.out, p.out_bf16, row * D + d, va);
-                    store_out<BF16>(p.out, p.out_bf16, row * D + d + 1, vb);
-                } else {
-                    float* dst = p.ws_o + (slot * G + head) * D + d;
-                    *reinterpret_cast<float2*>(dst) = make_float2(va, vb);
+            for (int i = 0; i < C::kMTiles; ++i) {
+                const int d = dbase + 2 * i;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int head = hh ? head1 : head0;
+                    if (head >= G) continue;
+                    const float f = hh ? f1 : f0;
+                    const float va = o[nt][i][hh] * f, vb = o[nt][i][2 + hh] * f;
+                    if (whole) {
+                        const size_t row = static_cast<size_t>(ub) * p.Hq + uh * G + head;
+                        store_out<BF16>(p.out, p.out_bf16, row * D + d, va);
+                        store_out<BF16>(p.out, p.out_bf16, row * D + d + 1, vb);
+                    } else {
+                        float* dst = p.ws_o + (slot * G + head) * D + d;
+                        *reinterpret_cast<float2*>(dst) = make_float2(va, vb);
+                    }
                 }
             }
-        }
-        if (whole) return;
-        if (g == 0) {
-            if (head0 < G) {
-                p.ws_m[slot * G + head0] = m0;
-                p.ws_l[slot * G + head0] = l0;
-            }
-            if (head1 < G) {
-                p.ws_m[slot * G + head1] = m1;
-                p.ws_l[slot * G + head1] = l1;
+            if (!whole && g == 0) {
+                if (head0 < G) {
+                    p.ws_m[slot * G + head0] = mst[nt][0];
+                    p.ws_l[slot * G + head0] = l0;
+                }
+                if (head1 < G) {
+                    p.ws_m[slot * G + head1] = mst[nt][1];
+                    p.ws_l[slot * G + head1] = l1;
+                }
             }
         }
     };
@@ -761,10 +801,14 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
             }
         }
 
-        // ---- S^T = K_page Q^T for each page (rows: tokens tA, tB; cols: heads 2c, 2c+1)
-        float acc[PPI][4];
+        // ---- S^T = K_page Q^T for each page (rows: tokens tA, tB; cols: heads 2c, 2c+1
+        //      of each 8-head group)
+        float acc[NT][PPI][4];
 #pragma unroll
-        for (int k = 0; k < PPI; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < PPI; ++k)
+                acc[nt][k][0] = acc[nt][k][1] = acc[nt][k][2] = acc[nt][k][3] = 0.f;
 #pragma unroll
         for (int s = 0; s < C::kSegs; ++s) {
             uint4 kx[PPI], ky[PPI];
@@ -781,21 +825,31 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                     const uint32_t wx[4] = {kx[k].x, kx[k].y, kx[k].z, kx[k].w};
                     const uint32_t wy[4] = {ky[k].x, ky[k].y, ky[k].z, ky[k].w};
                     if constexpr (BF16) {
-                        mma_bf16(acc[k], wx[2 * jj], wy[2 * jj], wx[2 * jj + 1], wy[2 * jj + 1],
-                                 qb[ks][0], qb[ks][1]);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 qf = qfrag(nt, ks);
+                            mma_bf16(acc[nt][k], wx[2 * jj], wy[2 * jj], wx[2 * jj + 1],
+                                     wy[2 * jj + 1], qf.x, qf.y);
+                        }
                     } else {
                         uint32_t xl, xh, yl, yh;
                         f16x2x2_from_e4m3x4(wx[jj], xl, xh);
                         f16x2x2_from_e4m3x4(wy[jj], yl, yh);
-                        mma_f16(acc[k], xl, yl, xh, yh, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 qf = qfrag(nt, ks);
+                            mma_f16(acc[nt][k], xl, yl, xh, yh, qf.x, qf.y);
+                        }
                     }
                 }
             }
         }
 
         // ---- logits (base 2), masked outside [lo, ctx) on boundary pages
-        float z[PPI][4], vs[PPI][2];
-        float mx0 = neg_inf(), mx1 = neg_inf();
+        float z[NT][PPI][4], vs[PPI][2];
+        float mx[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = neg_inf();
 #pragma unroll
         for (int k = 0; k < PPI; ++k) {
             const int posA = pos0 + k * kPage + tA, posB = pos0 + k * kPage + tB;
@@ -812,69 +866,71 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                 vs[k][0] = vA ? sk[16 + tA] : 0.f;
                 vs[k][1] = vB ? sk[16 + tB] : 0.f;
             }
-            z[k][0] = vA ? acc[k][0] * hs0 * ksA : neg_inf();
-            z[k][1] = vA ? acc[k][1] * hs1 * ksA : neg_inf();
-            z[k][2] = vB ? acc[k][2] * hs0 * ksB : neg_inf();
-            z[k][3] = vB ? acc[k][3] * hs1 * ksB : neg_inf();
-            mx0 = fmaxf(mx0, fmaxf(z[k][0], z[k][2]));
-            mx1 = fmaxf(mx1, fmaxf(z[k][1], z[k][3]));
-        }
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        // lazy running max: move it only when the group exceeds it by 2^kLazy
-        if (mx0 > m0 + kLazy) {
-            const float a = ex2(m0 - mx0);
-            l0 *= a;
-#pragma unroll
-            for (int i = 0; i < C::kMTiles; ++i) {
-                o[i][0] *= a;
-                o[i][2] *= a;
+            for (int nt = 0; nt < NT; ++nt) {
+                z[nt][k][0] = vA ? acc[nt][k][0] * hs[nt][0] * ksA : neg_inf();
+                z[nt][k][1] = vA ? acc[nt][k][1] * hs[nt][1] * ksA : neg_inf();
+                z[nt][k][2] = vB ? acc[nt][k][2] * hs[nt][0] * ksB : neg_inf();
+                z[nt][k][3] = vB ? acc[nt][k][3] * hs[nt][1] * ksB : neg_inf();
+                mx[nt][0] = fmaxf(mx[nt][0], fmaxf(z[nt][k][0], z[nt][k][2]));
+                mx[nt][1] = fmaxf(mx[nt][1], fmaxf(z[nt][k][1], z[nt][k][3]));
             }
-            m0 = mx0;
         }
-        if (mx1 > m1 + kLazy) {
-            const float a = ex2(m1 - mx1);
-            l1 *= a;
 #pragma unroll
-            for (int i = 0; i < C::kMTiles; ++i) {
-                o[i][1] *= a;
-                o[i][3] *= a;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx[nt][0] = fmaxf(mx[nt][0], __shfl_xor_sync(0xffffffffu, mx[nt][0], off));
+                mx[nt][1] = fmaxf(mx[nt][1], __shfl_xor_sync(0xffffffffu, mx[nt][1], off));
             }
-            m1 = mx1;
+            // lazy running max: move it only when the group exceeds it by 2^kLazy
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (mx[nt][hh] > mst[nt][hh] + kLazy) {
+                    const float a = ex2(mst[nt][hh] - mx[nt][hh]);
+                    lst[nt][hh] *= a;
+#pragma unroll
+                    for (int i = 0; i < C::kMTiles; ++i) {
+                        o[nt][i][hh] *= a;
+                        o[nt][i][2 + hh] *= a;
+                    }
+                    mst[nt][hh] = mx[nt][hh];
+                }
+            }
         }
 
 #pragma unroll
         for (int k = 0; k < PPI; ++k) {
-            // masked logits are -inf and give weight 0 (the running max is finite)
-            const float p0 = ex2(z[k][0] - m0), p1 = ex2(z[k][1] - m1);
-            const float p2 = ex2(z[k][2] - m0), p3 = ex2(z[k][3] - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // (clamped: only a per-token V scale above ~256 could reach f16's max)
-            const float w0 = fminf(p0 * vs[k][0] * kWScale, 65504.f);
-            const float w1 = fminf(p1 * vs[k][0] * kWScale, 65504.f);
-            const float w2 = fminf(p2 * vs[k][1] * kWScale, 65504.f);
-            const float w3 = fminf(p3 * vs[k][1] * kWScale, 65504.f);
-
-            // ---- P^T as the B operand: hi + lo halves, transposed by movmatrix
-            uint32_t bh0, bh1, bl0, bl1;
-            if constexpr (BF16) {
-                const uint32_t hA = pack_bf16x2(w0, w1), hB = pack_bf16x2(w2, w3);
-                const float2 fA = unpack_bf16x2(hA), fB = unpack_bf16x2(hB);
-                bh0 = movmatrix_trans(hA);
-                bh1 = movmatrix_trans(hB);
-                bl0 = movmatrix_trans(pack_bf16x2(w0 - fA.x, w1 - fA.y));
-                bl1 = movmatrix_trans(pack_bf16x2(w2 - fB.x, w3 - fB.y));
-            } else {
-                const uint32_t hA = pack_f16x2(w0, w1), hB = pack_f16x2(w2, w3);
-                const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
-                bh0 = movmatrix_trans(hA);
-                bh1 = movmatrix_trans(hB);
-                bl0 = movmatrix_trans(pack_f16x2(w0 - fA.x, w1 - fA.y));
-                bl1 = movmatrix_trans(pack_f16x2(w2 - fB.x, w3 - fB.y));
+            // ---- P^T as the B operand of each group: hi + lo halves, transposed by
+            //      movmatrix; masked logits are -inf and give weight 0 (the running
+            //      max is finite)
+            uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float p0 = ex2(z[nt][k][0] - mst[nt][0]), p1 = ex2(z[nt][k][1] - mst[nt][1]);
+                const float p2 = ex2(z[nt][k][2] - mst[nt][0]), p3 = ex2(z[nt][k][3] - mst[nt][1]);
+                lst[nt][0] += p0 + p2;
+                lst[nt][1] += p1 + p3;
+                // (clamped: only a per-token V scale above ~256 could reach f16's max)
+                const float w0 = fminf(p0 * vs[k][0] * kWScale, 65504.f);
+                const float w1 = fminf(p1 * vs[k][0] * kWScale, 65504.f);
+                const float w2 = fminf(p2 * vs[k][1] * kWScale, 65504.f);
+                const float w3 = fminf(p3 * vs[k][1] * kWScale, 65504.f);
+                if constexpr (BF16) {
+                    const uint32_t hA = pack_bf16x2(w0, w1), hB = pack_bf16x2(w2, w3);
+                    const float2 fA = unpack_bf16x2(hA), fB = unpack_bf16x2(hB);
+                    bh[nt][0] = movmatrix_trans(hA);
+                    bh[nt][1] = movmatrix_trans(hB);
+                    bl[nt][0] = movmatrix_trans(pack_bf16x2(w0 - fA.x, w1 - fA.y));
+                    bl[nt][1] = movmatrix_trans(pack_bf16x2(w2 - fB.x, w3 - fB.y));
+                } else {
+                    const uint32_t hA = pack_f16x2(w0, w1), hB = pack_f16x2(w2, w3);
+                    const float2 fA = unpack_f16x2(hA), fB = unpack_f16x2(hB);
+                    bh[nt][0] = movmatrix_trans(hA);
+                    bh[nt][1] = movmatrix_trans(hB);
+                    bl[nt][0] = movmatrix_trans(pack_f16x2(w0 - fA.x, w1 - fA.y));
+                    bl[nt][1] = movmatrix_trans(pack_f16x2(w2 - fB.x, w3 - fB.y));
+                }
             }
 
             // ---- V rows of tokens c, c+4, c+8, c+12 (k-slots 2c, 2c+1, 2c+8, 2c+9)
@@ -918,8 +974,11 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                     a1 = __byte_perm(vr[0][i], vr[1][i], 0x7632);
                     a2 = __byte_perm(vr[2][i], vr[3][i], 0x5410);
                     a3 = __byte_perm(vr[2][i], vr[3][i], 0x7632);
-                    mma_bf16(o[i], a0, a1, a2, a3, bh0, bh1);
-                    mma_bf16(o[i], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_bf16(o[nt][i], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                        mma_bf16(o[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    }
                 } else {
                     const int w = i >> 1;
                     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
@@ -927,8 +986,11 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 3 : 1)
                     const uint32_t x23 = __byte_perm(vr[2][w], vr[3][w], sel);
                     f16x2x2_from_e4m3x4(x01, a0, a1);
                     f16x2x2_from_e4m3x4(x23, a2, a3);
-                    mma_f16(o[i], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16(o[i], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16(o[nt][i], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                        mma_f16(o[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
         }
@@ -1065,12 +1127,12 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     }
 }
 
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED>
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          cudaStream_t stream) {
-    using C = Cfg<D, BF16>;
+    using C = Cfg<D, BF16, NT>;
     constexpr int kSmemBytes = FUSED ? C::kSmemFused : C::kSmem;
-    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED>;
+    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED, NT>;
     // opt in to the large dynamic shared-memory size once per context
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmemBytes, attr_done);
@@ -1101,37 +1163,48 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     return cudaLaunchKernelEx(&mcfg, split_merge_kernel<D>, p);
 }
 
-template <int D, bool FUSED>
+template <int D, bool FUSED, int NT>
 cudaError_t dispatch_dtype(const DecodeParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int kv_dtype, cudaStream_t s) {
-    if (kv_dtype == FP8KV_KV_BF16) return launch_split<D, true, false, FUSED>(p, kmap, vmap, s);
+    if (kv_dtype == FP8KV_KV_BF16)
+        return launch_split<D, true, false, FUSED, NT>(p, kmap, vmap, s);
     if (p.scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD)
-        return launch_split<D, false, true, FUSED>(p, kmap, vmap, s);
-    return launch_split<D, false, false, FUSED>(p, kmap, vmap, s);
+        return launch_split<D, false, true, FUSED, NT>(p, kmap, vmap, s);
+    return launch_split<D, false, false, FUSED, NT>(p, kmap, vmap, s);
 }
 
 template <int D>
 cudaError_t dispatch_fused(const DecodeParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int kv_dtype, bool fused, cudaStream_t s) {
-    return fused ? dispatch_dtype<D, true>(p, kmap, vmap, kv_dtype, s)
-                 : dispatch_dtype<D, false>(p, kmap, vmap, kv_dtype, s);
+    if (p.G > 8)
+        return fused ? dispatch_dtype<D, true, 2>(p, kmap, vmap, kv_dtype, s)
+                     : dispatch_dtype<D, false, 2>(p, kmap, vmap, kv_dtype, s);
+    return fused ? dispatch_dtype<D, true, 1>(p, kmap, vmap, kv_dtype, s)
+                 : dispatch_dtype<D, false, 1>(p, kmap, vmap, kv_dtype, s);
 }
 
-template <int D, bool BF16>
-constexpr int smem_of() { return Cfg<D, BF16>::kSmemFused; }
+template <int D, bool BF16, int NT>
+constexpr int smem_of() { return Cfg<D, BF16, NT>::kSmemFused; }
+
+template <int D, int NT>
+int ctas_of(bool bf) {
+    const int bytes = bf ? smem_of<D, true, NT>() : smem_of<D, false, NT>();
+    const int by_smem = (228 * 1024) / (bytes + 1024);
+    const int by_regs = decode_min_ctas<D, NT>();      // the launch bounds' register budget
+    const int n = by_smem < by_regs ? by_smem : by_regs;
+    return n < 1 ? 1 : n;
+}
 
 }  // namespace
 
-int decode_ctas_per_sm(int D, int kv_dtype) {
-    int bytes;
+int decode_ctas_per_sm(int D, int kv_dtype, int G) {
     const bool bf = kv_dtype == FP8KV_KV_BF16;
+    const bool two = G > 8;
     switch (D) {
-        case 64: bytes = bf ? smem_of<64, true>() : smem_of<64, false>(); break;
-        case 128: bytes = bf ? smem_of<128, true>() : smem_of<128, false>(); break;
-        default: bytes = bf ? smem_of<256, true>() : smem_of<256, false>(); break;
+        case 64: return two ? ctas_of<64, 2>(bf) : ctas_of<64, 1>(bf);
+        case 128: return two ? ctas_of<128, 2>(bf) : ctas_of<128, 1>(bf);
+        default: return two ? ctas_of<256, 2>(bf) : ctas_of<256, 1>(bf);
     }
-    int n = (228 * 1024) / (bytes + 1024);
-    return n < 1 ? 1 : (n > 4 ? 4 : n);
 }
 
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& kmap,

@@ -124,6 +124,8 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
 
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;
-int decode_ctas_per_sm(int D, int kv_dtype);
+// CTAs of the decode kernel resident per SM (shared memory and the register
+// budget of its launch bounds) for head dim D and G query heads per KV head.
+int decode_ctas_per_sm(int D, int kv_dtype, int G);
 
 }  // namespace fp8kv

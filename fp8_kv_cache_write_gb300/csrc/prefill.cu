@@ -84,11 +84,17 @@ struct PCfg {
     static constexpr int kElem = BF16 ? 2 : 1;
     static constexpr int kKeys = (BF16 || SPLIT) ? 64 : 128;
     static constexpr int kRowB = D * kElem;                 // bytes of a Q / K / V row
+    // Q, K and V rows are kept as panels of 128 bytes (128-byte swizzle), or as
+    // one 64-byte panel with the 64-byte swizzle (e4m3 at D 64); P rows are 128 bytes
+    static constexpr int kPanelB = kRowB < 128 ? kRowB : 128;
+    static constexpr int kCPR = kPanelB / 16;               // 16-byte chunks of a panel row
+    static constexpr int kKPP = kPanelB / 32;               // 32-byte k-steps of a panel row
+    static constexpr uint32_t kLayout = kPanelB == 128 ? kLayoutSw128 : kLayoutSw64;
     // tensor memory: S (or the two-level P V tile) from column 0, O from the
     // kernel's kOCol; D 128 takes 256 columns so two co-resident CTAs never wait
     // on each other
     static constexpr uint32_t kTmemCols = D <= 128 ? 256u : 512u;
-    static constexpr int kPanels = kRowB / 128;             // 128-byte panels of a row
+    static constexpr int kPanels = kRowB / kPanelB;         // panels of a row
     static constexpr int kQTerms = SPLIT ? 2 : 1;           // Q tiles (hi, lo)
     static constexpr int kQBytes = kRows * kRowB;           // one Q tile
     static constexpr int kKVBytes = kKeys * kRowB;          // one K (or V) tile
@@ -129,6 +135,8 @@ struct PCfg {
 // Dynamic shared memory of the kernel: the larger of its two operand layouts.
 template <int D, bool BF16>
 constexpr int prefill_smem() {
+    static_assert(PCfg<D, BF16, false>::kPanelB == 128 || PCfg<D, BF16, false>::kPanelB == 64,
+                  "panel rows of 64 or 128 bytes");
     return BF16 ? PCfg<D, true, false>::kSmem
                 : (PCfg<D, false, false>::kSmem > PCfg<D, false, true>::kSmem
                        ? PCfg<D, false, false>::kSmem
@@ -178,6 +186,17 @@ __device__ __forceinline__ float pow2_ceil(float x) {
 // 2^e as a float, e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) {
     return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
+// Byte offset of 16-byte chunk cc of row r in a panel of `panel_b`-byte rows laid
+// out as TMA's 128-byte (8 chunks, XOR row % 8) or 64-byte (4 chunks, XOR
+// (row / 2) % 4) swizzle writes it.
+template <int PANEL_B>
+__device__ __forceinline__ int swz_off(int r, int cc) {
+    if constexpr (PANEL_B == 128)
+        return r * 128 + ((cc ^ (r & 7)) << 4);
+    else
+        return r * 64 + ((cc ^ ((r >> 1) & 3)) << 4);
 }
 
 // Named barrier of the softmax warps only (the loader and MMA warps run on).
@@ -327,8 +346,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                     }
                 }
             }
-            const int panel = c >> 3, cc = c & 7;
-            const int off = panel * (kRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4);
+            const int panel = c / C::kCPR, cc = c % C::kCPR;
+            const int off = panel * (kRows * C::kPanelB) + swz_off<C::kPanelB>(r, cc);
             *reinterpret_cast<uint4*>(qtile + off) = make_uint4(w[0], w[1], w[2], w[3]);
             if constexpr (SPLIT)
                 *reinterpret_cast<uint4*>(qtile + C::kQBytes + off) =
@@ -389,8 +408,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             if (lane < n_pages) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_3d(dst + pn * (kKeys * 128) + lane * 2048, map, pn * 128, 0, z,
-                                bar(full0 + st));
+                    tma_load_3d(dst + pn * (kKeys * C::kPanelB) + lane * (kPage * C::kPanelB), map,
+                                pn * C::kPanelB, 0, z, bar(full0 + st));
                 if constexpr (PT) {
                     // the tile's K and V scale rows, into slot j % 4 (the softmax of
                     // tile j - 4 has finished with it: QK of j - 2 ran after it)
@@ -432,13 +451,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 const uint32_t kbase = sbase + C::kOffKV + (j & 1) * 2 * C::kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < C::kRowB / 32; ++kk) {    // 32-byte k-steps over D
-                    const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * (kKeys * 128) +
-                                                            (kk & 3) * 32, 16, 1024);
+                    const int pn = kk / C::kKPP, ks = kk % C::kKPP;
+                    const uint32_t off = pn * (kRows * C::kPanelB) + ks * 32;
+                    const uint64_t bd = smem_desc(kbase + pn * (kKeys * C::kPanelB) + ks * 32, 16,
+                                                  8 * C::kPanelB, C::kLayout);
 #pragma unroll
                     for (int t = 0; t < C::kQTerms; ++t) {       // split: Q hi, then Q lo
-                        const uint64_t ad =
-                            smem_desc_sw128(sbase + C::kOffQ + t * C::kQBytes + off, 16, 1024);
+                        const uint64_t ad = smem_desc(sbase + C::kOffQ + t * C::kQBytes + off, 16,
+                                                      8 * C::kPanelB, C::kLayout);
                         mma(tS, ad, bd, idesc_qk, (kk > 0 || t > 0) ? 1u : 0u);
                     }
                 }
@@ -454,10 +474,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 for (int kk = 0; kk < 128 / 32; ++kk) {
                     const int vk = kk % C::kPVSteps;
                     const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
-                    // V: MN-major; 8-key groups 1024 B apart, 128-byte D panels
-                    // kKeys * 128 B apart; one k-step = 32 / elem keys
-                    const uint64_t bd = smem_desc_sw128(vbase + vk * (32 / C::kElem) * 128,
-                                                        kKeys * 128, 1024);
+                    // V: MN-major; 8-key groups 8 panel rows apart, D panels
+                    // kKeys panel rows apart; one k-step = 32 / elem keys
+                    const uint64_t bd =
+                        smem_desc(vbase + vk * (32 / C::kElem) * C::kPanelB, kKeys * C::kPanelB,
+                                  8 * C::kPanelB, C::kLayout);
                     const uint32_t acc = TWO_LEVEL ? (kk > 0 ? 1u : 0u)
                                                    : ((j > 0 || kk > 0) ? 1u : 0u);
                     mma(tO, ad, bd, idesc_pv, acc);
@@ -781,11 +802,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                     break;
                 }
                 uint8_t* vt = smem + C::kOffKV + st * 2 * C::kKVBytes + C::kKVBytes;
-                for (int idx = tid; idx < kKeys * C::kPanels * 8; idx += kSoft) {
-                    const int chunk = idx & 7, row = (idx >> 3) % kKeys, pn = (idx >> 3) / kKeys;
+                for (int idx = tid; idx < kKeys * C::kPanels * C::kCPR; idx += kSoft) {
+                    const int chunk = idx % C::kCPR, row = (idx / C::kCPR) % kKeys,
+                              pn = (idx / C::kCPR) / kKeys;
                     if (j * kKeys + row >= ctx)
-                        *reinterpret_cast<uint4*>(vt + pn * (kKeys * 128) + row * 128 +
-                                                  chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vt + pn * (kKeys * C::kPanelB) +
+                                                  row * C::kPanelB + chunk * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async();
@@ -969,6 +992,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int D, int kv_dtype, int two_level,
                            int grid_x, cudaStream_t stream) {
     const bool bf = kv_dtype == FP8KV_KV_BF16;
+    if (D == 64) return launch_d<64>(p, kmap, vmap, bf, two_level, grid_x, stream);
     if (D == 128) return launch_d<128>(p, kmap, vmap, bf, two_level, grid_x, stream);
     return launch_d<256>(p, kmap, vmap, bf, two_level, grid_x, stream);
 }

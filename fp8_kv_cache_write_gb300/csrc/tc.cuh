@@ -31,16 +31,25 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor: start address, leading / stride byte offsets
-// (all >> 4), descriptor version 1, swizzle mode 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+// (all >> 4), descriptor version 1, layout type in bits 61..63 (2 = 128-byte
+// swizzle, 4 = 64-byte swizzle).
+constexpr uint32_t kLayoutSw128 = 2u;
+constexpr uint32_t kLayoutSw64 = 4u;
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(2u) << 61;
+    d |= static_cast<uint64_t>(layout) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, kLayoutSw128);
 }
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with an fp32 accumulator:

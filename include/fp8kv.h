@@ -38,8 +38,9 @@
  *     Per-token-head scales live beside the pages in fp32
  *     k_scale_cache / v_scale_cache [num_blocks][Hkv][16], indexed by the same
  *     block id and in-page offset.
- *   - Supported shapes: D in {64, 128, 256}; Hq % Hkv == 0; Hq / Hkv <= 8 for
- *     attention; base addresses 16-byte aligned.
+ *   - Supported shapes: D in {64, 128, 256}; Hq % Hkv == 0; decode attention
+ *     takes Hq / Hkv <= 16, prefill Hq / Hkv dividing 128; base addresses
+ *     16-byte aligned.
  */
 #ifndef FP8KV_H
 #define FP8KV_H
@@ -239,7 +240,7 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
  *                  them; setting both is FP8KV_ERR_INVALID, as is any other bit.
  *   out            [Tq][Hq][D] fp32 or bf16.
  * Supported: e4m3 cache (every scale mode) and its bf16 twin (bf16 Q, P and
- * cache, kind::f16; scales ignored), D in {128, 256}, Hq / Hkv dividing 128.
+ * cache, kind::f16; scales ignored), D in {64, 128, 256}, Hq / Hkv dividing 128.
  * Other shapes return FP8KV_ERR_UNSUPPORTED.  With q_scale or prob_scale equal
  * to 1.0 an e4m3 call succeeds and sets fp8kv_last_warning().
  */

@@ -103,7 +103,7 @@ def test_decode_rejects_bad_arguments_without_a_gpu(lib):
 
     assert call() == -1            # null pointers
     assert call(Hq=9) == -1        # Hq % Hkv
-    assert call(Hq=32, Hkv=2) == -2   # group of 16 query heads
+    assert call(Hq=34, Hkv=2) == -2   # group of 17 query heads (16 at most)
     assert call(D=80) == -2
     assert call(dtype=2) == -1
     assert call(mode=7) == -1
@@ -132,7 +132,7 @@ def test_prefill_rejects_bad_arguments_without_a_gpu(lib):
     assert call() == -1                 # null pointers
     assert call(Hq=9, Hkv=2) == -1      # Hq % Hkv
     assert call(Hq=9) == -2             # a group of 9 does not tile 128 MMA rows
-    assert call(D=64) == -2             # prefill tiles: D 128 or 256
+    assert call(D=80) == -2             # prefill tiles: D 64, 128 or 256
     assert call(dtype=2) == -1
     assert call(mode=3) == -1
     assert call(out_dtype=2) == -1

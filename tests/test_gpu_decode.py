@@ -42,10 +42,20 @@ def _check(w, kv_dtype, units=None, **kw):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8, 12, 16])
 def test_decode_ragged_parity(D, kv_dtype, mode, G):
     w = synth.decode_workload(100 + D + G, RAGGED, 2 * G, 2, D, mode, outlier_frac=0.01)
     e, _, _ = _check(w, kv_dtype)
+    assert e <= DECODE_TOL, e
+
+
+@pytest.mark.parametrize("G", [8, 16])
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_gqa_groups_beyond_eight_heads(G, splits):
+    # more than 8 query heads per KV head: two 8-head MMA groups share every
+    # K and V page; long, split contexts and per-token-head scales
+    w = synth.decode_workload(70 + G, [3000, 77, 1500], 2 * G, 2, 128, 2, outlier_frac=0.01)
+    e, _, _ = _check(w, 0, num_splits=splits)
     assert e <= DECODE_TOL, e
 
 

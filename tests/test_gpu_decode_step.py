@@ -45,7 +45,7 @@ def _history_only(w, kv_dtype, fill=None, err=None):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
-@pytest.mark.parametrize("G", [1, 8])
+@pytest.mark.parametrize("G", [1, 8, 16])
 def test_step_parity(D, kv_dtype, mode, G):
     w = synth.decode_workload(300 + D + G, RAGGED, 2 * G, 2, D, mode, outlier_frac=0.01)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -147,6 +147,23 @@ def test_prefill_q_and_prob_scales():
     assert float((scaled - plain).abs().max()) <= PREFILL_TOL
 
 
+@pytest.mark.parametrize("two_level", [False, True])
+@pytest.mark.parametrize("scale_mode", [0, 2])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (64, 8)])
+def test_prefill_head_dim_64(two_level, scale_mode, Hq, Hkv):
+    # head_dim 64 ("커널 및 퓨전 최적화": prefill tiling for head_dim 64): 64-byte
+    # e4m3 rows; rows under 8192 keys take split operands, the 9000-key sequence
+    # single ones
+    w = synth.prefill(seed=410 + Hq + scale_mode, ctx=(700, 9000, 33), chunk=(123, 160, 33),
+                      Hq=Hq, Hkv=Hkv, D=64)
+    dev_c, host_c = _caches(w, scale_mode=scale_mode)
+    out = _gpu(w, dev_c, scale_mode=scale_mode, two_level=two_level).cpu().numpy()
+    units = _rows(w, 3) if Hq == 8 else [(t, h) for t, h in _rows(w, 3) if h % 7 == 0]
+    ref = _oracle(w, host_c, units, scale_mode=scale_mode)
+    err = _max_err(w, out, ref, units)
+    assert err <= PREFILL_TOL, err
+
+
 def test_prefill_with_prequantized_q_isolates_p_rounding():
     # Single operands.  Feed the oracle the e4m3-rounded queries (its own
     # encoder, q_scale 1): the exact attention of those queries differs from
@@ -393,7 +410,8 @@ def _bf16_caches(w):
 
 @pytest.mark.parametrize("two_level", [False, True])
 @pytest.mark.parametrize("D,Hq,Hkv,ctx,chunk", [(256, 8, 1, (4100, 700), (123, 300)),
-                                                 (128, 8, 2, (5000, 33), (200, 33))])
+                                                 (128, 8, 2, (5000, 33), (200, 33)),
+                                                 (64, 64, 8, (3000, 17), (150, 17))])
 def test_bf16_twin_parity(two_level, D, Hq, Hkv, ctx, chunk):
     # The bf16 twin keeps Q in bf16 and rounds P to bf16 (8 mantissa bits), so it
     # meets the 1e-2 bar at every context length.

@@ -528,6 +528,62 @@ def _copies_for(bytes_per_copy):
     return max(2, math.ceil(260e6 / max(bytes_per_copy, 1)))
 
 
+def _oracle_decode_baseline(w, kv_dtype, mode, seconds=6.0, max_units=None):
+    """The oracle (float64, every host core) on a bounded sample of a decode
+    workload's (sequence, query head) units, extrapolated to the whole call.
+    Its cache is written by the oracle's own writer from the same bf16 inputs."""
+    import numpy as np
+
+    import oracle
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    nb, Hkv, D = w.num_blocks, w.Hkv, w.D
+    dt = np.uint8 if kv_dtype == 0 else np.uint16
+    kc, vc = np.zeros((nb, Hkv, 16, D), dt), np.zeros((nb, Hkv, 16, D), dt)
+    ks, vs = np.zeros((nb, Hkv, 16), np.float32), np.zeros((nb, Hkv, 16), np.float32)
+    k_s = None if w.k_scale is None else w.k_scale.cpu().numpy()
+    v_s = None if w.v_scale is None else w.v_scale.cpu().numpy()
+    for k, v, sl in ((w.k_hist, w.v_hist, w.hist_slots), (w.k_new, w.v_new, w.new_slots)):
+        assert oracle.kv_cache_write(bits(k), bits(v), sl.cpu().numpy(), kc, vc,
+                                     kv_dtype=kv_dtype, scale_mode=mode, k_scale=k_s,
+                                     v_scale=v_s, k_scale_cache=ks, v_scale_cache=vs) == 0
+    cores = len(os.sched_getaffinity(0))
+    ctx = w.context_lens.cpu().numpy()
+    vis = np.minimum(ctx, w.window) if w.window > 0 else ctx
+    all_units = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(all_units))
+    units, passes, secs = [], 0, 0.0
+    n = 4 if max_units is None else max_units
+    while True:                         # grow the sample until it takes ~1/4 of the budget
+        units = [all_units[i] for i in order[:n]]
+        t = time.perf_counter()
+        st, _ = oracle.decode_attn(bits(w.q), kc, vc, w.block_table.cpu().numpy(), ctx,
+                                   kv_dtype=kv_dtype, scale_mode=mode, k_scale=k_s,
+                                   v_scale=v_s, k_scale_cache=ks, v_scale_cache=vs,
+                                   window=w.window, units=units, nthreads=cores)
+        dt_s = time.perf_counter() - t
+        assert st == 0
+        if dt_s > seconds / 4 or n >= len(all_units) or max_units is not None:
+            break
+        n = min(len(all_units), n * 4)
+    secs, passes = dt_s, 1
+    while secs < seconds and passes < 64:
+        t = time.perf_counter()
+        oracle.decode_attn(bits(w.q), kc, vc, w.block_table.cpu().numpy(), ctx,
+                           kv_dtype=kv_dtype, scale_mode=mode, k_scale=k_s, v_scale=v_s,
+                           k_scale_cache=ks, v_scale_cache=vs, window=w.window, units=units,
+                           nthreads=cores)
+        secs += time.perf_counter() - t
+        passes += 1
+    keys_sample = sum(int(vis[b]) for b, _ in units)
+    keys_all = sum(int(vis[b]) for b, _ in all_units)
+    call_s = secs / passes * keys_all / max(keys_sample, 1)
+    return {"kind": "oracle", "cores": cores, "ms_per_call": call_s * 1e3,
+            "tokens_per_s": w.B / call_s,
+            "sample": f"{len(units)} of {len(all_units)} (sequence, query head) units, "
+                      f"{passes} pass(es), {secs:.1f} s; extrapolated by visible keys"}
+
+
 def run_extras(args, dev):
     """The other workloads: decode time against context length (fp8 vs bf16),
     the 131k needle, the 24-layer hybrid model, chunked FP8 prefill and the
@@ -588,7 +644,10 @@ def run_extras(args, dev):
             f["break_even_ctx"] = (f["a_us"] - fit["bf16"]["a_us"]) / db if db > 0 else None
         emit(fit)
 
-    # (2)-(5) the 131072-token needle, the hybrid model, prefill, the bulk write
+    # (2)-(6) the tiny decode, the 131072-token needle, the hybrid model, prefill,
+    # the bulk write
+    if want("tiny"):
+        _extra_tiny(fk, synth, dev, stream, emit)
     if want("needle"):
         _extra_needle(fk, synth, dev, stream, emit)
     if want("hybrid"):
@@ -597,6 +656,22 @@ def run_extras(args, dev):
         _extra_prefill(fk, synth, dev, stream, emit)
     if want("write"):
         _extra_write(fk, dev, stream, emit)
+
+
+def _extra_tiny(fk, synth, dev, stream, emit):
+    # 1 sequence, context 1024, 32/8 heads, D 128, per-tensor scale 1.0: a decode
+    # call is launch- and latency-bound (2 MiB of e4m3 KV)
+    E4, BF = fk.KV_E4M3, fk.KV_BF16
+    w = synth.tiny()
+    row = {"extra": "tiny_decode", "B": 1, "context": 1024}
+    for kv, name in ((E4, "fp8"), (BF, "bf16")):
+        d_b, _ = step_bytes(w, 1 if kv == E4 else 2, False)
+        caches = _caches_for(fk, w, kv, 0, dev, _copies_for(d_b))
+        ms = _time_graph(_decode_caller(fk, w, kv, 0, caches, dev), 64, stream)
+        row[name + "_us"] = ms * 1e3
+        del caches
+    row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 0, seconds=3.0)
+    emit(row)
 
 
 def _extra_needle(fk, synth, dev, stream, emit):
@@ -613,6 +688,7 @@ def _extra_needle(fk, synth, dev, stream, emit):
         del caches
         torch.cuda.empty_cache()
     row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
+    row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 1)
     emit(row)
 
 
@@ -637,16 +713,88 @@ def _extra_hybrid(fk, synth, dev, stream, emit):
                 calls[layer % 2](i * 12 + layer // 2)
         ms = _time_graph(step, 8, stream)
         per_type = [_time_graph(calls[lt], 24, stream) * 1e3 for lt in (0, 1)]
-        emit({"extra": "hybrid_24_layers", "variant": variant, "B": 32,
-              "ms_per_step": ms, "tokens_per_s": 32 / (ms / 1e3),
-              "window_layer_us": per_type[0], "full_layer_us": per_type[1]})
+        line = {"extra": "hybrid_24_layers", "variant": variant, "B": 32,
+                "ms_per_step": ms, "tokens_per_s": 32 / (ms / 1e3),
+                "window_layer_us": per_type[0], "full_layer_us": per_type[1]}
+        if variant == "window_bf16_full_fp8":
+            # the oracle on one layer of each type, 12 of each per step
+            cb = [_oracle_decode_baseline(wl[lt], dtypes[lt] if lt == 0 else 0,
+                                          0 if lt == 0 else 2, seconds=4.0) for lt in (0, 1)]
+            step_ms = 12 * (cb[0]["ms_per_call"] + cb[1]["ms_per_call"])
+            line["cpu_baseline"] = {"kind": "oracle", "cores": cb[1]["cores"],
+                                    "ms_per_step": step_ms, "tokens_per_s": 32 / (step_ms / 1e3),
+                                    "sample": "window layer: " + cb[0]["sample"] +
+                                              "; full layer: " + cb[1]["sample"]}
+        emit(line)
         del calls
         torch.cuda.empty_cache()
+
+
+def _fp8_mm_peak(dev, n=8192, reps=10):
+    """Dense e4m3 GEMM throughput of the library GEMM (torch._scaled_mm, bf16 out):
+    the measured fp8 tensor peak that the prefill's fraction is taken against."""
+    try:
+        g = torch.Generator(device=dev).manual_seed(3)
+        a = torch.randn(n, n, generator=g, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, generator=g, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(reps):
+            t0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            t1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, t0.elapsed_time(t1))
+        return 2.0 * n ** 3 / (best / 1e3) / 1e12
+    except Exception as e:                      # no fp8 GEMM in this torch build
+        return {"unavailable": str(e).splitlines()[0][:120]}
+
+
+def _oracle_prefill_baseline(w, rows=16, seconds=6.0):
+    """The oracle on `rows` query rows spread over the chunk (all query heads),
+    extrapolated to the whole chunk by (query, key) pairs."""
+    import numpy as np
+
+    import oracle
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    nb, Hkv, D = w.num_blocks, w.Hkv, w.D
+    kc, vc = np.zeros((nb, Hkv, 16, D), np.uint8), np.zeros((nb, Hkv, 16, D), np.uint8)
+    one = np.ones(1, np.float32)
+    assert oracle.kv_cache_write(bits(w.k_all), bits(w.v_all), w.all_slots.cpu().numpy(), kc, vc,
+                                 kv_dtype=0, scale_mode=0, k_scale=one, v_scale=one) == 0
+    nq = int(w.cu_seqlens_q[1])
+    c0 = int(w.context_lens[0]) - nq
+    toks = [int(t) for t in np.linspace(0, nq - 1, rows)]
+    units = [(t, h) for t in toks for h in range(w.Hq)]
+    cores = len(os.sched_getaffinity(0))
+    secs, passes = 0.0, 0
+    while passes == 0 or (secs < seconds and passes < 16):
+        t = time.perf_counter()
+        st, _ = oracle.prefill_attn(bits(w.q), w.cu_seqlens_q.cpu().numpy(), kc, vc,
+                                    w.block_table.cpu().numpy(), w.context_lens.cpu().numpy(),
+                                    kv_dtype=0, scale_mode=0, k_scale=one, v_scale=one,
+                                    units=units, nthreads=cores)
+        secs += time.perf_counter() - t
+        passes += 1
+        assert st == 0
+    pairs_sample = sum(c0 + t + 1 for t in toks)
+    pairs_all = sum(c0 + i + 1 for i in range(nq))
+    call_s = secs / passes * pairs_all / pairs_sample
+    return {"kind": "oracle", "cores": cores, "ms_per_call": call_s * 1e3,
+            "tflops": 4.0 * D * w.Hq * pairs_all / call_s / 1e12,
+            "sample": f"{rows} of {nq} query rows x {w.Hq} heads, {passes} pass(es), "
+                      f"{secs:.1f} s; extrapolated by (query, key) pairs"}
 
 
 def _extra_prefill(fk, synth, dev, stream, emit):
     # chunked prefill: 4096 new queries over 32768 cached tokens, 8/1 heads, D=256
     E4, BF = fk.KV_E4M3, fk.KV_BF16
+    peak = _fp8_mm_peak(dev)
+    emit({"extra": "fp8_dense_gemm_peak", "how": "torch._scaled_mm e4m3 8192^3, bf16 out, "
+                                                  "best of 10", "tflops": peak})
     w = synth.prefill(device=dev)
     q, cu = w.q.to(dev), w.cu_seqlens_q.to(dev)
     bt, cl = w.block_table.to(dev), w.context_lens.to(dev)
@@ -670,8 +818,13 @@ def _extra_prefill(fk, synth, dev, stream, emit):
                 q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=kv, k_scale=one, v_scale=one,
                 two_level=two, split=split, out=out)
             ms = _time_graph(fn, 10, stream)
-            emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": name, "two_level": two,
-                  "split": split, "ms": ms, "tflops": flops / ms / 1e9})
+            line = {"extra": "prefill_chunk4096_ctx32768_d256", "kv": name, "two_level": two,
+                    "split": split, "ms": ms, "tflops": flops / ms / 1e9}
+            if kv == E4 and isinstance(peak, float):
+                line["frac_of_fp8_peak"] = flops / ms / 1e9 / peak
+            if kv == E4 and not two and split == "auto":
+                line["cpu_baseline"] = _oracle_prefill_baseline(w)
+            emit(line)
         del kc, vc
         torch.cuda.empty_cache()
     # the same chunk over a per-token-head e4m3 cache (scales computed at write time)
@@ -761,9 +914,8 @@ def main():
                          "older pages are written before the preceding kernel starts)")
     ap.add_argument("--extras", nargs="?", const="all", default=None,
                     choices=["all", "itl", "needle", "hybrid", "prefill", "write"],
-                    help="time the other workloads (context sweep, needle, hybrid, prefill, "
-                         "bulk write; all by default) instead of the headline step; one JSON "
-                         "line each")
+                    help="time the other workloads (itl, tiny, needle, hybrid, prefill, write; "
+                         "all by default) instead of the headline step; one JSON line each")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -895,6 +895,56 @@ def _extra_write(fk, dev, stream, emit):
         torch.cuda.empty_cache()
 
 
+def run_profile_case(args):
+    """A few eager calls of one kernel on one workload, nothing else on the GPU:
+    the target of the ncu captures summarised under profiles/."""
+    import fp8_kv_cache_write_gb300 as fk
+    from fp8_kv_cache_write_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    case = args.profile
+    if case in ("hybrid_full", "hybrid_window", "needle"):
+        if case == "needle":
+            w, kv, mode = synth.needle(device=dev), fk.KV_E4M3, 1
+        else:
+            w = synth.hybrid_layer(layer=1 if case == "hybrid_full" else 0, device=dev)
+            kv = w.extra["kv_dtype"]
+            mode = 2 if kv == fk.KV_E4M3 else 0
+        caches = _caches_for(fk, w, kv, mode, dev, 1)
+        fn = _decode_caller(fk, w, kv, mode, caches, dev, window=w.window)
+    elif case in ("prefill", "prefill_pt"):
+        w = synth.prefill(device=dev)
+        mode = 2 if case == "prefill_pt" else 0
+        one = torch.ones(1, dtype=torch.float32, device=dev)
+        kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=torch.uint8, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.num_blocks, w.Hkv, 16, dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        fk.kv_cache_write(w.k_all.to(dev), w.v_all.to(dev), w.all_slots.to(dev), kc, vc,
+                          kv_dtype=fk.KV_E4M3, scale_mode=mode, k_scale=one, v_scale=one,
+                          k_scale_cache=ks, v_scale_cache=vs)
+        q, cu = w.q.to(dev), w.cu_seqlens_q.to(dev)
+        bt, cl = w.block_table.to(dev), w.context_lens.to(dev)
+        out = torch.empty(q.shape[0], w.Hq, w.D, dtype=torch.float32, device=dev)
+        fn = lambda i: fk.prefill_attn(q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=fk.KV_E4M3,
+                                       scale_mode=mode, k_scale=one, v_scale=one,
+                                       k_scale_cache=ks, v_scale_cache=vs, out=out)
+    else:                                           # bulk write, llama8b history
+        w = synth.llama8b(device=dev)
+        kh, vh, hs = w.k_hist.to(dev), w.v_hist.to(dev), w.hist_slots.to(dev)
+        kc = torch.zeros(w.num_blocks, w.Hkv, 16, w.D, dtype=torch.uint8, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.num_blocks, w.Hkv, 16, dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        fn = lambda i: fk.kv_cache_write(kh, vh, hs, kc, vc, kv_dtype=fk.KV_E4M3,
+                                         scale_mode=fk.SCALE_PER_TOKEN_HEAD,
+                                         k_scale_cache=ks, v_scale_cache=vs)
+    for i in range(args.calls):
+        fn(i)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile": case, "calls": args.calls}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -913,11 +963,20 @@ def main():
                          "first; 2 = early set-up and page streaming: the step's tables and "
                          "older pages are written before the preceding kernel starts)")
     ap.add_argument("--extras", nargs="?", const="all", default=None,
-                    choices=["all", "itl", "needle", "hybrid", "prefill", "write"],
+                    choices=["all", "itl", "tiny", "needle", "hybrid", "prefill", "write"],
                     help="time the other workloads (itl, tiny, needle, hybrid, prefill, write; "
                          "all by default) instead of the headline step; one JSON line each")
+    ap.add_argument("--profile", default=None,
+                    choices=["hybrid_full", "hybrid_window", "needle", "prefill", "prefill_pt",
+                             "write"],
+                    help="run --calls eager calls of one workload's kernel (for profiler "
+                         "captures; prints no measurement)")
+    ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.profile:
+        run_profile_case(args)
+        return
 
     world, rank, local = dist_env()
     if world > 1:

@@ -198,6 +198,9 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
             decode_ctas_per_sm(D, 0, Hkv > 0 ? Hq / Hkv : 1);
         const int64_t by_work = (work + 15) / 16;
         if (by_work < n) n = by_work;
+        // units of at most 16 visible pages (a sliding window): one worker warp
+        // per unit, so that every unit ends in its own warp (no partials to merge)
+        if (maxvis <= 16) n = (units + kDecodeWarps - 1) / kDecodeWarps;
     }
     if (n > work) n = work;
     if (n > 1024) n = 1024;

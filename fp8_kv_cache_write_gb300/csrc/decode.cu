@@ -59,7 +59,8 @@ struct Cfg {
     // two independent pages between waits
     static constexpr int kPPI = kRowB <= 128 ? 2 : 1;
     static constexpr int kStageB = 2 * kPPI * kTileB; // K tiles, then V tiles
-    static constexpr int kStagesRaw = 16384 / kStageB;
+    // bytes in flight per warp: 16 KiB, 12 KiB for 64-byte rows (4 CTAs per SM)
+    static constexpr int kStagesRaw = (kRowB == 64 ? 12288 : 16384) / kStageB;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kSegs = kRowB / 64;          // 64-byte segments of a row
     static constexpr int kKPerSeg = 4 / kElem;        // QK k-steps per segment
@@ -281,16 +282,19 @@ __device__ __noinline__ bool store_new_token_row(const int32_t* bt_row, int64_t 
     return ok;
 }
 
-// CTAs resident per SM: 3 (12 warps, 168 registers at most) for D <= 128 with
-// one 8-head group, else 2.
-template <int D, int NT>
-constexpr int decode_min_ctas() { return D <= 128 && NT == 1 ? 3 : 2; }
+// CTAs resident per SM: 4 (16 warps, 128 registers at most) for 64-byte rows
+// (e4m3 at D 64: short pages, more warps hide their latency), 3 (168 registers)
+// for other rows up to 256 bytes with one 8-head group, else 2.
+template <int D, bool BF16, int NT>
+constexpr int decode_min_ctas() {
+    return NT > 1 || D > 128 ? 2 : (D * (BF16 ? 2 : 1) == 64 ? 4 : 3);
+}
 
 // FUSED: a decode step -- the kernel also stores every sequence's new token
 // (k_new / v_new at position ctx - 1).  NT: 8-head groups per KV head (1 for
 // G <= 8, 2 for G <= 16); the groups share every K and V conversion.
 template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
-__global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, NT>())
+__global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
     using C = Cfg<D, BF16, NT>;
@@ -1190,7 +1194,8 @@ template <int D, int NT>
 int ctas_of(bool bf) {
     const int bytes = bf ? smem_of<D, true, NT>() : smem_of<D, false, NT>();
     const int by_smem = (228 * 1024) / (bytes + 1024);
-    const int by_regs = decode_min_ctas<D, NT>();      // the launch bounds' register budget
+    // the launch bounds' register budget
+    const int by_regs = bf ? decode_min_ctas<D, true, NT>() : decode_min_ctas<D, false, NT>();
     const int n = by_smem < by_regs ? by_smem : by_regs;
     return n < 1 ? 1 : n;
 }

@@ -373,20 +373,27 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
         const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const int32_t* bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
         int issued = 0;
-        // block ids of tile j's pages (lane = page), loaded one tile ahead so that
-        // no iteration waits for its page-table row
-        auto tile_blk = [&](int j) -> int {
-            const int pg = j * (kKeys / kPage) + lane;
-            return (j < n_tiles && lane < kKeys / kPage && pg < ctx_pages) ? bt_row[pg] : 0;
+        // block ids of 32 pages at a time (lane = page), the next 32 loaded while
+        // these are used, so that no tile's copies wait for a page-table row
+        constexpr int kPPT = kKeys / kPage;            // pages per tile (8 or 4)
+        static_assert(32 % kPPT == 0, "a tile's pages lie in one batch of 32");
+        auto bt_load = [&](int base) -> int {
+            const int pg = base + lane;
+            return pg < ctx_pages ? bt_row[pg] : 0;
         };
-        int blk_next = tile_blk(0);
+        int bt_base = 0;
+        int bt_cur = bt_load(0), bt_nxt = bt_load(32);
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
-            const int page0 = j * (kKeys / kPage);
+            const int page0 = j * kPPT;
             int n_pages = ctx_pages - page0;
-            n_pages = n_pages > kKeys / kPage ? kKeys / kPage : n_pages;
-            int blk = blk_next;
-            blk_next = tile_blk(j + 1);
+            n_pages = n_pages > kPPT ? kPPT : n_pages;
+            if (page0 >= bt_base + 32) {
+                bt_base += 32;
+                bt_cur = bt_nxt;
+                bt_nxt = bt_load(bt_base + 32);
+            }
+            int blk = __shfl_sync(0xffffffffu, bt_cur, (page0 - bt_base + lane) & 31);
             int z = 0;
             if (lane < n_pages) {
                 if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {

@@ -69,6 +69,9 @@ def test_decode_plan_is_consistent(lib):
     # a window bounds the visible pages: 128 keys touch at most 9 pages per unit
     s, _ = fk.decode_plan(1, 8, 8, 64, 4096, 128, 1000)
     assert s <= 9 * 8
+    # ... and then the automatic plan gives every (seq, KV head) unit one warp
+    s, _ = fk.decode_plan(32, 64, 8, 64, 2048, 128)
+    assert s * 4 == 32 * 8
     # small work: at least 16 tiles per CTA
     s, _ = fk.decode_plan(1, 32, 8, 128, 64, 0)
     assert s <= (8 * 64 + 15) // 16

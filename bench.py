@@ -187,6 +187,16 @@ def step_bytes(w, kv_elem_bytes: int, per_token_scales: bool):
     return kv + q + out + bt, write
 
 
+def visible_kv_bytes(w, kv_elem_bytes: int, per_token_scales: bool):
+    """Key and value bytes (+ per-token-head scales) that one decode call over
+    `w` must read: the last `w.window` keys of each sequence when the layer has a
+    sliding window, else all of them."""
+    ctx = w.context_lens.to(torch.int64)
+    if getattr(w, "window", 0):
+        ctx = torch.clamp(ctx, max=int(w.window))
+    return int(ctx.sum()) * w.Hkv * (2 * w.D * kv_elem_bytes + (8 if per_token_scales else 0))
+
+
 def build_caches(w, kv_dtype, dev, rotations):
     import fp8_kv_cache_write_gb300 as fk
     dt = torch.uint8 if kv_dtype == fk.KV_E4M3 else torch.bfloat16
@@ -713,9 +723,20 @@ def _extra_hybrid(fk, synth, dev, stream, emit):
                 calls[layer % 2](i * 12 + layer // 2)
         ms = _time_graph(step, 8, stream)
         per_type = [_time_graph(calls[lt], 24, stream) * 1e3 for lt in (0, 1)]
+        kv_b = [visible_kv_bytes(wl[lt], 1 if dtypes[lt] == E4 else 2, dtypes[lt] == E4)
+                for lt in (0, 1)]
+        step_b = 12 * (kv_b[0] + kv_b[1])
+        hbm = measured_peaks()[0]
         line = {"extra": "hybrid_24_layers", "variant": variant, "B": 32,
                 "ms_per_step": ms, "tokens_per_s": 32 / (ms / 1e3),
-                "window_layer_us": per_type[0], "full_layer_us": per_type[1]}
+                "window_layer_us": per_type[0], "full_layer_us": per_type[1],
+                "algorithmic_bytes_per_step": step_b,
+                "step_gbs": step_b / (ms / 1e3) / 1e9,
+                "step_frac_of_hbm": step_b / (ms / 1e3) / 1e9 / hbm,
+                "full_layer_bytes": kv_b[1],
+                "full_layer_gbs": kv_b[1] / per_type[1] / 1e3,
+                "full_layer_frac_of_hbm": kv_b[1] / per_type[1] / 1e3 / hbm,
+                "window_layer_bytes": kv_b[0]}
         if variant == "window_bf16_full_fp8":
             # the oracle on one layer of each type, 12 of each per step
             cb = [_oracle_decode_baseline(wl[lt], dtypes[lt] if lt == 0 else 0,

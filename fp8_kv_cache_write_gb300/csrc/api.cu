@@ -433,11 +433,12 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     p.scale_mode = kv_dtype == FP8KV_KV_E4M3 ? scale_mode : FP8KV_SCALE_PER_TENSOR;
     p.flags = flags;
     p.err = err_flag;
+    // the kernels stream pages from these (and the fused step also stores into them)
+    p.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+    p.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
     if (fused) {
         p.k_new = static_cast<const __nv_bfloat16*>(k_new);
         p.v_new = static_cast<const __nv_bfloat16*>(v_new);
-        p.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
-        p.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
     }
     cudaError_t e = launch_paged_decode(p, kmap, vmap, D, kv_dtype, fused,
                                         static_cast<cudaStream_t>(cuda_stream));

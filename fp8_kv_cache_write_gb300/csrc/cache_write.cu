@@ -43,7 +43,7 @@ __device__ __forceinline__ float row_scale(const float (&f)[N], const WriteParam
 #pragma unroll
         for (int o = kLanes / 2; o > 0; o >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
-        return __fdiv_rn(amax, 448.0f);
+        return amax_over_448(amax);
     } else if constexpr (MODE == FP8KV_SCALE_PER_HEAD) {
         return (which ? p.v_scale : p.k_scale)[h];
     } else {
@@ -64,8 +64,8 @@ __device__ __forceinline__ void unpack8(uint4 x, float* f) {
 namespace staged {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
-constexpr int kStages = 3;
-constexpr int kTileBytes = 12288;                     // per tensor (K or V) per stage
+constexpr int kStages = 4;
+constexpr int kTileBytes = 8192;                      // per tensor (K or V) per stage
 constexpr int kSmemBytes = kStages * 2 * kTileBytes + 2 * kStages * 8;
 constexpr int kCtasPerSm = 3;
 // bulk writes only: below this many (token, head) rows the direct kernel runs
@@ -74,7 +74,7 @@ constexpr int64_t kMinRows = 8192;
 
 // CTA c takes chunks c, c + gridDim.x, ...; chunk i holds rows
 // [i * rows_per_chunk, min(rows, (i + 1) * rows_per_chunk)) of K and of V
-// (rows_per_chunk <= 12 KiB / (2 D)).  hkv_shift = log2(Hkv) when Hkv is a power
+// (rows_per_chunk <= 8 KiB / (2 D)).  hkv_shift = log2(Hkv) when Hkv is a power
 // of two, else -1.
 template <int D, int MODE, bool BF16>
 __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
                                  int hkv_shift) {
     using namespace staged;
     constexpr int kMaxRows = kTileBytes / (D * 2);
-    constexpr int kLanes = D / 16;                    // lanes per row, 16 values each
+    constexpr int kLanes = D / 32;                    // lanes per row, 32 values each
     constexpr int kRowsPerPass = 32 / kLanes;
     constexpr int kPasses = 2 * kMaxRows / (kRowsPerPass * kConsumerWarps);
     static_assert(kPasses * kRowsPerPass * kConsumerWarps == 2 * kMaxRows, "row split");
@@ -173,38 +173,44 @@ __global__ void __launch_bounds__(staged::kThreads, staged::kCtasPerSm)
             }
             const int h = hh[it];
             const int64_t row = (blk * p.Hkv + h) * kPage + off;
-            // the lane's values: [8l, 8l + 8) and [D/2 + 8l, D/2 + 8l + 8), so each
-            // 16-byte shared-memory read of a row is contiguous over its lanes
+            // the lane's values: [16l, 16l + 16) and [D/2 + 16l, D/2 + 16l + 16) (four
+            // 16-byte shared-memory reads); its codes are two 16-byte stores
             const uint8_t* src = tile + which * kTileBytes + rr * (D * 2);
-            const uint4 a = *reinterpret_cast<const uint4*>(src + l * 16);
-            const uint4 b = *reinterpret_cast<const uint4*>(src + D + l * 16);
+            const uint4 a0 = *reinterpret_cast<const uint4*>(src + l * 32);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(src + l * 32 + 16);
+            const uint4 b0 = *reinterpret_cast<const uint4*>(src + D + l * 32);
+            const uint4 b1 = *reinterpret_cast<const uint4*>(src + D + l * 32 + 16);
             if constexpr (BF16) {
                 uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache) +
                                row * (D * 2);
-                *reinterpret_cast<uint4*>(dst + l * 16) = a;
-                *reinterpret_cast<uint4*>(dst + D + l * 16) = b;
+                *reinterpret_cast<uint4*>(dst + l * 32) = a0;
+                *reinterpret_cast<uint4*>(dst + l * 32 + 16) = a1;
+                *reinterpret_cast<uint4*>(dst + D + l * 32) = b0;
+                *reinterpret_cast<uint4*>(dst + D + l * 32 + 16) = b1;
             } else {
-                float f[16];
-                unpack8(a, f);
-                unpack8(b, f + 8);
+                float f[32];
+                unpack8(a0, f);
+                unpack8(a1, f + 8);
+                unpack8(b0, f + 16);
+                unpack8(b1, f + 24);
                 const float s = row_scale<MODE, kLanes>(f, p, which, h, group_mask);
                 if constexpr (MODE == FP8KV_SCALE_PER_TOKEN_HEAD) {
                     if (l == 0) (which ? p.v_scale_cache : p.k_scale_cache)[row] = s;
                 }
-                uint32_t w[4] = {0u, 0u, 0u, 0u};   // a zero scale writes code 0
+                uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};   // a zero scale writes code 0
                 uint32_t redo = 0u;
                 if (s != 0.0f) redo = e4m3_codes_by_multiply(f, s, w);
                 uint8_t* dst = reinterpret_cast<uint8_t*>(which ? p.v_cache : p.k_cache) + row * D;
-                *reinterpret_cast<uint2*>(dst + l * 8) = make_uint2(w[0], w[1]);
-                *reinterpret_cast<uint2*>(dst + D / 2 + l * 8) = make_uint2(w[2], w[3]);
+                *reinterpret_cast<uint4*>(dst + l * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(dst + D / 2 + l * 16) = make_uint4(w[4], w[5], w[6], w[7]);
                 while (redo) {                       // rare: reread the pair, divide, restore
                     const int i = __ffs(redo) - 1;
                     redo &= redo - 1u;
-                    // byte offset of the pair's two codes from dst + 8 l
-                    const int e = i < 4 ? 2 * i : D / 2 + 2 * (i - 4);
+                    // the pair's two codes, from dst + 16 l, and its two bf16 values
+                    const int e = i < 8 ? 2 * i : D / 2 + 2 * (i - 8);
                     const uint32_t pr = *reinterpret_cast<const uint32_t*>(
-                        src + (i < 4 ? l * 16 + 4 * i : D + l * 16 + 4 * (i - 4)));
-                    *reinterpret_cast<uint16_t*>(dst + l * 8 + e) = e4m3x2_by_divide(
+                        src + (i < 8 ? l * 32 + 4 * i : D + l * 32 + 4 * (i - 8)));
+                    *reinterpret_cast<uint16_t*>(dst + l * 16 + e) = e4m3x2_by_divide(
                         bf16_bits_to_float(pr & 0xffffu), bf16_bits_to_float(pr >> 16), s);
                 }
             }

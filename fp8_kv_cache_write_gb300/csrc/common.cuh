@@ -143,6 +143,20 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
         : "memory");
 }
 
+// One lane's 16-byte asynchronous copy global -> shared (both 16-byte aligned),
+// with an L2 cache policy.  Completion is tracked per thread (cp_async_mbar_arrive).
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "l"(pol)
+                 : "memory");
+}
+
+// The barrier receives this thread's arrival once all of its earlier cp.async
+// copies have landed (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Fetch the 128-byte line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
@@ -214,7 +228,9 @@ __device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], 
     const float r_lo = __fmul_rn(r, 1.0f - 0x1p-19f);
     const float r_hi = __fmul_rn(r, 1.0f + 0x1p-19f);
     const uint64_t rl = pack_f32x2(r_lo, r_lo), rh = pack_f32x2(r_hi, r_hi);
-    uint32_t redo = 0u;
+    // the two bracketing products' codes differ somewhere iff diff != 0 (one
+    // three-input logic op per pair); which pairs, only in that rare case
+    uint32_t diff = 0u;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
         const uint64_t x2 = pack_f32x2(f[2 * i], f[2 * i + 1]);
@@ -224,9 +240,33 @@ __device__ __forceinline__ uint32_t e4m3_codes_by_multiply(const float (&f)[N], 
             w[i >> 1] |= lo << 16;
         else
             w[i >> 1] = lo;
+        diff |= lo ^ hi;
+    }
+    if (!fast) return N >= 64 ? ~0u : (1u << (N / 2)) - 1u;
+    if (diff == 0u) return 0u;
+    uint32_t redo = 0u;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const uint32_t lo = (w[i >> 1] >> (16 * (i & 1))) & 0xffffu;
+        const uint32_t hi = e4m3x2_from_f32x2(mul_f32x2(pack_f32x2(f[2 * i], f[2 * i + 1]), rh));
         redo |= static_cast<uint32_t>(lo != hi) << i;
     }
-    return fast ? redo : (N >= 64 ? ~0u : (1u << (N / 2)) - 1u);
+    return redo;
+}
+
+// fp32(a / 448) -- the per-token-head scale of a row whose max |x| is a -- for
+// a = 0, +inf or any finite non-negative bf16 value (a row maximum of bf16
+// inputs always is one).  Division by a constant through its correctly rounded
+// reciprocal y and one remainder correction (Markstein's method: q0 = a y,
+// r = a - 448 q0 exactly by a fused multiply-add, q = q0 + r y), which rounds
+// exactly like the IEEE quotient for every such a (checked exhaustively over
+// all finite bf16 values; the writer's tests compare the scales bit for bit).
+__device__ __forceinline__ float amax_over_448(float a) {
+    constexpr float y = 0x1.24924ap-9f;             // fp32(1 / 448)
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, 448.0f, a);
+    const float q = __fmaf_rn(r, y, q0);
+    return a == __int_as_float(0x7f800000) ? a : q;
 }
 
 // Phase 2 for one pair: codes of fp32(x0 / s), fp32(x1 / s) by IEEE divides.

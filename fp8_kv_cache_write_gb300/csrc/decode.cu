@@ -59,6 +59,10 @@ struct Cfg {
     // two independent pages between waits
     static constexpr int kPPI = kRowB <= 128 ? 2 : 1;
     static constexpr int kStageB = 2 * kPPI * kTileB; // K tiles, then V tiles
+    // how a stage is filled: 64-byte rows (1 KiB tiles) by 16-byte copies from
+    // every lane (many small requests in flight stream short tiles faster),
+    // other rows by one lane's tensor copies
+    static constexpr bool kLaneCopies = kRowB == 64;
     // bytes in flight per warp: 16 KiB, 12 KiB for 64-byte rows (4 CTAs per SM)
     static constexpr int kStagesRaw = (kRowB == 64 ? 12288 : 16384) / kStageB;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
@@ -331,10 +335,14 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
     //      tiles; every warp is an independent worker (no block-wide barrier)
     if (lane == 0) {                      // ring barriers (their fences overlap the loads below)
-        for (int s = 0; s < C::kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        // lane copies: every lane arrives once per stage; TMA: lane 0 only
+        for (int s = 0; s < C::kStages; ++s)
+            mbar_init(smem_addr(&bars[s]), C::kLaneCopies ? 32 : 1);
         mbar_init_fence();
-        prefetch_tmap(&kmap);
-        prefetch_tmap(&vmap);
+        if constexpr (!C::kLaneCopies) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
     }
     if (!early_setup) pdl_wait();         // the preceding kernel's writes are visible
     // the page table's lines reach L2 while the context lengths are read (the
@@ -723,29 +731,63 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 }
                 if (here[k]) tx += 2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0);
             }
-            if (lane == 0) {
+            if constexpr (C::kLaneCopies) {
+                // every lane copies 16-byte pieces lane, lane + 32, ... of each tile
+                // (the whole warp keeps many small requests in flight, which streams
+                // short tiles faster than one bulk request per tile) into the
+                // 128-byte-swizzled layout the math reads; the stage's barrier
+                // completes when every lane's copies have landed
                 const uint32_t bar = smem_addr(&bars[st]);
                 const uint32_t base = smem_addr(ring + st * C::kStageB);
                 const uint64_t pol = l2_evict_first();   // pages are read once
-                fence_proxy_async();
-                mbar_arrive_expect_tx(bar, tx);
 #pragma unroll
                 for (int k = 0; k < PPI; ++k) {
                     if (!here[k]) continue;
-                    const int z = blk[k] * p.Hkv + h_i;
+                    const size_t z = static_cast<size_t>(blk[k]) * p.Hkv + h_i;
+                    const uint8_t* ksrc = p.k_cache + z * C::kTileB + lane * 16;
+                    const uint8_t* vsrc = p.v_cache + z * C::kTileB + lane * 16;
 #pragma unroll
-                    for (int box = 0; box < C::kBoxes; ++box) {
-                        tma_load_3d_hint(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0,
-                                         z, bar, pol);
-                        tma_load_3d_hint(base + (PPI + k) * C::kTileB + box * 2048, &vmap,
-                                         box * 128, 0, z, bar, pol);
+                    for (int i = 0; i < C::kTileB / 512; ++i) {
+                        const int o = lane * 16 + i * 512;
+                        const uint32_t soff = chunk_off<C::kRowB>(o / C::kRowB, (o % C::kRowB) >> 4);
+                        cp_async16_hint(base + k * C::kTileB + soff, ksrc + i * 512, pol);
+                        cp_async16_hint(base + (PPI + k) * C::kTileB + soff, vsrc + i * 512, pol);
                     }
                     if constexpr (PER_TOKEN) {
-                        const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
-                        bulk_load_hint(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64,
-                                       bar, pol);
-                        bulk_load_hint(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage,
-                                       64, bar, pol);
+                        if (lane < 8) {          // 64 bytes of k scales, then 64 of v scales
+                            const float* src = (lane < 4 ? p.k_scale_cache : p.v_scale_cache) +
+                                               z * kPage + (lane & 3) * 4;
+                            cp_async16_hint(smem_addr(scl + (st * PPI + k) * C::kScaleB) + lane * 16,
+                                            src, pol);
+                        }
+                    }
+                }
+                cp_async_mbar_arrive(bar);
+            } else {
+                if (lane == 0) {
+                    const uint32_t bar = smem_addr(&bars[st]);
+                    const uint32_t base = smem_addr(ring + st * C::kStageB);
+                    const uint64_t pol = l2_evict_first();   // pages are read once
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+                    for (int k = 0; k < PPI; ++k) {
+                        if (!here[k]) continue;
+                        const int z = blk[k] * p.Hkv + h_i;
+#pragma unroll
+                        for (int box = 0; box < C::kBoxes; ++box) {
+                            tma_load_3d_hint(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0,
+                                             z, bar, pol);
+                            tma_load_3d_hint(base + (PPI + k) * C::kTileB + box * 2048, &vmap,
+                                             box * 128, 0, z, bar, pol);
+                        }
+                        if constexpr (PER_TOKEN) {
+                            const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
+                            bulk_load_hint(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                                           bar, pol);
+                            bulk_load_hint(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage,
+                                           64, bar, pol);
+                        }
                     }
                 }
             }

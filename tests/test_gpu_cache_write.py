@@ -240,3 +240,54 @@ def test_bulk_write_from_pinned_host_memory():
         assert np.array_equal(got[0], okc) and np.array_equal(got[1], ovc)
         assert np.array_equal(got[2].view(np.uint32), oks.view(np.uint32))
         assert np.array_equal(got[3].view(np.uint32), ovs.view(np.uint32))
+
+
+@pytest.mark.parametrize("path", ["staged", "direct"])
+@pytest.mark.parametrize("D", [64, 256])
+def test_scale_of_every_bf16_row_maximum(path, D):
+    # Per-token-head scales: every finite non-negative bf16 value (0, subnormals,
+    # up to the largest) is the max |x| of some K row, plus one row whose maximum
+    # is +inf and rows holding NaN (which the maximum ignores).  Stored scales
+    # must be fp32(amax / 448) bit for bit and the codes the oracle's, through
+    # the staged kernel (one bulk call) and the plain-load kernel (calls of
+    # fewer than 8192 rows).
+    amax = (np.arange(0x7f80, dtype=np.uint32) << 16).view(np.float32)
+    rng = np.random.default_rng(D)
+    n = amax.size
+    x = amax[:, None].astype(np.float64) * rng.uniform(-1.0, 1.0, (n, D))
+    col = rng.integers(0, D, n)
+    x[np.arange(n), col] = amax * np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    extra = rng.standard_normal((3, D))
+    extra[0, 7] = np.inf                         # infinite maximum: scale +inf
+    extra[1, 9] = np.nan                         # NaN ignored by the maximum
+    extra[2, ::5] = np.nan
+    x = np.concatenate([x, extra])
+    T = x.shape[0]
+    k = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).reshape(T, 1, D)
+    v = k.flip(0).contiguous()
+    nb = (T + 15) // 16
+    slots = torch.randperm(nb * 16, generator=torch.Generator().manual_seed(D))[:T].to(torch.int64)
+    kc = torch.zeros((nb, 1, 16, D), dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    ks = torch.zeros((nb, 1, 16), device="cuda")
+    vs = ks.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    step = T if path == "staged" else 8000
+    for a in range(0, T, step):
+        fk.kv_cache_write(k[a:a + step].cuda(), v[a:a + step].cuda(), slots[a:a + step].cuda(),
+                          kc, vc, kv_dtype=0, scale_mode=2, k_scale_cache=ks, v_scale_cache=vs,
+                          err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    okc = np.zeros((nb, 1, 16, D), np.uint8)
+    ovc = okc.copy()
+    oks = np.zeros((nb, 1, 16), np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_cache_write(bits16(k), bits16(v), slots.numpy(), okc, ovc, kv_dtype=0,
+                                 scale_mode=2, k_scale_cache=oks, v_scale_cache=ovs) == 0
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+    for got, want in ((kc.cpu().numpy(), okc), (vc.cpu().numpy(), ovc)):
+        nan = (want & 0x7F) == 0x7F              # NaN codes: the sign is not compared
+        assert np.array_equal(got[~nan], want[~nan])
+        assert np.all((got[nan] & 0x7F) == 0x7F)

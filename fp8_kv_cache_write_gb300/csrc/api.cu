@@ -117,10 +117,13 @@ struct MapKey {
     int row_bytes;
     int64_t nbh;
     bool sw64;
+    int depth;
 };
 
+// depth: (block, head) tiles per box, adjacent heads of one block (decode units
+// of packed heads take 2)
 bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
-                 bool sw64 = false) {
+                 bool sw64 = false, int depth = 1) {
     sw64 = sw64 && row_bytes == 64;
     struct Entry {
         MapKey key;
@@ -131,7 +134,7 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
     thread_local int next = 0;
     for (auto& e : cache)
         if (e.used && e.key.base == base && e.key.row_bytes == row_bytes && e.key.nbh == nbh &&
-            e.key.sw64 == sw64) {
+            e.key.sw64 == sw64 && e.key.depth == depth) {
             *out = e.map;
             return true;
         }
@@ -148,13 +151,13 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
     } else if (row_bytes == 64) {
         dims[0] = 128; dims[1] = 8; dims[2] = static_cast<cuuint64_t>(nbh);
         strides[0] = 128; strides[1] = 1024;
-        box[0] = 128; box[1] = 8; box[2] = 1;
+        box[0] = 128; box[1] = 8; box[2] = static_cast<cuuint32_t>(depth);
     } else {
         dims[0] = static_cast<cuuint64_t>(row_bytes); dims[1] = 16;
         dims[2] = static_cast<cuuint64_t>(nbh);
         strides[0] = static_cast<cuuint64_t>(row_bytes);
         strides[1] = static_cast<cuuint64_t>(row_bytes) * 16;
-        box[0] = 128; box[1] = 16; box[2] = 1;
+        box[0] = 128; box[1] = 16; box[2] = static_cast<cuuint32_t>(depth);
     }
     CUtensorMap m;
     CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
@@ -162,7 +165,7 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
                     sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
-    cache[next] = Entry{MapKey{base, row_bytes, nbh, sw64}, m, true};
+    cache[next] = Entry{MapKey{base, row_bytes, nbh, sw64, depth}, m, true};
     next = (next + 1) % 8;
     *out = m;
     return true;
@@ -179,7 +182,8 @@ struct Plan {
 // an explicit count n asks for about n partitions per (seq, KV head) unit;
 // max_ctas > 0 caps the CTA count.
 // Workspace: one (m, l, O) slot per (warp, unit) pair a warp can touch, i.e.
-// 4 * num_splits + B * Hkv slots of G query heads.
+// 4 * num_splits + B * Hkv / hpt slots of G * hpt query heads, for the heads per
+// unit hpt of the e4m3 cache (at least the bf16 cache's, so the size covers both).
 int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Plan* out,
          int64_t max_ctas = 0) {
     int maxvis = max_blocks;
@@ -190,26 +194,26 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     if (maxvis < 1) maxvis = 1;
     const int64_t units = static_cast<int64_t>(B) * Hkv;
     const int64_t work = units * maxvis;
+    const int G1 = Hkv > 0 ? Hq / Hkv : 1;
+    const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, G1, Hkv);
     int64_t n;
     if (req > 0) {
         n = static_cast<int64_t>(req) * units;
     } else {
-        n = static_cast<int64_t>(sm_count()) *
-            decode_ctas_per_sm(D, 0, Hkv > 0 ? Hq / Hkv : 1);
+        n = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0, G1, Hkv);
         const int64_t by_work = (work + 15) / 16;
         if (by_work < n) n = by_work;
         // units of at most 16 visible pages (a sliding window): one worker warp
         // per unit, so that every unit ends in its own warp (no partials to merge)
-        if (maxvis <= 16) n = (units + kDecodeWarps - 1) / kDecodeWarps;
+        if (maxvis <= 16) n = (units / hpt + kDecodeWarps - 1) / kDecodeWarps;
     }
     if (n > work) n = work;
     if (n > 1024) n = 1024;
     if (max_ctas > 0 && n > max_ctas) n = max_ctas;
     if (n < 1) n = 1;
     out->num_splits = static_cast<int>(n);
-    const int64_t G = Hkv > 0 ? Hq / Hkv : 1;
     const int64_t workers = n * kDecodeWarps;      // every warp is a worker
-    out->workspace_bytes = static_cast<size_t>(workers + units) * G *
+    out->workspace_bytes = static_cast<size_t>(workers + units / hpt) * G1 * hpt *
                            (static_cast<size_t>(D) + 2) * sizeof(float);
     return FP8KV_OK;
 }
@@ -399,8 +403,10 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
     const int64_t nbh = num_blocks * Hkv;
+    const int hpt = decode_heads_per_unit(D, kv_dtype, Hq / Hkv, Hkv);
     CUtensorMap kmap, vmap;
-    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap) || !make_kv_map(v_cache, row_bytes, nbh, &vmap))
+    if (!make_kv_map(k_cache, row_bytes, nbh, &kmap, false, hpt) ||
+        !make_kv_map(v_cache, row_bytes, nbh, &vmap, false, hpt))
         return FP8KV_ERR_CUDA;
 
     DecodeParams p{};
@@ -416,6 +422,9 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
+    p.hpt = hpt;
+    p.Hu = Hkv / hpt;
+    p.Gu = p.G * hpt;
     p.num_blocks = num_blocks;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.window = window;
@@ -423,7 +432,7 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     {
         float* ws = static_cast<float*>(workspace);
         const size_t rows = (static_cast<size_t>(pl.num_splits) * kDecodeWarps +
-                             static_cast<size_t>(B) * Hkv) * (Hq / Hkv);
+                             static_cast<size_t>(B) * p.Hu) * p.Gu;
         p.ws_o = ws;
         p.ws_m = ws + rows * D;
         p.ws_l = p.ws_m + rows;
@@ -461,10 +470,12 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
     int64_t max_ctas = 0;
     if (num_splits == 0 && Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 && valid_d(D)) {
         // slots that fit, less the one per unit, over the 4 worker warps of a CTA
+        // (a worker's slot holds hpt KV heads' query heads, as the planner sizes it)
+        const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, Hq / Hkv, Hkv);
         const int64_t slot_bytes = static_cast<int64_t>(Hq / Hkv) * (D + 2) * sizeof(float);
         const int64_t spare = static_cast<int64_t>(scratch_bytes) / slot_bytes -
                               static_cast<int64_t>(B) * Hkv;
-        max_ctas = spare / kDecodeWarps;
+        max_ctas = spare / (static_cast<int64_t>(kDecodeWarps) * hpt);
         if (max_ctas < 1) return FP8KV_ERR_WORKSPACE;
     }
     return paged_decode(q, nullptr, nullptr, k_cache, v_cache, kv_dtype, scale_mode, k_scale,

@@ -11,17 +11,23 @@
 //
 // Design (GB300):
 //   * one wave of CTAs of 4 warps; every warp is an independent worker: the
-//     (seq, KV head, page) tiles of the whole launch are flattened and each warp
-//     takes an equal consecutive share, crossing (seq, KV head) units where its
-//     share does, so any mix of context lengths keeps all SMs equally busy.
-//     Each warp runs its own TMA ring that streams straight across unit
+//     (seq, unit, page) tiles of the whole launch are flattened and each warp
+//     takes an equal consecutive share, crossing units where its share does, so
+//     any mix of context lengths keeps all SMs equally busy.  A unit is one KV
+//     head, or -- with G = 2 or 4 query heads per KV head, an even KV head count
+//     and tiles of at most 2 KiB -- two adjacent KV heads, whose query heads
+//     share the 8 MMA columns and whose page tiles are adjacent in the cache
+//     (one copy request and one softmax serve both).
+//     Each warp runs its own ring that streams straight across unit
 //     boundaries: lane 0 issues 3-D tiled tensor copies (128-byte swizzle) of the
 //     K and V page tiles -- plus the 64-byte per-token scale rows -- onto an
-//     mbarrier, S stages ahead; two pages per iteration.
+//     mbarrier, S stages ahead (1 KiB tiles: 16-byte copies from every lane);
+//     two tiles per iteration.
 //   * math on the legacy tensor pipe (mma.sync m16n8k16, fp32 accumulate):
-//     S^T = K_page . Q^T with M = 16 page tokens, N = 8 query heads of the GQA
-//     group, K = D; then O^T += V_page^T . P^T with M = D, N = heads, K = the 16
-//     tokens.  e4m3 codes convert exactly to f16 (one cvt per pair), Q is
+//     S^T = K_page . Q^T with M = 16 page tokens, N = 8 query heads of the
+//     unit, K = D; then O^T += V_page^T . P^T with M = D, N = heads, K = the 16
+//     tokens (for a unit of two KV heads, each head's P^T keeps only its own
+//     columns).  e4m3 codes convert exactly to f16 (one cvt per pair), Q is
 //     scaled by a per-head power of two into f16's top binade (exact), and P is
 //     split into hi + lo halves so the PV product keeps ~22 bits.
 //   * per-token-head scales fold out of the dot products: one multiply per
@@ -50,15 +56,21 @@ constexpr int kWarps = kDecodeWarps;
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 constexpr float kMaxInit = -1.0e30f;   // running-max start: finite, below any real logit
 
-template <int D, bool BF16, int NT = 1>
+template <int D, bool BF16, int NT = 1, int HPT = 1>
 struct Cfg {
     static constexpr int kElem = BF16 ? 2 : 1;
     static constexpr int kRowB = D * kElem;           // bytes of one token row
     static constexpr int kTileB = kPage * kRowB;      // bytes of one (page, head) tile
-    // pages per iteration: two when a page tile is small, so each warp works on
-    // two independent pages between waits
-    static constexpr int kPPI = kRowB <= 128 ? 2 : 1;
-    static constexpr int kStageB = 2 * kPPI * kTileB; // K tiles, then V tiles
+    // HPT = 2 packs two adjacent KV heads (of at most 4 query heads each) into
+    // the 8 MMA columns: their tiles of a page are adjacent in the cache, so one
+    // copy request moves both, and one softmax serves both.  Tiles of at most
+    // 2 KiB only (shared memory).
+    static_assert(HPT == 1 || (HPT == 2 && kRowB <= 128 && NT == 1), "head packing");
+    // pages per iteration: two when a page tile is small and heads are not
+    // packed, so each warp works on two independent tiles between waits
+    static constexpr int kPPI = HPT > 1 ? 1 : (kRowB <= 128 ? 2 : 1);
+    static constexpr int kTiles = kPPI * HPT;         // (page, head) tiles per tensor per stage
+    static constexpr int kStageB = 2 * kTiles * kTileB; // K tiles, then V tiles
     // how a stage is filled: 64-byte rows (1 KiB tiles) by 16-byte copies from
     // every lane (many small requests in flight stream short tiles faster),
     // other rows by one lane's tensor copies
@@ -74,10 +86,10 @@ struct Cfg {
     static constexpr int kVWords = kVBytes / 4;
     static constexpr int kBoxes = kRowB >= 128 ? kRowB / 128 : 1;
     static constexpr int kWarpSmem = kStages * kStageB;
-    static constexpr int kScaleB = 128;               // k scales + v scales of one page
+    static constexpr int kScaleB = 128;               // k + v scales of one (page, head) tile
     static constexpr int kMaxSeg = 16;                // segments a warp lists per pass
-    static constexpr int kSegInts = 9;                // ints of one segment record
-    static constexpr int kOffBars = kWarps * kWarpSmem + kWarps * kStages * kPPI * kScaleB;
+    static constexpr int kSegInts = 7;                // ints of one segment record
+    static constexpr int kOffBars = kWarps * kWarpSmem + kWarps * kStages * kTiles * kScaleB;
     static constexpr int kOffSegs = kOffBars + kWarps * kStages * 8;
     static constexpr int kOffShare = kOffSegs + kWarps * kMaxSeg * kSegInts * 4;  // [warp][resume, end]
     static constexpr int kOffCtx = kOffShare + kWarps * 16;    // [warp][32] context lengths
@@ -90,7 +102,7 @@ struct Cfg {
     // (as stored in the cache) and its two per-token-head scales
     static constexpr int kOffNew = kOffQsm + kQsmBytes;
     static constexpr int kNewB = (2 * kRowB + 8 + 15) / 16 * 16;
-    static constexpr int kSmemFused = kSmem + kWarps * kNewB;
+    static constexpr int kSmemFused = kSmem + kWarps * HPT * kNewB;
     static_assert(kSegs * kKPerSeg == kKSteps, "k-step split");
 };
 
@@ -296,13 +308,16 @@ constexpr int decode_min_ctas() {
 
 // FUSED: a decode step -- the kernel also stores every sequence's new token
 // (k_new / v_new at position ctx - 1).  NT: 8-head groups per KV head (1 for
-// G <= 8, 2 for G <= 16); the groups share every K and V conversion.
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
+// G <= 8, 2 for G <= 16); the groups share every K and V conversion.  HPT: KV
+// heads per unit (2: adjacent heads h, h + 1 share the 8 columns, G <= 4 each).
+// A unit is (sequence, group of HPT KV heads) with Gu = G * HPT query heads.
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT>
 __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-    using C = Cfg<D, BF16, NT>;
+    using C = Cfg<D, BF16, NT, HPT>;
     constexpr int PPI = C::kPPI;
+    constexpr int TT = C::kTiles;
     constexpr int kMaxSeg = C::kMaxSeg;
     constexpr int kSegInts = C::kSegInts;
     extern __shared__ uint8_t smem_raw[];
@@ -311,7 +326,15 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int G = p.G;
+    const int G = p.G;                      // query heads per KV head
+    const int Gu = p.Gu;                    // query heads (columns) per unit
+    // the KV head (within the unit) of this lane's accumulator columns 2c, 2c + 1
+    // (the same head for both: G is even when heads are packed)
+    const int hl_lane = HPT > 1 ? ((2 * c) / G < HPT ? (2 * c) / G : HPT - 1) : 0;
+    // PV B-operand masks: column g belongs to KV head g / G of the unit
+    uint32_t bmask[HPT];
+#pragma unroll
+    for (int hl = 0; hl < HPT; ++hl) bmask[hl] = g / G == hl ? ~0u : 0u;
     pdl_trigger();                        // split_merge may launch while this runs
     // Ordering against the preceding kernel of the stream (programmatic launch):
     // by default the kernel waits for it before reading any global memory.  With
@@ -325,12 +348,12 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     const bool early_pages = (p.flags & FP8KV_DECODE_EARLY_PAGES) != 0;
 
     uint8_t* ring = smem + warp * C::kWarpSmem;
-    uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * PPI * C::kScaleB;
+    uint8_t* scl = smem + kWarps * C::kWarpSmem + warp * C::kStages * TT * C::kScaleB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars) + warp * C::kStages;
     int* seg = reinterpret_cast<int*>(smem + C::kOffSegs) + warp * kMaxSeg * kSegInts;
-    // segment record i: seg[9i + 0..8] = sequence b, KV head h, first page, end
-    // page, flags (2: starts the unit, 4: ends it), visible positions [lo, ctx),
-    // and the bits of the per-tensor / per-head K and V scales (1 otherwise)
+    // segment record i: seg[7i + 0..6] = sequence b, unit head group h (KV heads
+    // h HPT .. h HPT + HPT - 1), first page, end page, flags (2: starts the unit,
+    // 4: ends it), visible positions [lo, ctx)
 
     // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
     //      tiles; every warp is an independent worker (no block-wide barrier)
@@ -366,7 +389,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
             if (b0 == 0) ctx32[lane] = craw;
             int lo_, ctx_, plo_, phi_;
             visible_of(p, craw, lo_, ctx_, plo_, phi_, blockIdx.x == 0 && warp == 0);
-            w = phi_ > plo_ ? static_cast<long long>(phi_ - plo_) * p.Hkv : 0;
+            w = phi_ > plo_ ? static_cast<long long>(phi_ - plo_) * p.Hu : 0;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
@@ -406,7 +429,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 visible_of(p, b0 == 0 ? ctx32[lane] : p.context_lens[bb], lo_, ctx_, plo_, phi_,
                            false);
             const int n = phi_ > plo_ ? phi_ - plo_ : 0;
-            const long long w = static_cast<long long>(n) * p.Hkv;
+            const long long w = static_cast<long long>(n) * p.Hu;
             long long incl = w;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -424,7 +447,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 const int slo = __shfl_sync(0xffffffffu, lo_, src);
                 const int sctx = __shfl_sync(0xffffffffu, ctx_, src);
                 const int splo = __shfl_sync(0xffffffffu, plo_, src);
-                while (t < t1 && t < sb + static_cast<long long>(sn) * p.Hkv && k < kMaxSeg) {
+                while (t < t1 && t < sb + static_cast<long long>(sn) * p.Hu && k < kMaxSeg) {
                     // t - sb < pages * Hkv < 2^31 (checked on the host)
                     const int hq = static_cast<int>(t - sb) / sn;
                     const long long unit_base = sb + static_cast<long long>(hq) * sn;
@@ -438,14 +461,6 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                         r[4] = (t == unit_base ? 2 : 0) | (seg_end == unit_base + sn ? 4 : 0);
                         r[5] = slo;
                         r[6] = sctx;
-                        float ks = 1.f, vs = 1.f;
-                        if constexpr (!BF16 && !PER_TOKEN) {
-                            const int si = p.scale_mode == FP8KV_SCALE_PER_HEAD ? hq : 0;
-                            ks = p.k_scale[si];
-                            vs = p.v_scale[si];
-                        }
-                        r[7] = __float_as_int(ks);
-                        r[8] = __float_as_int(vs);
                     }
                     t = seg_end;
                     ++k;
@@ -463,12 +478,21 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     uint32_t qb[NT == 1 ? C::kKSteps : 1][2];
     uint2* qsm = reinterpret_cast<uint2*>(smem + C::kOffQsm) + warp * NT * C::kKSteps * 32;
     float hs[NT][2];                        // log2-domain logit multipliers, heads 2c, 2c+1
-    auto load_q = [&](int b, int h, float kconst) {
+    // the per-tensor or per-head scale of KV head hk (1 for the bf16 cache and for
+    // per-token-head scales, which apply per token)
+    auto const_scale = [&](const float* arr, int hk) -> float {
+        if constexpr (!BF16 && !PER_TOKEN)
+            return arr[p.scale_mode == FP8KV_SCALE_PER_HEAD ? hk : 0];
+        else
+            return 1.f;
+    };
+    auto load_q = [&](int b, int h) {
     if constexpr (NT > 1) __syncwarp();     // the previous segment's fragments are read
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-    const int hl = nt * 8 + g;              // head within the group
-    const int hq_g = h * G + hl;
+    const int hl = nt * 8 + g;              // column (query head) within the unit
+    const int hq_g = h * Gu + hl;
+    const float kconst = hl < Gu ? const_scale(p.k_scale, h * HPT + hl / G) : 1.f;
     float qscale = 0.f;                     // log2-domain logit multiplier of head hl
     {
         const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(b) * p.Hq + hq_g) * D;
@@ -477,7 +501,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
         for (int ks = 0; ks < C::kKSteps; ++ks) {
             const int s = ks / C::kKPerSeg, jj = ks % C::kKPerSeg;
             const int d0 = s * (64 / C::kElem) + c * (16 / C::kElem) + 4 * jj;
-            raw[ks] = hl < G ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
+            raw[ks] = hl < Gu ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
         }
         uint2 frag[C::kKSteps];
         if constexpr (BF16) {
@@ -592,13 +616,15 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
         const int ub = seg[kSegInts * si + 0], uh = seg[kSegInts * si + 1];
         const int flags = seg[kSegInts * si + 4];
         const bool whole = flags == 6;           // starts and ends the unit
-        const float vconst = __int_as_float(seg[kSegInts * si + 8]) / kWScale;
         const int dbase = perm8(g) * (D / 8);
-        const size_t unit = static_cast<size_t>(ub) * p.Hkv + uh;
+        const size_t unit = static_cast<size_t>(ub) * p.Hu + uh;
         const size_t slot = static_cast<size_t>(FP8KV_WORKER) + unit;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int head0 = nt * 8 + 2 * c, head1 = head0 + 1;
+            const int head0 = nt * 8 + 2 * c, head1 = head0 + 1;   // columns of the unit
+            // V scale of their KV head (both columns belong to the same one)
+            const float vconst =
+                (head0 < Gu ? const_scale(p.v_scale, uh * HPT + head0 / G) : 1.f) / kWScale;
             const float l0 = lst[nt][0], l1 = lst[nt][1];
             const float f0 = whole ? (l0 > 0.f ? vconst / l0 : 0.f) : vconst;
             const float f1 = whole ? (l1 > 0.f ? vconst / l1 : 0.f) : vconst;
@@ -608,27 +634,27 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int head = hh ? head1 : head0;
-                    if (head >= G) continue;
+                    if (head >= Gu) continue;
                     const float f = hh ? f1 : f0;
                     const float va = o[nt][i][hh] * f, vb = o[nt][i][2 + hh] * f;
                     if (whole) {
-                        const size_t row = static_cast<size_t>(ub) * p.Hq + uh * G + head;
+                        const size_t row = static_cast<size_t>(ub) * p.Hq + uh * Gu + head;
                         store_out<BF16>(p.out, p.out_bf16, row * D + d, va);
                         store_out<BF16>(p.out, p.out_bf16, row * D + d + 1, vb);
                     } else {
-                        float* dst = p.ws_o + (slot * G + head) * D + d;
+                        float* dst = p.ws_o + (slot * Gu + head) * D + d;
                         *reinterpret_cast<float2*>(dst) = make_float2(va, vb);
                     }
                 }
             }
             if (!whole && g == 0) {
-                if (head0 < G) {
-                    p.ws_m[slot * G + head0] = mst[nt][0];
-                    p.ws_l[slot * G + head0] = l0;
+                if (head0 < Gu) {
+                    p.ws_m[slot * Gu + head0] = mst[nt][0];
+                    p.ws_l[slot * Gu + head0] = l0;
                 }
-                if (head1 < G) {
-                    p.ws_m[slot * G + head1] = mst[nt][1];
-                    p.ws_l[slot * G + head1] = l1;
+                if (head1 < Gu) {
+                    p.ws_m[slot * Gu + head1] = mst[nt][1];
+                    p.ws_l[slot * Gu + head1] = l1;
                 }
             }
         }
@@ -641,25 +667,33 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     //      before the store.
     constexpr int kLB = C::kRowB / 32;                // stored bytes per lane
     using LaneT = typename LaneBytes<kLB>::T;
-    uint8_t* newtok = smem + C::kOffNew + warp * C::kNewB;
-    auto store_new_token = [&](int b, int h, int ctx, float ksc, float vsc) -> bool {
+    // one area per KV head of the unit
+    uint8_t* newtok = smem + C::kOffNew + warp * HPT * C::kNewB;
+    auto store_new_token = [&](int b, int hk, int hl, int ctx) -> bool {
         return store_new_token_row<D, BF16, PER_TOKEN>(
             p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq, p.num_blocks, p.Hkv,
             p.k_new, p.v_new, p.k_cache, p.v_cache, const_cast<float*>(p.k_scale_cache),
-            const_cast<float*>(p.v_scale_cache), p.err, newtok, lane, b, h, ctx, ksc, vsc);
+            const_cast<float*>(p.v_scale_cache), p.err, newtok + hl * C::kNewB, lane, b, hk, ctx,
+            const_scale(p.k_scale, hk), const_scale(p.v_scale, hk));
     };
-    // overwrite token row r of page k of stage st with the stored new token
+    // overwrite token row r of page k of stage st (every KV head of the unit)
+    // with the stored new tokens
     auto patch_new_token = [&](uint8_t* stage, int st, int k, int r) {
         const int off = chunk_off<C::kRowB>(r, (lane * kLB) >> 4) + ((lane * kLB) & 15);
-        *reinterpret_cast<LaneT*>(stage + k * C::kTileB + off) =
-            *reinterpret_cast<const LaneT*>(newtok + lane * kLB);
-        *reinterpret_cast<LaneT*>(stage + (PPI + k) * C::kTileB + off) =
-            *reinterpret_cast<const LaneT*>(newtok + C::kRowB + lane * kLB);
-        if constexpr (PER_TOKEN) {
-            if (lane == 0) {
-                float* sk = reinterpret_cast<float*>(scl + (st * PPI + k) * C::kScaleB);
-                sk[r] = reinterpret_cast<const float*>(newtok + 2 * C::kRowB)[0];
-                sk[16 + r] = reinterpret_cast<const float*>(newtok + 2 * C::kRowB)[1];
+#pragma unroll
+        for (int hl = 0; hl < HPT; ++hl) {
+            const uint8_t* area = newtok + hl * C::kNewB;
+            const int tt = k * HPT + hl;
+            *reinterpret_cast<LaneT*>(stage + tt * C::kTileB + off) =
+                *reinterpret_cast<const LaneT*>(area + lane * kLB);
+            *reinterpret_cast<LaneT*>(stage + (TT + tt) * C::kTileB + off) =
+                *reinterpret_cast<const LaneT*>(area + C::kRowB + lane * kLB);
+            if constexpr (PER_TOKEN) {
+                if (lane == 0) {
+                    float* sc = reinterpret_cast<float*>(scl + (st * PPI + k) * HPT * C::kScaleB);
+                    sc[hl * 16 + r] = reinterpret_cast<const float*>(area + 2 * C::kRowB)[0];
+                    sc[(HPT + hl) * 16 + r] = reinterpret_cast<const float*>(area + 2 * C::kRowB)[1];
+                }
             }
         }
         // the slot is refilled by TMA later: order these generic writes first
@@ -729,7 +763,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                     if (lane == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
                     blk[k] = 0;              // load an in-range page, masked later
                 }
-                if (here[k]) tx += 2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0);
+                if (here[k]) tx += HPT * (2 * C::kTileB + (PER_TOKEN ? C::kScaleB : 0));
             }
             if constexpr (C::kLaneCopies) {
                 // every lane copies 16-byte pieces lane, lane + 32, ... of each tile
@@ -743,21 +777,26 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 #pragma unroll
                 for (int k = 0; k < PPI; ++k) {
                     if (!here[k]) continue;
-                    const size_t z = static_cast<size_t>(blk[k]) * p.Hkv + h_i;
+                    // the unit's HPT tiles of the page are adjacent in the cache
+                    const size_t z = static_cast<size_t>(blk[k]) * p.Hkv + h_i * HPT;
                     const uint8_t* ksrc = p.k_cache + z * C::kTileB + lane * 16;
                     const uint8_t* vsrc = p.v_cache + z * C::kTileB + lane * 16;
 #pragma unroll
-                    for (int i = 0; i < C::kTileB / 512; ++i) {
+                    for (int i = 0; i < HPT * C::kTileB / 512; ++i) {
                         const int o = lane * 16 + i * 512;
-                        const uint32_t soff = chunk_off<C::kRowB>(o / C::kRowB, (o % C::kRowB) >> 4);
-                        cp_async16_hint(base + k * C::kTileB + soff, ksrc + i * 512, pol);
-                        cp_async16_hint(base + (PPI + k) * C::kTileB + soff, vsrc + i * 512, pol);
+                        const int ot = o % C::kTileB;
+                        const uint32_t soff = (o / C::kTileB) * C::kTileB +
+                                              chunk_off<C::kRowB>(ot / C::kRowB, (ot % C::kRowB) >> 4);
+                        cp_async16_hint(base + k * HPT * C::kTileB + soff, ksrc + i * 512, pol);
+                        cp_async16_hint(base + (TT + k * HPT) * C::kTileB + soff, vsrc + i * 512, pol);
                     }
                     if constexpr (PER_TOKEN) {
-                        if (lane < 8) {          // 64 bytes of k scales, then 64 of v scales
-                            const float* src = (lane < 4 ? p.k_scale_cache : p.v_scale_cache) +
-                                               z * kPage + (lane & 3) * 4;
-                            cp_async16_hint(smem_addr(scl + (st * PPI + k) * C::kScaleB) + lane * 16,
+                        // 64 HPT bytes of k scales, then as many of v scales
+                        if (lane < 8 * HPT) {
+                            const bool kk = lane < 4 * HPT;
+                            const float* src = (kk ? p.k_scale_cache : p.v_scale_cache) + z * kPage +
+                                               (kk ? lane : lane - 4 * HPT) * 4;
+                            cp_async16_hint(smem_addr(scl + (st * PPI + k) * HPT * C::kScaleB) + lane * 16,
                                             src, pol);
                         }
                     }
@@ -773,20 +812,22 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 #pragma unroll
                     for (int k = 0; k < PPI; ++k) {
                         if (!here[k]) continue;
-                        const int z = blk[k] * p.Hkv + h_i;
+                        // one box holds the unit's HPT adjacent tiles of the page
+                        const int z = blk[k] * p.Hkv + h_i * HPT;
 #pragma unroll
                         for (int box = 0; box < C::kBoxes; ++box) {
-                            tma_load_3d_hint(base + k * C::kTileB + box * 2048, &kmap, box * 128, 0,
-                                             z, bar, pol);
-                            tma_load_3d_hint(base + (PPI + k) * C::kTileB + box * 2048, &vmap,
+                            tma_load_3d_hint(base + k * HPT * C::kTileB + box * 2048, &kmap,
+                                             box * 128, 0, z, bar, pol);
+                            tma_load_3d_hint(base + (TT + k * HPT) * C::kTileB + box * 2048, &vmap,
                                              box * 128, 0, z, bar, pol);
                         }
                         if constexpr (PER_TOKEN) {
-                            const uint32_t sdst = smem_addr(scl + (st * PPI + k) * C::kScaleB);
-                            bulk_load_hint(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage, 64,
+                            const uint32_t sdst = smem_addr(scl + (st * PPI + k) * HPT * C::kScaleB);
+                            bulk_load_hint(sdst, p.k_scale_cache + static_cast<size_t>(z) * kPage,
+                                           64 * HPT, bar, pol);
+                            bulk_load_hint(sdst + 64 * HPT,
+                                           p.v_scale_cache + static_cast<size_t>(z) * kPage, 64 * HPT,
                                            bar, pol);
-                            bulk_load_hint(sdst + 64, p.v_scale_cache + static_cast<size_t>(z) * kPage,
-                                           64, bar, pol);
                         }
                     }
                 }
@@ -808,13 +849,14 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
             const int b = seg[kSegInts * si + 0];
             const int pb = seg[kSegInts * si + 2], pe = seg[kSegInts * si + 3];
             const int lo = seg[kSegInts * si + 5], ctx = seg[kSegInts * si + 6];
-            load_q(b, seg[kSegInts * si + 1], __int_as_float(seg[kSegInts * si + 7]));
-            bool new_tok = false;           // this segment holds the unit's new token
+            load_q(b, seg[kSegInts * si + 1]);
+            bool new_tok = false;           // this segment holds the unit's new tokens
             if constexpr (FUSED) {
-                if ((seg[kSegInts * si + 4] & 4) && ctx >= 1)
-                    new_tok = store_new_token(b, seg[kSegInts * si + 1], ctx,
-                                              __int_as_float(seg[kSegInts * si + 7]),
-                                              __int_as_float(seg[kSegInts * si + 8]));
+                if ((seg[kSegInts * si + 4] & 4) && ctx >= 1) {
+#pragma unroll
+                    for (int hl = 0; hl < HPT; ++hl)   // same block for every head: same result
+                        new_tok = store_new_token(b, seg[kSegInts * si + 1] * HPT + hl, hl, ctx);
+                }
             }
             reset_state();
             for (int cpg = pb; cpg < pe; cpg += PPI) {
@@ -847,19 +889,20 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
             }
         }
 
-        // ---- S^T = K_page Q^T for each page (rows: tokens tA, tB; cols: heads 2c, 2c+1
-        //      of each 8-head group)
-        float acc[NT][PPI][4];
+        // ---- S^T = K_tile Q^T for each (page, head) tile (rows: tokens tA, tB; cols:
+        //      heads 2c, 2c+1 of each 8-head group; with packed heads every tile
+        //      fills all columns, of which the lane keeps its own head's)
+        float acc[NT][TT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int k = 0; k < PPI; ++k)
+            for (int k = 0; k < TT; ++k)
                 acc[nt][k][0] = acc[nt][k][1] = acc[nt][k][2] = acc[nt][k][3] = 0.f;
 #pragma unroll
         for (int s = 0; s < C::kSegs; ++s) {
-            uint4 kx[PPI], ky[PPI];
+            uint4 kx[TT], ky[TT];
 #pragma unroll
-            for (int k = 0; k < PPI; ++k) {
+            for (int k = 0; k < TT; ++k) {
                 kx[k] = *reinterpret_cast<const uint4*>(stage + k * C::kTileB + koffA[s]);
                 ky[k] = *reinterpret_cast<const uint4*>(stage + k * C::kTileB + koffB[s]);
             }
@@ -867,7 +910,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
             for (int jj = 0; jj < C::kKPerSeg; ++jj) {
                 const int ks = s * C::kKPerSeg + jj;
 #pragma unroll
-                for (int k = 0; k < PPI; ++k) {
+                for (int k = 0; k < TT; ++k) {
                     const uint32_t wx[4] = {kx[k].x, kx[k].y, kx[k].z, kx[k].w};
                     const uint32_t wy[4] = {ky[k].x, ky[k].y, ky[k].z, ky[k].w};
                     if constexpr (BF16) {
@@ -904,20 +947,29 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
             float ksA = 1.f, ksB = 1.f;
             vs[k][0] = vs[k][1] = 1.f;
             if constexpr (PER_TOKEN) {
-                const float* sk = reinterpret_cast<const float*>(scl + (st * PPI + k) * C::kScaleB);
+                // the page's scales: [k of head 0..HPT-1][v of head 0..HPT-1] x 16 tokens
+                const float* sk = reinterpret_cast<const float*>(scl + (st * PPI + k) * HPT * C::kScaleB) +
+                                  hl_lane * 16;
                 ksA = sk[tA];
                 ksB = sk[tB];
                 // scales of masked tokens may be any bits (slots never written,
                 // pages not fetched): zero them so that 0 * scale stays 0
-                vs[k][0] = vA ? sk[16 + tA] : 0.f;
-                vs[k][1] = vB ? sk[16 + tB] : 0.f;
+                vs[k][0] = vA ? sk[HPT * 16 + tA] : 0.f;
+                vs[k][1] = vB ? sk[HPT * 16 + tB] : 0.f;
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                z[nt][k][0] = vA ? acc[nt][k][0] * hs[nt][0] * ksA : neg_inf();
-                z[nt][k][1] = vA ? acc[nt][k][1] * hs[nt][1] * ksA : neg_inf();
-                z[nt][k][2] = vB ? acc[nt][k][2] * hs[nt][0] * ksB : neg_inf();
-                z[nt][k][3] = vB ? acc[nt][k][3] * hs[nt][1] * ksB : neg_inf();
+                // the accumulators of this lane's head's tile
+                float a4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a4[i] = acc[nt][k * HPT][i];
+                    if constexpr (HPT > 1) a4[i] = hl_lane == 1 ? acc[nt][k * HPT + 1][i] : a4[i];
+                }
+                z[nt][k][0] = vA ? a4[0] * hs[nt][0] * ksA : neg_inf();
+                z[nt][k][1] = vA ? a4[1] * hs[nt][1] * ksA : neg_inf();
+                z[nt][k][2] = vB ? a4[2] * hs[nt][0] * ksB : neg_inf();
+                z[nt][k][3] = vB ? a4[3] * hs[nt][1] * ksB : neg_inf();
                 mx[nt][0] = fmaxf(mx[nt][0], fmaxf(z[nt][k][0], z[nt][k][2]));
                 mx[nt][1] = fmaxf(mx[nt][1], fmaxf(z[nt][k][1], z[nt][k][3]));
             }
@@ -979,8 +1031,13 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 }
             }
 
+            // ---- per KV head of the unit: its V tile, and P^T restricted to its
+            //      columns (the B operand's column is the lane's g)
+#pragma unroll
+            for (int hl = 0; hl < HPT; ++hl) {
+            const uint32_t mb = HPT > 1 ? bmask[hl] : ~0u;
             // ---- V rows of tokens c, c+4, c+8, c+12 (k-slots 2c, 2c+1, 2c+8, 2c+9)
-            const uint8_t* vt = stage + (PPI + k) * C::kTileB;
+            const uint8_t* vt = stage + (TT + k * HPT + hl) * C::kTileB;
             uint32_t vr[4][C::kVWords];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -1022,8 +1079,8 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                     a3 = __byte_perm(vr[2][i], vr[3][i], 0x7632);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        mma_bf16(o[nt][i], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                        mma_bf16(o[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                        mma_bf16(o[nt][i], a0, a1, a2, a3, bh[nt][0] & mb, bh[nt][1] & mb);
+                        mma_bf16(o[nt][i], a0, a1, a2, a3, bl[nt][0] & mb, bl[nt][1] & mb);
                     }
                 } else {
                     const int w = i >> 1;
@@ -1034,11 +1091,12 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                     f16x2x2_from_e4m3x4(x23, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        mma_f16(o[nt][i], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                        mma_f16(o[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                        mma_f16(o[nt][i], a0, a1, a2, a3, bh[nt][0] & mb, bh[nt][1] & mb);
+                        mma_f16(o[nt][i], a0, a1, a2, a3, bl[nt][0] & mb, bl[nt][1] & mb);
                     }
                 }
             }
+            }   // heads of the unit
         }
 
         __syncwarp();
@@ -1059,12 +1117,12 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 #undef FP8KV_WORKER
 }
 
-// split_merge, one block per query head (b, hq) of unit (b, h = hq / G): the
+// split_merge, one block per query head (b, hq) of unit (b, h = hq / Gu): the
 // workers (warps) whose shares touched a unit left partials (m, l, O) in slots
 // worker + unit and recorded the first and last of them; combine them as
 // O = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w.  A unit one worker covered
 // whole was written by that worker; an empty unit gets a zero row.  The block's
-// warps (4 to 16, sized by the launch to the parts per unit) take the parts
+// warps (4 to 8, sized by the launch to the parts per unit) take the parts
 // round-robin, each lane D/32 columns, all loads of a chunk of parts in flight
 // together, and meet in shared memory ([warps][D + 2] floats, dynamic).
 template <int D>
@@ -1077,8 +1135,8 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     float* sm_l = sm_m + nw;                    // [nw]
     const int row = blockIdx.x;                 // b * Hq + hq
     const int b = row / p.Hq, hq = row % p.Hq;
-    const int G = p.G, h = hq / G, head = hq % G;
-    const int unit = b * p.Hkv + h;
+    const int Gu = p.Gu, h = hq / Gu, head = hq % Gu;
+    const int unit = b * p.Hu + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // context_lens are read before the wait only when the caller allows it (the
     // decode kernel lets this one start early; it has waited for its own
@@ -1094,7 +1152,7 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
         int nb = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int bb = b0 + lane;
-            const long long w = bb < p.B ? static_cast<long long>(vis_pages(p, bb)) * p.Hkv : 0;
+            const long long w = bb < p.B ? static_cast<long long>(vis_pages(p, bb)) * p.Hu : 0;
             long long incl = w;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -1135,7 +1193,7 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
         for (int q = 0; q < kChunk; ++q) {
             const long long w = w0 + nw * q;
             const bool ok = w <= last;
-            const size_t sl = (static_cast<size_t>(ok ? w : first) + unit) * G + head;
+            const size_t sl = (static_cast<size_t>(ok ? w : first) + unit) * Gu + head;
             mi[q] = ok ? p.ws_m[sl] : neg_inf();
             li[q] = ok ? p.ws_l[sl] : 0.f;
 #pragma unroll
@@ -1173,12 +1231,12 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     }
 }
 
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          cudaStream_t stream) {
-    using C = Cfg<D, BF16, NT>;
+    using C = Cfg<D, BF16, NT, HPT>;
     constexpr int kSmemBytes = FUSED ? C::kSmemFused : C::kSmem;
-    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED, NT>;
+    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED, NT, HPT>;
     // opt in to the large dynamic shared-memory size once per context
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmemBytes, attr_done);
@@ -1197,11 +1255,13 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
     if (e != cudaSuccess) return e;
-    // merge block: about 4 parts per warp at the launch's mean parts per unit
-    const long long units = static_cast<long long>(p.B) * p.Hkv;
+    // merge block: about 4 parts per warp at the launch's mean parts per unit,
+    // 4 to 8 warps (larger merge blocks hold SM slots the next decode grid,
+    // launched early, is waiting for: 16-warp blocks cost 4 us a step)
+    const long long units = static_cast<long long>(p.B) * p.Hu;
     const long long mean_parts = (static_cast<long long>(p.num_splits) * kWarps + units - 1) / units + 1;
     long long mw = (mean_parts + 3) / 4;
-    mw = mw < 4 ? 4 : (mw > 16 ? 16 : mw);
+    mw = mw < 4 ? 4 : (mw > 8 ? 8 : mw);
     cudaLaunchConfig_t mcfg = cfg;
     mcfg.gridDim = dim3(p.B * p.Hq);
     mcfg.blockDim = dim3(static_cast<unsigned>(32 * mw));
@@ -1209,14 +1269,25 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     return cudaLaunchKernelEx(&mcfg, split_merge_kernel<D>, p);
 }
 
+// packed heads (p.hpt == 2) only where the host allows them: one 8-head group,
+// tiles of at most 2 KiB
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
+cudaError_t dispatch_hpt(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         cudaStream_t s) {
+    if constexpr (NT == 1 && D * (BF16 ? 2 : 1) <= 128) {
+        if (p.hpt == 2) return launch_split<D, BF16, PER_TOKEN, FUSED, NT, 2>(p, kmap, vmap, s);
+    }
+    return launch_split<D, BF16, PER_TOKEN, FUSED, NT, 1>(p, kmap, vmap, s);
+}
+
 template <int D, bool FUSED, int NT>
 cudaError_t dispatch_dtype(const DecodeParams& p, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int kv_dtype, cudaStream_t s) {
     if (kv_dtype == FP8KV_KV_BF16)
-        return launch_split<D, true, false, FUSED, NT>(p, kmap, vmap, s);
+        return dispatch_hpt<D, true, false, FUSED, NT>(p, kmap, vmap, s);
     if (p.scale_mode == FP8KV_SCALE_PER_TOKEN_HEAD)
-        return launch_split<D, false, true, FUSED, NT>(p, kmap, vmap, s);
-    return launch_split<D, false, false, FUSED, NT>(p, kmap, vmap, s);
+        return dispatch_hpt<D, false, true, FUSED, NT>(p, kmap, vmap, s);
+    return dispatch_hpt<D, false, false, FUSED, NT>(p, kmap, vmap, s);
 }
 
 template <int D>
@@ -1229,28 +1300,45 @@ cudaError_t dispatch_fused(const DecodeParams& p, const CUtensorMap& kmap,
                  : dispatch_dtype<D, false, 1>(p, kmap, vmap, kv_dtype, s);
 }
 
-template <int D, bool BF16, int NT>
-constexpr int smem_of() { return Cfg<D, BF16, NT>::kSmemFused; }
+template <int D, bool BF16, int NT, int HPT>
+constexpr int smem_of() { return Cfg<D, BF16, NT, HPT>::kSmemFused; }
 
-template <int D, int NT>
-int ctas_of(bool bf) {
-    const int bytes = bf ? smem_of<D, true, NT>() : smem_of<D, false, NT>();
-    const int by_smem = (228 * 1024) / (bytes + 1024);
+template <int D, bool BF16, int NT, int HPT>
+int ctas_of() {
+    const int by_smem = (228 * 1024) / (smem_of<D, BF16, NT, HPT>() + 1024);
     // the launch bounds' register budget
-    const int by_regs = bf ? decode_min_ctas<D, true, NT>() : decode_min_ctas<D, false, NT>();
+    const int by_regs = decode_min_ctas<D, BF16, NT>();
     const int n = by_smem < by_regs ? by_smem : by_regs;
     return n < 1 ? 1 : n;
 }
 
+template <int D, int NT>
+int ctas_of(bool bf) { return bf ? ctas_of<D, true, NT, 1>() : ctas_of<D, false, NT, 1>(); }
+
 }  // namespace
 
-int decode_ctas_per_sm(int D, int kv_dtype, int G) {
+int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv) {
+    const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
+    return (G == 2 || G == 4) && Hkv % 2 == 0 && row_bytes <= 128 ? 2 : 1;
+}
+
+int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv) {
     const bool bf = kv_dtype == FP8KV_KV_BF16;
-    const bool two = G > 8;
+    if (G > 8) {
+        switch (D) {
+            case 64: return ctas_of<64, 2>(bf);
+            case 128: return ctas_of<128, 2>(bf);
+            default: return ctas_of<256, 2>(bf);
+        }
+    }
+    if (decode_heads_per_unit(D, kv_dtype, G, Hkv) == 2) {   // rows of at most 128 bytes
+        if (D == 64) return bf ? ctas_of<64, true, 1, 2>() : ctas_of<64, false, 1, 2>();
+        return ctas_of<128, false, 1, 2>();
+    }
     switch (D) {
-        case 64: return two ? ctas_of<64, 2>(bf) : ctas_of<64, 1>(bf);
-        case 128: return two ? ctas_of<128, 2>(bf) : ctas_of<128, 1>(bf);
-        default: return two ? ctas_of<256, 2>(bf) : ctas_of<256, 1>(bf);
+        case 64: return ctas_of<64, 1>(bf);
+        case 128: return ctas_of<128, 1>(bf);
+        default: return ctas_of<256, 1>(bf);
     }
 }
 

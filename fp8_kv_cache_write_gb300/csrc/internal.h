@@ -49,9 +49,12 @@ struct DecodeParams {
     float scale_log2;            // softmax_scale * log2(e)
     int window;
     int num_splits;              // CTAs of the decode grid
-    float* ws_m;                 // [4*num_splits + B*Hkv][G] running max (log2 units)
-    float* ws_l;                 // [4*num_splits + B*Hkv][G] softmax denominator
-    float* ws_o;                 // [4*num_splits + B*Hkv][G][D] unnormalised output
+    int hpt;                     // KV heads per unit (decode_heads_per_unit)
+    int Hu;                      // units per sequence, Hkv / hpt
+    int Gu;                      // query heads per unit, G * hpt
+    float* ws_m;                 // [4*num_splits + B*Hu][Gu] running max (log2 units)
+    float* ws_l;                 // [4*num_splits + B*Hu][Gu] softmax denominator
+    float* ws_o;                 // [4*num_splits + B*Hu][Gu][D] unnormalised output
     void* out;                   // [B][Hq][D]
     int out_bf16;
     int scale_mode;
@@ -124,8 +127,13 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
 
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;
+// KV heads per decode unit: 2 packs adjacent KV heads h, h + 1 (G = 2 or 4
+// query heads each, an even Hkv, tiles of at most 2 KiB) into one unit whose
+// tiles are copied together and share the 8 MMA columns; else 1.
+int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv);
 // CTAs of the decode kernel resident per SM (shared memory and the register
-// budget of its launch bounds) for head dim D and G query heads per KV head.
-int decode_ctas_per_sm(int D, int kv_dtype, int G);
+// budget of its launch bounds) for head dim D, G query heads per KV head and
+// Hkv KV heads.
+int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv);
 
 }  // namespace fp8kv

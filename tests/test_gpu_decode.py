@@ -42,9 +42,20 @@ def _check(w, kv_dtype, units=None, **kw):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
-@pytest.mark.parametrize("G", [1, 4, 8, 12, 16])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 12, 16])
 def test_decode_ragged_parity(D, kv_dtype, mode, G):
+    # 2 KV heads: with G = 2 or 4 and rows of at most 128 bytes both heads form
+    # one unit (their tiles copied together, their query heads sharing the 8
+    # MMA columns); per-head scales then differ between the columns of a unit
     w = synth.decode_workload(100 + D + G, RAGGED, 2 * G, 2, D, mode, outlier_frac=0.01)
+    e, _, _ = _check(w, kv_dtype)
+    assert e <= DECODE_TOL, e
+
+
+@pytest.mark.parametrize("kv_dtype,mode", [(0, 1), (0, 2), (1, 0)])
+def test_odd_kv_head_count_with_four_query_heads(kv_dtype, mode):
+    # G = 4 but Hkv = 3: heads are not packed in pairs (one KV head per unit)
+    w = synth.decode_workload(41, [2000, 17, 600], 12, 3, 128, mode, outlier_frac=0.01)
     e, _, _ = _check(w, kv_dtype)
     assert e <= DECODE_TOL, e
 
@@ -94,8 +105,9 @@ def test_page_permutation_invariance():
 
 @pytest.mark.parametrize("window", [1, 17, 128, 5000])
 @pytest.mark.parametrize("kv_dtype", [0, 1])
-def test_window(window, kv_dtype):
-    w = synth.decode_workload(9, [0, 5, 130, 1000, 4000], 16, 2, 64, 2, window=window)
+@pytest.mark.parametrize("Hq", [16, 8])
+def test_window(window, kv_dtype, Hq):
+    w = synth.decode_workload(9, [0, 5, 130, 1000, 4000], Hq, 2, 64, 2, window=window)
     e, _, _ = _check(w, kv_dtype)
     assert e <= DECODE_TOL, e
     if window >= 4000:     # a window covering the context is full attention

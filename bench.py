@@ -496,6 +496,12 @@ def _time_graph(fn, n_calls, stream, warmup=3):
     return t0.elapsed_time(t1) / (2 * n_calls)
 
 
+# launch-overlap flags of the decode calls the extras time (--decode-flags): the
+# kernel before each call is the previous call's split_merge, which writes only
+# `out`, so page streaming may start before it ends
+_DECODE_FLAGS = 0
+
+
 def _decode_caller(fk, w, kv_dtype, mode, caches, dev, window=0):
     q, bt, cl = w.q.to(dev), w.block_table.to(dev), w.context_lens.to(dev)
     _, ws_bytes = fk.decode_plan(w.B, w.Hq, w.Hkv, w.D, bt.shape[1], window)
@@ -508,7 +514,7 @@ def _decode_caller(fk, w, kv_dtype, mode, caches, dev, window=0):
         kc, vc, ks, vs = caches[i % len(caches)]
         fk.paged_decode_attn(q, kc, vc, bt, cl, kv_dtype=kv_dtype, scale_mode=mode,
                              k_scale=ksc, v_scale=vsc, k_scale_cache=ks, v_scale_cache=vs,
-                             window=window, workspace=ws, out=out)
+                             window=window, workspace=ws, out=out, flags=_DECODE_FLAGS)
     return decode
 
 
@@ -1011,6 +1017,8 @@ def main():
 
     if args.extras and args.impl == "ours":
         import fp8_kv_cache_write_gb300 as fk
+        global _DECODE_FLAGS
+        _DECODE_FLAGS = args.decode_flags
         fk.lib()
         dev = torch.device("cuda", local)
         torch.cuda.set_device(dev)

@@ -195,12 +195,12 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
     const int64_t units = static_cast<int64_t>(B) * Hkv;
     const int64_t work = units * maxvis;
     const int G1 = Hkv > 0 ? Hq / Hkv : 1;
-    const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, G1, Hkv);
+    const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, G1, Hkv, B);
     int64_t n;
     if (req > 0) {
         n = static_cast<int64_t>(req) * units;
     } else {
-        n = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0, G1, Hkv);
+        n = static_cast<int64_t>(sm_count()) * decode_ctas_per_sm(D, 0, G1, Hkv, B);
         const int64_t by_work = (work + 15) / 16;
         if (by_work < n) n = by_work;
         // units of at most 16 visible pages (a sliding window): one worker warp
@@ -403,7 +403,7 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
     const int64_t nbh = num_blocks * Hkv;
-    const int hpt = decode_heads_per_unit(D, kv_dtype, Hq / Hkv, Hkv);
+    const int hpt = decode_heads_per_unit(D, kv_dtype, Hq / Hkv, Hkv, B);
     CUtensorMap kmap, vmap;
     if (!make_kv_map(k_cache, row_bytes, nbh, &kmap, false, hpt) ||
         !make_kv_map(v_cache, row_bytes, nbh, &vmap, false, hpt))
@@ -471,7 +471,7 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
     if (num_splits == 0 && Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 && valid_d(D)) {
         // slots that fit, less the one per unit, over the 4 worker warps of a CTA
         // (a worker's slot holds hpt KV heads' query heads, as the planner sizes it)
-        const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, Hq / Hkv, Hkv);
+        const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, Hq / Hkv, Hkv, B);
         const int64_t slot_bytes = static_cast<int64_t>(Hq / Hkv) * (D + 2) * sizeof(float);
         const int64_t spare = static_cast<int64_t>(scratch_bytes) / slot_bytes -
                               static_cast<int64_t>(B) * Hkv;

@@ -1122,7 +1122,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
 // worker + unit and recorded the first and last of them; combine them as
 // O = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w.  A unit one worker covered
 // whole was written by that worker; an empty unit gets a zero row.  The block's
-// warps (4 to 8, sized by the launch to the parts per unit) take the parts
+// warps (4 to 16, sized by the launch to the parts per unit) take the parts
 // round-robin, each lane D/32 columns, all loads of a chunk of parts in flight
 // together, and meet in shared memory ([warps][D + 2] floats, dynamic).
 template <int D>
@@ -1256,12 +1256,14 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
     if (e != cudaSuccess) return e;
     // merge block: about 4 parts per warp at the launch's mean parts per unit,
-    // 4 to 8 warps (larger merge blocks hold SM slots the next decode grid,
-    // launched early, is waiting for: 16-warp blocks cost 4 us a step)
+    // 4 to 16 warps; at most 8 when there are more merge blocks than SMs (larger
+    // blocks then hold SM slots the next decode grid, launched early, is
+    // waiting for: 16-warp blocks cost 4 us a step on the Llama-shaped batch)
     const long long units = static_cast<long long>(p.B) * p.Hu;
     const long long mean_parts = (static_cast<long long>(p.num_splits) * kWarps + units - 1) / units + 1;
+    const long long cap = static_cast<long long>(p.B) * p.Hq > 152 ? 8 : 16;
     long long mw = (mean_parts + 3) / 4;
-    mw = mw < 4 ? 4 : (mw > 8 ? 8 : mw);
+    mw = mw < 4 ? 4 : (mw > cap ? cap : mw);
     cudaLaunchConfig_t mcfg = cfg;
     mcfg.gridDim = dim3(p.B * p.Hq);
     mcfg.blockDim = dim3(static_cast<unsigned>(32 * mw));
@@ -1317,12 +1319,14 @@ int ctas_of(bool bf) { return bf ? ctas_of<D, true, NT, 1>() : ctas_of<D, false,
 
 }  // namespace
 
-int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv) {
+int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv, int B) {
     const int row_bytes = D * (kv_dtype == FP8KV_KV_BF16 ? 2 : 1);
-    return (G == 2 || G == 4) && Hkv % 2 == 0 && row_bytes <= 128 ? 2 : 1;
+    // few units (B Hkv < 32): halving them doubles the parts each merge combines
+    return (G == 2 || G == 4) && Hkv % 2 == 0 && row_bytes <= 128 &&
+                   static_cast<long long>(B) * Hkv >= 32 ? 2 : 1;
 }
 
-int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv) {
+int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv, int B) {
     const bool bf = kv_dtype == FP8KV_KV_BF16;
     if (G > 8) {
         switch (D) {
@@ -1331,7 +1335,7 @@ int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv) {
             default: return ctas_of<256, 2>(bf);
         }
     }
-    if (decode_heads_per_unit(D, kv_dtype, G, Hkv) == 2) {   // rows of at most 128 bytes
+    if (decode_heads_per_unit(D, kv_dtype, G, Hkv, B) == 2) {   // rows of at most 128 bytes
         if (D == 64) return bf ? ctas_of<64, true, 1, 2>() : ctas_of<64, false, 1, 2>();
         return ctas_of<128, false, 1, 2>();
     }

@@ -128,12 +128,13 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
 // Decode kernel geometry used by the planner and the tensor maps.
 constexpr int kDecodeWarps = 4;
 // KV heads per decode unit: 2 packs adjacent KV heads h, h + 1 (G = 2 or 4
-// query heads each, an even Hkv, tiles of at most 2 KiB) into one unit whose
-// tiles are copied together and share the 8 MMA columns; else 1.
-int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv);
+// query heads each, an even Hkv, tiles of at most 2 KiB, at least 32 (sequence,
+// KV head) pairs in the batch) into one unit whose tiles are copied together
+// and share the 8 MMA columns; else 1.
+int decode_heads_per_unit(int D, int kv_dtype, int G, int Hkv, int B);
 // CTAs of the decode kernel resident per SM (shared memory and the register
-// budget of its launch bounds) for head dim D, G query heads per KV head and
-// Hkv KV heads.
-int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv);
+// budget of its launch bounds) for head dim D, G query heads per KV head, Hkv
+// KV heads and B sequences.
+int decode_ctas_per_sm(int D, int kv_dtype, int G, int Hkv, int B);
 
 }  // namespace fp8kv

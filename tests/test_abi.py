@@ -59,14 +59,15 @@ def test_decode_plan_is_consistent(lib):
     # num_splits = CTAs of the balanced partition (4 worker warps each); one
     # workspace slot per warp plus one per unit, of the unit's query heads x
     # (D + 2) floats.  A unit packs two adjacent KV heads (hpt = 2) when each has
-    # 2 or 4 query heads, Hkv is even and an e4m3 row is at most 128 bytes.
+    # 2 or 4 query heads, Hkv is even, an e4m3 row is at most 128 bytes and the
+    # batch holds at least 32 (sequence, KV head) pairs.
     for B, Hq, Hkv, D, mbs, win in [(8, 32, 8, 128, 1375, 0), (1, 64, 8, 128, 8192, 0),
                                     (32, 64, 8, 64, 2048, 128), (1, 32, 8, 128, 64, 0),
                                     (4, 16, 8, 64, 100, 0), (2, 12, 3, 128, 50, 0),
                                     (8, 32, 8, 256, 100, 0)]:
         s, ws = fk.decode_plan(B, Hq, Hkv, D, mbs, win)
         G = Hq // Hkv
-        hpt = 2 if G in (2, 4) and Hkv % 2 == 0 and D <= 128 else 1
+        hpt = 2 if G in (2, 4) and Hkv % 2 == 0 and D <= 128 and B * Hkv >= 32 else 1
         assert 1 <= s <= 1024
         assert ws == (4 * s * hpt + B * Hkv) * G * (D + 2) * 4
         for req in (1, 2, 7):

@@ -44,18 +44,21 @@ def _check(w, kv_dtype, units=None, **kw):
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 12, 16])
 def test_decode_ragged_parity(D, kv_dtype, mode, G):
-    # 2 KV heads: with G = 2 or 4 and rows of at most 128 bytes both heads form
-    # one unit (their tiles copied together, their query heads sharing the 8
-    # MMA columns); per-head scales then differ between the columns of a unit
-    w = synth.decode_workload(100 + D + G, RAGGED, 2 * G, 2, D, mode, outlier_frac=0.01)
+    # 8 sequences x 4 KV heads: with G = 2 or 4 and rows of at most 128 bytes
+    # adjacent KV heads form one unit (their tiles copied together, their query
+    # heads sharing the 8 MMA columns); per-head scales then differ between the
+    # columns of a unit
+    w = synth.decode_workload(100 + D + G, RAGGED, 4 * G, 4, D, mode, outlier_frac=0.01)
     e, _, _ = _check(w, kv_dtype)
     assert e <= DECODE_TOL, e
 
 
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 1), (0, 2), (1, 0)])
-def test_odd_kv_head_count_with_four_query_heads(kv_dtype, mode):
-    # G = 4 but Hkv = 3: heads are not packed in pairs (one KV head per unit)
-    w = synth.decode_workload(41, [2000, 17, 600], 12, 3, 128, mode, outlier_frac=0.01)
+@pytest.mark.parametrize("ctx,Hkv", [([2000, 17, 600] * 4, 3), ([2000, 17, 600], 2)])
+def test_four_query_heads_without_packing(kv_dtype, mode, ctx, Hkv):
+    # G = 4 but an odd KV head count, or fewer than 32 (sequence, KV head)
+    # pairs: one KV head per unit
+    w = synth.decode_workload(41, ctx, 4 * Hkv, Hkv, 128, mode, outlier_frac=0.01)
     e, _, _ = _check(w, kv_dtype)
     assert e <= DECODE_TOL, e
 
@@ -72,7 +75,7 @@ def test_gqa_groups_beyond_eight_heads(G, splits):
 
 @pytest.mark.parametrize("splits", [1, 2, 7, 0])
 def test_split_count_invariance(splits):
-    w = synth.decode_workload(7, [2000, 33, 900], 32, 8, 128, 2, outlier_frac=0.01)
+    w = synth.decode_workload(7, [2000, 33, 900, 1500], 32, 8, 128, 2, outlier_frac=0.01)
     gc = gpu_fill(w, 0)
     ref = gpu_decode(w, gc, num_splits=1).cpu().numpy()
     got = gpu_decode(w, gc, num_splits=splits).cpu().numpy()
@@ -105,9 +108,9 @@ def test_page_permutation_invariance():
 
 @pytest.mark.parametrize("window", [1, 17, 128, 5000])
 @pytest.mark.parametrize("kv_dtype", [0, 1])
-@pytest.mark.parametrize("Hq", [16, 8])
-def test_window(window, kv_dtype, Hq):
-    w = synth.decode_workload(9, [0, 5, 130, 1000, 4000], Hq, 2, 64, 2, window=window)
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (32, 8)])
+def test_window(window, kv_dtype, Hq, Hkv):
+    w = synth.decode_workload(9, [0, 5, 130, 1000, 4000], Hq, Hkv, 64, 2, window=window)
     e, _, _ = _check(w, kv_dtype)
     assert e <= DECODE_TOL, e
     if window >= 4000:     # a window covering the context is full attention

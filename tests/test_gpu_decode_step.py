@@ -45,9 +45,11 @@ def _history_only(w, kv_dtype, fill=None, err=None):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("kv_dtype,mode", [(0, 0), (0, 1), (0, 2), (1, 0)])
-@pytest.mark.parametrize("G", [1, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
 def test_step_parity(D, kv_dtype, mode, G):
-    w = synth.decode_workload(300 + D + G, RAGGED, 2 * G, 2, D, mode, outlier_frac=0.01)
+    # 8 sequences x 4 KV heads: G = 2 and 4 pack adjacent KV heads into one unit
+    # (rows of at most 128 bytes), whose new tokens the same warp stores
+    w = synth.decode_workload(300 + D + G, RAGGED, 4 * G, 4, D, mode, outlier_frac=0.01)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     gc = _history_only(w, kv_dtype, err=err)
     out = _step(w, gc, err)

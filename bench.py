@@ -500,6 +500,8 @@ def _time_graph(fn, n_calls, stream, warmup=3):
 # kernel before each call is the previous call's split_merge, which writes only
 # `out`, so page streaming may start before it ends
 _DECODE_FLAGS = 0
+# the oracle timed beside the extras (off with --no-cpu-baseline)
+_CPU_BASELINE = True
 
 
 def _decode_caller(fk, w, kv_dtype, mode, caches, dev, window=0):
@@ -686,7 +688,8 @@ def _extra_tiny(fk, synth, dev, stream, emit):
         ms = _time_graph(_decode_caller(fk, w, kv, 0, caches, dev), 64, stream)
         row[name + "_us"] = ms * 1e3
         del caches
-    row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 0, seconds=3.0)
+    if _CPU_BASELINE:
+        row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 0, seconds=3.0)
     emit(row)
 
 
@@ -704,7 +707,8 @@ def _extra_needle(fk, synth, dev, stream, emit):
         del caches
         torch.cuda.empty_cache()
     row["fp8_speedup"] = row["bf16_us"] / row["fp8_us"]
-    row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 1)
+    if _CPU_BASELINE:
+        row["cpu_baseline"] = _oracle_decode_baseline(w, 0, 1)
     emit(row)
 
 
@@ -743,7 +747,7 @@ def _extra_hybrid(fk, synth, dev, stream, emit):
                 "full_layer_gbs": kv_b[1] / per_type[1] / 1e3,
                 "full_layer_frac_of_hbm": kv_b[1] / per_type[1] / 1e3 / hbm,
                 "window_layer_bytes": kv_b[0]}
-        if variant == "window_bf16_full_fp8":
+        if variant == "window_bf16_full_fp8" and _CPU_BASELINE:
             # the oracle on one layer of each type, 12 of each per step
             cb = [_oracle_decode_baseline(wl[lt], dtypes[lt] if lt == 0 else 0,
                                           0 if lt == 0 else 2, seconds=4.0) for lt in (0, 1)]
@@ -849,7 +853,7 @@ def _extra_prefill(fk, synth, dev, stream, emit):
                     "split": split, "ms": ms, "tflops": flops / ms / 1e9}
             if kv == E4 and isinstance(peak, float):
                 line["frac_of_fp8_peak"] = flops / ms / 1e9 / peak
-            if kv == E4 and not two and split == "auto":
+            if kv == E4 and not two and split == "auto" and _CPU_BASELINE:
                 line["cpu_baseline"] = _oracle_prefill_baseline(w)
             emit(line)
         del kc, vc
@@ -1017,8 +1021,9 @@ def main():
 
     if args.extras and args.impl == "ours":
         import fp8_kv_cache_write_gb300 as fk
-        global _DECODE_FLAGS
+        global _DECODE_FLAGS, _CPU_BASELINE
         _DECODE_FLAGS = args.decode_flags
+        _CPU_BASELINE = not args.no_cpu_baseline
         fk.lib()
         dev = torch.device("cuda", local)
         torch.cuda.set_device(dev)

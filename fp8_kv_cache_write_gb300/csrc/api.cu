@@ -174,13 +174,15 @@ bool make_kv_map(const void* base, int row_bytes, int64_t nbh, CUtensorMap* out,
 struct Plan {
     int num_splits;          // CTAs of the decode grid (work partitions)
     size_t workspace_bytes;
+    bool cta_units;          // one CTA per unit, combining in shared memory
 };
 
 // Decode planner.  The launch's (seq, KV head, page) tiles are split evenly over
 // the 4 warps of `num_splits` CTAs.  Automatic: one wave of resident CTAs, but no fewer than
 // 16 tiles per CTA for the upper bound of the work (B * Hkv * visible pages);
 // an explicit count n asks for about n partitions per (seq, KV head) unit;
-// max_ctas > 0 caps the CTA count.
+// max_ctas > 0 caps the CTA count.  Sliding windows of at most 16 visible pages
+// under the automatic plan take one CTA per unit instead (no workspace).
 // Workspace: one (m, l, O) slot per (warp, unit) pair a warp can touch, i.e.
 // 4 * num_splits + B * Hkv / hpt slots of G * hpt query heads, for the heads per
 // unit hpt of the e4m3 cache (at least the bf16 cache's, so the size covers both).
@@ -207,6 +209,18 @@ int plan(int B, int Hq, int Hkv, int D, int max_blocks, int window, int req, Pla
         // per unit, so that every unit ends in its own warp (no partials to merge)
         if (maxvis <= 16) n = (units / hpt + kDecodeWarps - 1) / kDecodeWarps;
     }
+    // sliding windows (few pages per unit), automatic plan, one 8-column group:
+    // one CTA per unit, whose 4 warps split the unit's pages and combine their
+    // partials in shared memory -- no workspace, no split_merge launch
+    const int64_t cta_units = units / hpt;
+    if (req == 0 && window > 0 && maxvis <= 16 && G1 * hpt <= 8 && cta_units >= 1 &&
+        cta_units <= 65535) {
+        out->num_splits = static_cast<int>(cta_units);
+        out->workspace_bytes = 16;
+        out->cta_units = true;
+        return FP8KV_OK;
+    }
+    out->cta_units = false;
     if (n > work) n = work;
     if (n > 1024) n = 1024;
     if (max_ctas > 0 && n > max_ctas) n = max_ctas;
@@ -429,6 +443,8 @@ int paged_decode(const void* q, const void* k_new, const void* v_new, const void
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.window = window;
     p.num_splits = pl.num_splits;
+    p.cta_units = pl.cta_units ? 1 : 0;
+    if (p.cta_units) p.num_splits = B * p.Hu;   // one CTA per unit of this cache's kind
     {
         float* ws = static_cast<float*>(workspace);
         const size_t rows = (static_cast<size_t>(pl.num_splits) * kDecodeWarps +

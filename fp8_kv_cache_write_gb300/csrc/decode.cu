@@ -93,9 +93,12 @@ struct Cfg {
     static constexpr int kOffSegs = kOffBars + kWarps * kStages * 8;
     static constexpr int kOffShare = kOffSegs + kWarps * kMaxSeg * kSegInts * 4;  // [warp][resume, end]
     static constexpr int kOffCtx = kOffShare + kWarps * 16;    // [warp][32] context lengths
+    // CTA units: what each warp left for the CTA's combine (0 nothing, 1 a partial
+    // in its ring, 2 its unit's output, written whole)
+    static constexpr int kOffFlag = kOffCtx + kWarps * 128;
     // NT = 2 (more than 8 query heads per KV head): each warp's query fragments of
     // both 8-head groups, [group][k-step][lane] (8 bytes each), in shared memory
-    static constexpr int kOffQsm = kOffCtx + kWarps * 128;
+    static constexpr int kOffQsm = kOffFlag + kWarps * 4;
     static constexpr int kQsmBytes = NT > 1 ? kWarps * NT * kKSteps * 32 * 8 : 0;
     static constexpr int kSmem = 1024 + kOffQsm + kQsmBytes;
     // fused step only, after the above: per warp the new token's K row, V row
@@ -306,12 +309,53 @@ constexpr int decode_min_ctas() {
     return NT > 1 || D > 128 ? 2 : (D * (BF16 ? 2 : 1) == 64 ? 4 : 3);
 }
 
+// CTA units: the CTA's unit (b, h) = (blockIdx.x / Hu, blockIdx.x % Hu); its
+// warps left partials (O [Gu][D], m [Gu], l [Gu] at the start of their ring,
+// flag 1), or wrote the unit whole (flag 2), or had no pages (flag 0).  Rows
+// b Hq + h Gu + col get O = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w; an empty
+// unit gets zero rows.  Called by every thread after a CTA barrier.
+template <int D, bool BF16>
+__device__ __noinline__ void cta_combine(const DecodeParams& p, const uint8_t* smem, int warp_smem,
+                                         int off_flag) {
+    const volatile int* flag = reinterpret_cast<const volatile int*>(smem + off_flag);
+    const int Gu = p.Gu;
+    int parts = 0, whole = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        parts += flag[w] == 1;
+        whole += flag[w] == 2;
+    }
+    if (parts == 0 && whole > 0) return;
+    const size_t row0 = static_cast<size_t>(blockIdx.x / p.Hu) * p.Hq +
+                        static_cast<size_t>(blockIdx.x % p.Hu) * Gu;
+    for (int idx = threadIdx.x; idx < Gu * D; idx += blockDim.x) {
+        const int col = idx / D, d = idx - col * D;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            if (flag[w] == 1)
+                M = fmaxf(M, reinterpret_cast<const float*>(smem + w * warp_smem)[Gu * D + col]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            if (flag[w] == 1) {
+                const float* po = reinterpret_cast<const float*>(smem + w * warp_smem);
+                const float a = ex2(po[Gu * D + col] - M);
+                L += a * po[Gu * D + Gu + col];
+                O += a * po[col * D + d];
+            }
+        store_out<BF16>(p.out, p.out_bf16, (row0 + col) * D + d, L > 0.f ? O / L : 0.f);
+    }
+}
+
 // FUSED: a decode step -- the kernel also stores every sequence's new token
 // (k_new / v_new at position ctx - 1).  NT: 8-head groups per KV head (1 for
 // G <= 8, 2 for G <= 16); the groups share every K and V conversion.  HPT: KV
 // heads per unit (2: adjacent heads h, h + 1 share the 8 columns, G <= 4 each).
 // A unit is (sequence, group of HPT KV heads) with Gu = G * HPT query heads.
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT>
+// CTA: CTA units (p.cta_units) -- a template parameter, so that the flattened
+// partition's instances carry none of its code.
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT, bool CTA>
 __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -335,7 +379,10 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     uint32_t bmask[HPT];
 #pragma unroll
     for (int hl = 0; hl < HPT; ++hl) bmask[hl] = g / G == hl ? ~0u : 0u;
-    pdl_trigger();                        // split_merge may launch while this runs
+    // split_merge may launch while this runs; CTA units have no merge and trigger
+    // at their end (a next decode grid launched now would take SM slots as they
+    // free up and spread over several waves)
+    if constexpr (!CTA) pdl_trigger();
     // Ordering against the preceding kernel of the stream (programmatic launch):
     // by default the kernel waits for it before reading any global memory.  With
     // FP8KV_DECODE_EARLY_SETUP the set-up below -- shares, segments, page-table
@@ -378,18 +425,37 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
              ln += static_cast<long long>(gridDim.x) * 32)
             prefetch_l2(reinterpret_cast<const void*>(base + ln * 128));
     }
+    // CTA units (p.cta_units): CTA u takes unit u = (b, h) whole, its 4 warps
+    // splitting the unit's pages; they combine in shared memory, no split_merge
+    constexpr bool cta_mode = CTA;
+    if (cta_mode && static_cast<int>(blockIdx.x) >= p.B * p.Hu) return;   // (the whole CTA)
     // the first 32 context lengths are read once and kept in shared memory
     volatile int* ctx32 = reinterpret_cast<volatile int*>(smem + C::kOffCtx) + 32 * warp;
     long long W = 0;
+    long long cu_base = 0;                // CTA units: tile index of sequence cu_b's first tile
+    int cu_pages = 0;                     //            and its visible pages
+    const int cu_b = static_cast<int>(blockIdx.x) / p.Hu;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
         long long w = 0;
+        int np = 0;
         if (bb < p.B) {
             const int craw = p.context_lens[bb];
             if (b0 == 0) ctx32[lane] = craw;
             int lo_, ctx_, plo_, phi_;
             visible_of(p, craw, lo_, ctx_, plo_, phi_, blockIdx.x == 0 && warp == 0);
-            w = phi_ > plo_ ? static_cast<long long>(phi_ - plo_) * p.Hu : 0;
+            np = phi_ > plo_ ? phi_ - plo_ : 0;
+            w = static_cast<long long>(np) * p.Hu;
+        }
+        if (cta_mode && cu_b >= b0 && cu_b < b0 + 32) {
+            long long incl = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            cu_base = W + __shfl_sync(0xffffffffu, incl - w, cu_b - b0);
+            cu_pages = __shfl_sync(0xffffffffu, np, cu_b - b0);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
@@ -399,10 +465,19 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                                     ? W : static_cast<long long>(gridDim.x) * kWarps;
     // worker id, recomputed where needed so it does not hold registers
 #define FP8KV_WORKER (static_cast<long long>(blockIdx.x) * kWarps + warp)
-    if (FP8KV_WORKER >= n_workers) return;
+    volatile int* cta_flag = reinterpret_cast<volatile int*>(smem + C::kOffFlag);
+    if (!cta_mode && FP8KV_WORKER >= n_workers) return;
     // [resume, end) of the share lives in shared memory (kept out of registers)
     volatile long long* share = reinterpret_cast<volatile long long*>(smem + C::kOffShare) + 2 * warp;
-    if (lane == 0) {
+    if (cta_mode) {
+        if (lane == 0) {
+            const int cu_h = static_cast<int>(blockIdx.x) - cu_b * p.Hu;
+            const long long t0 = cu_base + static_cast<long long>(cu_h) * cu_pages;
+            share[0] = t0 + (static_cast<long long>(warp) * cu_pages) / kWarps;
+            share[1] = t0 + (static_cast<long long>(warp + 1) * cu_pages) / kWarps;
+            cta_flag[warp] = 0;
+        }
+    } else if (lane == 0) {
         // floor(w W / n) for w and w + 1 with one 64-bit division: W = q n + r,
         // so w W / n = w q + w r / n, and w r < 2^24 (w, r < 4096)
         const long long q = W / n_workers, r = W - q * n_workers;
@@ -619,6 +694,11 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
         const int dbase = perm8(g) * (D / 8);
         const size_t unit = static_cast<size_t>(ub) * p.Hu + uh;
         const size_t slot = static_cast<size_t>(FP8KV_WORKER) + unit;
+        // CTA units: a partial goes to this warp's ring (its streaming is over):
+        // O [Gu][D], then m [Gu], l [Gu]
+        float* cta_o = reinterpret_cast<float*>(ring);
+        float* cta_m = cta_o + Gu * D;
+        float* cta_l = cta_m + Gu;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int head0 = nt * 8 + 2 * c, head1 = head0 + 1;   // columns of the unit
@@ -642,22 +722,25 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                         store_out<BF16>(p.out, p.out_bf16, row * D + d, va);
                         store_out<BF16>(p.out, p.out_bf16, row * D + d + 1, vb);
                     } else {
-                        float* dst = p.ws_o + (slot * Gu + head) * D + d;
+                        float* dst = cta_mode ? cta_o + head * D + d : p.ws_o + (slot * Gu + head) * D + d;
                         *reinterpret_cast<float2*>(dst) = make_float2(va, vb);
                     }
                 }
             }
             if (!whole && g == 0) {
+                float* dm = cta_mode ? cta_m : p.ws_m + slot * Gu;
+                float* dl = cta_mode ? cta_l : p.ws_l + slot * Gu;
                 if (head0 < Gu) {
-                    p.ws_m[slot * Gu + head0] = mst[nt][0];
-                    p.ws_l[slot * Gu + head0] = l0;
+                    dm[head0] = mst[nt][0];
+                    dl[head0] = l0;
                 }
                 if (head1 < Gu) {
-                    p.ws_m[slot * Gu + head1] = mst[nt][1];
-                    p.ws_l[slot * Gu + head1] = l1;
+                    dm[head1] = mst[nt][1];
+                    dl[head1] = l1;
                 }
             }
         }
+        if (cta_mode && lane == 0) cta_flag[warp] = whole ? 2 : 1;
     };
 
     // ---- FUSED: the new token of unit (b, h) sits at position ctx - 1 on the
@@ -1114,6 +1197,14 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
         }
         jring += consumed;
     }
+    // ---- CTA units: combine the warps' partials of the CTA's unit (out of line,
+    //      so that it does not weigh on the streaming loop's registers)
+    if constexpr (CTA) {
+        pdl_wait();                       // (warps without pages have not waited yet)
+        __syncthreads();                  // every warp of the CTA gets here
+        cta_combine<D, BF16>(p, smem, C::kWarpSmem, C::kOffFlag);
+        pdl_trigger();                    // the next kernel may start: this grid is ending
+    }
 #undef FP8KV_WORKER
 }
 
@@ -1231,12 +1322,12 @@ __global__ void __launch_bounds__(512) split_merge_kernel(const DecodeParams p) 
     }
 }
 
-template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT>
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT, bool CTA>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          cudaStream_t stream) {
     using C = Cfg<D, BF16, NT, HPT>;
     constexpr int kSmemBytes = FUSED ? C::kSmemFused : C::kSmem;
-    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED, NT, HPT>;
+    auto kern = paged_decode_kernel<D, BF16, PER_TOKEN, FUSED, NT, HPT, CTA>;
     // opt in to the large dynamic shared-memory size once per context
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmemBytes, attr_done);
@@ -1254,7 +1345,7 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || CTA) return e;   // CTA units combine in the kernel
     // merge block: about 4 parts per warp at the launch's mean parts per unit,
     // 4 to 16 warps; at most 8 when there are more merge blocks than SMs (larger
     // blocks then hold SM slots the next decode grid, launched early, is
@@ -1273,13 +1364,22 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& kmap, const C
 
 // packed heads (p.hpt == 2) only where the host allows them: one 8-head group,
 // tiles of at most 2 KiB
+template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT, int HPT>
+cudaError_t dispatch_cta(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         cudaStream_t s) {
+    if constexpr (NT == 1) {                    // CTA units: one 8-column group
+        if (p.cta_units) return launch_split<D, BF16, PER_TOKEN, FUSED, NT, HPT, true>(p, kmap, vmap, s);
+    }
+    return launch_split<D, BF16, PER_TOKEN, FUSED, NT, HPT, false>(p, kmap, vmap, s);
+}
+
 template <int D, bool BF16, bool PER_TOKEN, bool FUSED, int NT>
 cudaError_t dispatch_hpt(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          cudaStream_t s) {
     if constexpr (NT == 1 && D * (BF16 ? 2 : 1) <= 128) {
-        if (p.hpt == 2) return launch_split<D, BF16, PER_TOKEN, FUSED, NT, 2>(p, kmap, vmap, s);
+        if (p.hpt == 2) return dispatch_cta<D, BF16, PER_TOKEN, FUSED, NT, 2>(p, kmap, vmap, s);
     }
-    return launch_split<D, BF16, PER_TOKEN, FUSED, NT, 1>(p, kmap, vmap, s);
+    return dispatch_cta<D, BF16, PER_TOKEN, FUSED, NT, 1>(p, kmap, vmap, s);
 }
 
 template <int D, bool FUSED, int NT>

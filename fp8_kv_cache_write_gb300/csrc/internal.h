@@ -49,6 +49,7 @@ struct DecodeParams {
     float scale_log2;            // softmax_scale * log2(e)
     int window;
     int num_splits;              // CTAs of the decode grid
+    int cta_units;               // 1: CTA u takes unit u whole (B * Hu CTAs), no split_merge
     int hpt;                     // KV heads per unit (decode_heads_per_unit)
     int Hu;                      // units per sequence, Hkv / hpt
     int Gu;                      // query heads per unit, G * hpt

@@ -1057,6 +1057,15 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 mx[nt][1] = fmaxf(mx[nt][1], fmaxf(z[nt][k][1], z[nt][k][3]));
             }
         }
+        // lazy running max: it moves only when a column's logits exceed it by
+        // 2^kLazy.  The running max is the same in the 8 lanes of a column, so one
+        // vote on the lanes' own logits tells whether any column needs it; only
+        // then are the columns' maxima reduced across lanes
+        bool move = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            move |= mx[nt][0] > mst[nt][0] + kLazy || mx[nt][1] > mst[nt][1] + kLazy;
+        if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -1064,7 +1073,6 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                 mx[nt][0] = fmaxf(mx[nt][0], __shfl_xor_sync(0xffffffffu, mx[nt][0], off));
                 mx[nt][1] = fmaxf(mx[nt][1], __shfl_xor_sync(0xffffffffu, mx[nt][1], off));
             }
-            // lazy running max: move it only when the group exceeds it by 2^kLazy
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 if (mx[nt][hh] > mst[nt][hh] + kLazy) {
@@ -1078,6 +1086,7 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
                     mst[nt][hh] = mx[nt][hh];
                 }
             }
+        }
         }
 
 #pragma unroll

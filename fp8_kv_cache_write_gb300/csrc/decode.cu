@@ -259,22 +259,37 @@ __device__ __noinline__ bool store_new_token_row(const int32_t* bt_row, int64_t 
                 ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, off));
                 va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, off));
             }
-            sk = __fdiv_rn(ka, 448.0f);
-            sv = __fdiv_rn(va, 448.0f);
+            sk = amax_over_448(ka);
+            sv = amax_over_448(va);
         } else {
             sk = ksc;
             sv = vsc;
         }
+        // codes of fp32(x / s): the cache writer's certified multiplies, and its
+        // IEEE divides for a pair they cannot certify
         uint16_t kc[kNE / 2], vc[kNE / 2];
+        auto encode = [](const float* x, float sc, uint16_t* code) {
+            if (sc == 0.0f) {                 // a zero scale stores code 0
 #pragma unroll
-        for (int i = 0; i < kNE / 2; ++i) {
-            kc[i] = sk != 0.0f ? e4m3x2_from_f32(__fdiv_rn(kf[2 * i], sk),
-                                                 __fdiv_rn(kf[2 * i + 1], sk))
-                               : uint16_t{0};
-            vc[i] = sv != 0.0f ? e4m3x2_from_f32(__fdiv_rn(vf[2 * i], sv),
-                                                 __fdiv_rn(vf[2 * i + 1], sv))
-                               : uint16_t{0};
-        }
+                for (int i = 0; i < kNE / 2; ++i) code[i] = 0;
+                return;
+            }
+            const uint32_t e = (__float_as_uint(sc) >> 23) & 0xffu;
+            const bool fast = e >= 1u && e <= 252u;
+            const float r = __fdividef(1.0f, sc);
+            const uint64_t rl = pack_f32x2(__fmul_rn(r, 1.0f - 0x1p-19f), __fmul_rn(r, 1.0f - 0x1p-19f));
+            const uint64_t rh = pack_f32x2(__fmul_rn(r, 1.0f + 0x1p-19f), __fmul_rn(r, 1.0f + 0x1p-19f));
+#pragma unroll
+            for (int i = 0; i < kNE / 2; ++i) {
+                const uint64_t x2 = pack_f32x2(x[2 * i], x[2 * i + 1]);
+                const uint32_t lo = e4m3x2_from_f32x2(mul_f32x2(x2, rl));
+                const uint32_t hi = e4m3x2_from_f32x2(mul_f32x2(x2, rh));
+                code[i] = fast && lo == hi ? static_cast<uint16_t>(lo)
+                                           : e4m3x2_by_divide(x[2 * i], x[2 * i + 1], sc);
+            }
+        };
+        encode(kf, sk, kc);
+        encode(vf, sv, vc);
         memcpy(&kst, kc, kLB);
         memcpy(&vst, vc, kLB);
     }

@@ -484,7 +484,13 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
                               int out_dtype, int32_t* err_flag, void* cuda_stream) {
     g_warning.clear();
     int64_t max_ctas = 0;
-    if (num_splits == 0 && Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 && valid_d(D)) {
+    Plan cta;                                    // a short sliding window needs no scratch
+    const bool cta_units = Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 && valid_d(D) &&
+                           plan(B, Hq, Hkv, D, max_blocks_per_seq, window, num_splits, &cta) ==
+                               FP8KV_OK &&
+                           cta.cta_units;
+    if (num_splits == 0 && !cta_units && Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && B > 0 &&
+        valid_d(D)) {
         // slots that fit, less the one per unit, over the 4 worker warps of a CTA
         // (a worker's slot holds hpt KV heads' query heads, as the planner sizes it)
         const int hpt = decode_heads_per_unit(D, FP8KV_KV_E4M3, Hq / Hkv, Hkv, B);

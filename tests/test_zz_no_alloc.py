@@ -117,3 +117,16 @@ def test_noalloc_rejects_a_batch_whose_unit_slots_alone_exceed_the_array():
             torch.zeros(B, 4, dtype=torch.int32, device="cuda"),
             torch.zeros(B, dtype=torch.int32, device="cuda"), kv_dtype=0, scale_mode=0,
             k_scale=one, v_scale=one, out=torch.empty(B, Hq, D, device="cuda"))
+
+
+def test_noalloc_sliding_window_uses_no_scratch():
+    # a sliding window of at most 16 visible pages takes one CTA per unit that
+    # combines in shared memory: no scratch, and no limit from the unit slots
+    w = synth.hybrid_layer(layer=0)
+    c = gpu_fill(w, fk.KV_BF16)
+    want = gpu_decode(w, c).cpu().numpy()
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+    for _ in range(2):
+        got = _noalloc_call(w, c, out).cpu().numpy()
+        np.testing.assert_allclose(got, want, rtol=RTOL, atol=ATOL)
+

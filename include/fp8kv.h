@@ -112,8 +112,15 @@ int fp8kv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mappi
  *   max_blocks_per_seq  columns of block_table (upper bound on pages per sequence)
  *   window              0 = full attention, else the last `window` keys
  *   num_splits          0 = choose automatically, else the requested split count
- *   *num_splits_out     the split count the kernel will use
+ *   *num_splits_out     the split count the kernel will use (CTAs of its grid)
  *   *workspace_bytes_out  bytes of workspace needed (split partials)
+ * Automatic plans: one wave of CTAs over all (sequence, KV head, page) tiles,
+ * with partials merged by a second kernel; a sliding window of at most 16
+ * visible pages per sequence instead takes one CTA per (sequence, KV head)
+ * unit that combines its warps' partials itself (workspace_bytes_out 16).  With
+ * 2 or 4 query heads per KV head, an even Hkv, rows of at most 128 bytes and
+ * B * Hkv >= 32, a unit is two adjacent KV heads; the workspace is sized for
+ * that (an upper bound for the bf16 cache too).
  */
 int fp8kv_decode_plan(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int window,
                       int num_splits, int* num_splits_out, size_t* workspace_bytes_out);
@@ -280,7 +287,8 @@ int fp8kv_quantize_e4m3(const float* x, float scale, uint8_t* out, int64_t n,
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  The caller still passes q, the caches, the tables and `out`.
  *   - num_splits 0: the automatic plan, lowered to the largest CTA count whose
- *     partials fit the array.  If not even one CTA fits (one slot per
+ *     partials fit the array (a short sliding window needs none of it: its
+ *     plan combines inside each CTA).  If not even one CTA fits (one slot per
  *     (sequence, KV head) unit alone, B * Hq * (D + 2) * 4 bytes, exceeds the
  *     array), or an explicit num_splits plan (fp8kv_decode_plan) needs more
  *     than the array holds, the call returns FP8KV_ERR_WORKSPACE and launches

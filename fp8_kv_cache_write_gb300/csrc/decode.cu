@@ -417,8 +417,9 @@ __global__ void __launch_bounds__(kWarps * 32, decode_min_ctas<D, BF16, NT>())
     // h HPT .. h HPT + HPT - 1), first page, end page, flags (2: starts the unit,
     // 4: ends it), visible positions [lo, ctx)
 
-    // ---- this warp's equal share [t0, t1) of the launch's W (seq, KV head, page)
-    //      tiles; every warp is an independent worker (no block-wide barrier)
+    // ---- this warp's equal share [t0, t1) of the launch's W (seq, unit, page)
+    //      tiles; every warp is an independent worker (no block-wide barrier but
+    //      the one that ends a CTA-units launch)
     if (lane == 0) {                      // ring barriers (their fences overlap the loads below)
         // lane copies: every lane arrives once per stage; TMA: lane 0 only
         for (int s = 0; s < C::kStages; ++s)

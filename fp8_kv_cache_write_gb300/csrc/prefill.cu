@@ -27,10 +27,11 @@
 //
 // Design (GB300):
 //   * one CTA per (tile of 128 / G query tokens x the G query heads of a KV
-//     head) = 128 MMA rows; softmax warps own one row each per thread (softmax,
-//     P quantization, rescale, epilogue), two loader warps issue TMA (K tiles,
-//     V tiles), one warp allocates tensor memory and issues the MMAs from one
-//     thread.
+//     head) = 128 MMA rows; a softmax thread owns one row and one part of every
+//     tile's keys and of O's columns (two parts, four with per-token-head
+//     scales; the parts' row maxima and sums meet in shared memory), two
+//     loader warps issue TMA (K tiles, V tiles), one warp allocates tensor
+//     memory and issues the MMAs from one thread.
 //   * per KV tile (128 keys single, 64 keys split): S = Q8 K^T (kind::f8f6f4, M
 //     128, N = keys, K = D in steps of 32) into TMEM; softmax reads S with
 //     tcgen05.ld, writes P8 (e4m3) to shared memory; O += P8 V (M 128, N = D,
@@ -77,7 +78,7 @@ struct Soft {
     static constexpr float kLift = SPLIT ? 256.f : (PT ? 32.f : 1.f);
 };
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool PT>
 struct PCfg {
     // e4m3 tiles hold 128 keys (8 pages), bf16 and split tiles 64 keys (4 pages):
     // every P row is 128 bytes (bf16: 64 weights; split: 64 hi + 64 lo weights)
@@ -106,20 +107,24 @@ struct PCfg {
     // e4m3 only: 16 x 128-byte rows of 1.0 (the bf16 D 256 tiles leave no room)
     static constexpr int kOffOnes = kOffP + 2 * kPBytes;
     static constexpr int kOffOnes2 = kOffOnes + (BF16 ? 0 : 16 * 128);
-    // softmax warps: two per row quarter, each on half of a tile's keys (the
-    // row maxima meet in shared memory), except bf16 D 256 whose tiles leave
-    // no shared memory for that exchange (one warp per quarter)
-    static constexpr int kHalves = (BF16 && D == 256) ? 1 : 2;
-    static constexpr int kSoftWarps = 4 * kHalves;
+    // softmax warps: kParts per row quarter, each on a contiguous part of a
+    // tile's keys and of O's columns (the row maxima and sums meet in shared
+    // memory).  Two, except: per-token-head scales, whose column factors make
+    // the softmax the longest stage, take four (32 keys of a single tile, 16 of
+    // a split one) so that four warps per scheduler hide each other's
+    // latencies; bf16 at D 256 takes one (its tiles leave no shared memory for
+    // the exchange).
+    static constexpr int kParts = (BF16 && D == 256) ? 1 : (PT ? 4 : 2);
+    static constexpr int kSoftWarps = 4 * kParts;
     static constexpr int kThreads = 32 * (kSoftWarps + 3);   // + K loader, MMA, V loader
-    static constexpr int kOffPMax = kOffOnes2;               // [2][kHalves][128] partial maxima
-    // split: per row, 2^-e of the row's Q scaling, then the halves' |q| maxima [2][128]
-    static constexpr int kOffRow = kOffPMax + (kHalves == 2 ? 2 * 2 * kRows * 4 : 0);
-    static constexpr int kRowBytes = SPLIT ? 3 * kRows * 4 : 0;
+    static constexpr int kOffPMax = kOffOnes2;               // [2][kParts][128] partial maxima
+    // split: per row, 2^-e of the row's Q scaling, then the parts' |q| maxima [kParts][128]
+    static constexpr int kOffRow = kOffPMax + (kParts > 1 ? 2 * kParts * kRows * 4 : 0);
+    static constexpr int kRowBytes = SPLIT ? (1 + kParts) * kRows * 4 : 0;
     static constexpr int kOffBar = kOffRow + kRowBytes;
     static constexpr int kNumBars = 20;
     // per-token-head scales (e4m3 only): 4 slots of [k scales][v scales] of a
-    // tile (128 floats each), then the halves' V-scale maxima [2][2]
+    // tile (128 floats each), then the parts' V-scale maxima [2][kParts]
     static constexpr int kOffScl = kOffBar + kNumBars * 8;
     static constexpr int kSclBytes = BF16 ? 0 : 4 * 1024 + 16 * 4;
     static constexpr int kOffMisc = kOffScl + kSclBytes;    // tmem slot, abort flag
@@ -129,18 +134,24 @@ struct PCfg {
     static constexpr int kOffPtf = (kOffMisc + 16 + 15) / 16 * 16;
     static constexpr int kPtfBytes = BF16 ? 0 : kSoftWarps * 128 * 4;
     static constexpr int kSmem = 1024 + kOffPtf + kPtfBytes;
-    static_assert(kKeys / kHalves % 32 == 0, "a half tile is a whole number of 32-key loads");
+    static_assert(kKeys / kParts % 16 == 0, "a part is a whole number of 16-key loads");
+    static_assert(D / kParts % 16 == 0, "a part of O is a whole number of 16-column loads");
+    static_assert(2 * kParts <= 16, "the V-scale maxima fit their slot");
+    static_assert(kSmem <= 227 * 1024, "one CTA's shared memory fits an SM");
 };
 
 // Dynamic shared memory of the kernel: the larger of its two operand layouts.
-template <int D, bool BF16>
+template <int D, bool BF16, bool PT>
 constexpr int prefill_smem() {
-    static_assert(PCfg<D, BF16, false>::kPanelB == 128 || PCfg<D, BF16, false>::kPanelB == 64,
-                  "panel rows of 64 or 128 bytes");
-    return BF16 ? PCfg<D, true, false>::kSmem
-                : (PCfg<D, false, false>::kSmem > PCfg<D, false, true>::kSmem
-                       ? PCfg<D, false, false>::kSmem
-                       : PCfg<D, false, true>::kSmem);
+    using C1 = PCfg<D, BF16, false, PT>;
+    static_assert(C1::kPanelB == 128 || C1::kPanelB == 64, "panel rows of 64 or 128 bytes");
+    if constexpr (BF16) {
+        return C1::kSmem;
+    } else {
+        using C2 = PCfg<D, false, true, PT>;
+        static_assert(C1::kThreads == C2::kThreads, "single and split bodies run in one launch");
+        return C1::kSmem > C2::kSmem ? C1::kSmem : C2::kSmem;
+    }
 }
 
 // barrier indices
@@ -230,10 +241,10 @@ template <int D, bool TWO_LEVEL, bool BF16, bool PT, bool SPLIT>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                              const PrefillParams& p, uint8_t* smem,
                                              const CtaGeo& cg) {
-    using C = PCfg<D, BF16, SPLIT>;
+    using C = PCfg<D, BF16, SPLIT, PT>;
     using S = Soft<SPLIT, PT>;
     constexpr int kKeys = C::kKeys;
-    constexpr int kHalves = C::kHalves;
+    constexpr int kParts = C::kParts;
     constexpr int kSoft = 32 * C::kSoftWarps;          // softmax threads
     // K and V tiles come from two loader warps: a single warp issuing every copy
     // of a tile held the pipeline back
@@ -268,7 +279,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
         mbar_init(bar(kPvDone1), 1);
         mbar_init(bar(kPvtFree), kSoft);
         mbar_init(bar(kMmaIdle), 1);
-        for (int i = 0; i < 4; ++i) mbar_init(bar(kPair0 + i), 64);   // the two warps of a quarter
+        for (int i = 0; i < 4; ++i) mbar_init(bar(kPair0 + i), 32 * kParts);   // a quarter's warps
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -278,13 +289,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
     //   single: e4m3(q / q_scale); bf16: q itself;
     //   split:  hi = e4m3(q 2^e_r), lo = e4m3(q 2^e_r - hi), with 2^e_r putting the
     //           row's max |q| into [128, 256) (exact scaling; 2^-e_r goes to the logits)
-    float* rowinfo = reinterpret_cast<float*>(smem + C::kOffRow);   // split: [3][128]
+    float* rowinfo = reinterpret_cast<float*>(smem + C::kOffRow);   // split: [1 + kParts][128]
     if (warp < C::kSoftWarps) {
         const int r = tid & (kRows - 1);
-        const int half = tid / kRows;                   // which chunks of the row
+        const int part = tid / kRows;                   // which chunks of the row
         const int tk = tok0 + r / G, head = r % G;
         uint8_t* qtile = smem + C::kOffQ;
-        constexpr int kChunks = C::kRowB / 16 / kHalves;
+        constexpr int kChunks = C::kRowB / 16 / kParts;
+        static_assert(C::kRowB / 16 % kParts == 0, "the Q row's chunks split evenly");
         const __nv_bfloat16* qrow =
             p.q + (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D;
         float qmul = 1.f;                               // split: 2^e_r
@@ -292,7 +304,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             float amax = 0.f;
             if (tk < nq) {
 #pragma unroll 4
-                for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
+                for (int c = part * kChunks; c < (part + 1) * kChunks; ++c) {
                     const uint4 a = *reinterpret_cast<const uint4*>(qrow + c * 16);
                     const uint4 bq = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
                     const uint32_t in[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
@@ -303,9 +315,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                     }
                 }
             }
-            rowinfo[kRows + half * kRows + r] = amax;
+            rowinfo[kRows + part * kRows + r] = amax;
             soft_sync(kSoft);
-            amax = fmaxf(rowinfo[kRows + r], rowinfo[2 * kRows + r]);
+#pragma unroll
+            for (int o = 0; o < kParts; ++o) amax = fmaxf(amax, rowinfo[kRows + o * kRows + r]);
             int e = 0;
             if (amax > 0.f) {
                 int ex;
@@ -314,10 +327,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 e = e > 120 ? 120 : (e < -120 ? -120 : e);
             }
             qmul = exp2i(e);
-            if (half == 0) rowinfo[r] = exp2i(-e);
+            if (part == 0) rowinfo[r] = exp2i(-e);
         }
 #pragma unroll 4
-        for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {   // 16-byte chunks
+        for (int c = part * kChunks; c < (part + 1) * kChunks; ++c) {   // 16-byte chunks
             uint32_t w[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
             if (tk < nq) {
                 const __nv_bfloat16* src = qrow + c * (16 / C::kElem);
@@ -544,19 +557,21 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
         __syncwarp();
     } else {
         // =============================== softmax / correction / epilogue
-        // row r of TMEM lane quarter warp % 4; key half kh of every tile (columns
+        // row r of TMEM lane quarter warp % 4; key part kh of every tile (columns
         // [kh * kKH, (kh + 1) * kKH)) and of O's columns
         const int r = 32 * (warp & 3) + lane;
         const int kh = warp / 4;
-        constexpr int kKH = kKeys / kHalves;            // keys of a tile this thread owns
-        constexpr int kDH = D / kHalves;                // O columns this thread owns
+        constexpr int kKH = kKeys / kParts;             // keys of a tile this thread owns
+        constexpr int kDH = D / kParts;                 // O columns this thread owns
+        constexpr int kSW = kKH >= 32 ? 32 : kKH;       // columns of one S load
+        constexpr int kCW = kDH >= 32 ? 32 : kDH;       // columns of one O load / store
         const int tk = tok0 + r / G;
         const bool row_ok = tk < nq;
         const int pos_r = row_ok ? pos_base + tk : -1;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        float* pmax = reinterpret_cast<float*>(smem + C::kOffPMax);   // [2][kHalves][128]
+        float* pmax = reinterpret_cast<float*>(smem + C::kOffPMax);   // [2][kParts][128]
         int pair_phase = 0;
-        // the two warps of a quarter meet (an mbarrier with a bounded wait, so a
+        // the warps of a quarter meet (an mbarrier with a bounded wait, so a
         // stuck partner ends in FP8KV_ERR_TIMEOUT rather than a hang)
         auto pair_sync = [&]() -> bool {
             mbar_arrive(bar(kPair0 + (warp & 3)));
@@ -590,8 +605,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
         const float llift = log2f(lift);
         // PT: running power-of-two bound of the V scales folded into the weights
         float e_run = 0.f;
-        float* ebuf = reinterpret_cast<float*>(smem + C::kOffScl + 4 * 1024);   // [2][2]
-        float m = kMaxInitP, l = 0.f;                  // l: this half's keys (summed at the end)
+        float* ebuf = reinterpret_cast<float*>(smem + C::kOffScl + 4 * 1024);   // [2][kParts]
+        float m = kMaxInitP, l = 0.f;                  // l: this part's keys (summed at the end)
         bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
             const int st = j & 1;
@@ -600,12 +615,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 break;
             }
             tc_fence_after();
-            uint32_t sb[kKH];                   // raw S of this row's half: all loads, one wait
+            uint32_t sb[kKH];                   // raw S of this row's part: all loads, one wait
 #pragma unroll
-            for (int cch = 0; cch < kKH / 32; ++cch) {
-                uint32_t* dst = sb + cch * 32;
-                tmem_ld32(tmem + lane_addr + kh * kKH + cch * 32,
-                          *reinterpret_cast<uint32_t(*)[32]>(dst));
+            for (int cch = 0; cch < kKH / kSW; ++cch) {
+                uint32_t* dst = sb + cch * kSW;
+                tmem_ld_n<kSW>(tmem + lane_addr + kh * kKH + cch * kSW,
+                               *reinterpret_cast<uint32_t(*)[kSW]>(dst));
             }
             tmem_wait_ld();
             tc_fence_before();
@@ -624,25 +639,39 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             const float* ksl = reinterpret_cast<const float*>(smem + C::kOffScl + (j & 3) * 1024) +
                                kh * kKH;
             const float* vsl = ksl + 128;
-            // PT: this warp's column factors (every lane of the warp works on this half)
+            // PT: this warp's column factors (every lane of the warp works on this part)
             float* ptf = reinterpret_cast<float*>(smem + C::kOffPtf) + warp * 128;
             if constexpr (PT) {
                 __syncwarp();                   // the previous tile's factors are read
 #pragma unroll
                 for (int i = lane; i < kKH; i += 32) ptf[i] = ksl[i] * scol;
                 __syncwarp();
+                // the factors come as 16-byte broadcast loads (four keys each)
+                const float4* ptf4 = reinterpret_cast<const float4*>(ptf);
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < kKH; ++i) {
-                        s[i] = __uint_as_float(sb[i]) * ptf[i];
-                        mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                    for (int i4 = 0; i4 < kKH / 4; ++i4) {
+                        const float4 f4 = ptf4[i4];
+                        const float fk[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = 4 * i4 + u;
+                            s[i] = __uint_as_float(sb[i]) * fk[u];
+                            mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                        }
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < kKH; ++i) {
-                        s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) * ptf[i]
-                                                 : -__int_as_float(0x7f800000);
-                        mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                    for (int i4 = 0; i4 < kKH / 4; ++i4) {
+                        const float4 f4 = ptf4[i4];
+                        const float fk[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = 4 * i4 + u;
+                            s[i] = key0 + i <= pos_r ? __uint_as_float(sb[i]) * fk[u]
+                                                     : -__int_as_float(0x7f800000);
+                            mxp[i & 7] = fmaxf(mxp[i & 7], s[i]);
+                        }
                     }
                 }
             } else if (full) {
@@ -660,25 +689,29 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             }
             float mx_raw = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-            float vmax = 0.f;                   // PT: this half's largest V scale
+            float vmax = 0.f;                   // PT: this part's largest V scale
             if constexpr (PT) {
-                // every lane of the warp works on this half: the lanes share the
+                // every lane of the warp works on this part: the lanes share the
                 // keys with written scales and meet in a shuffle reduction
                 const int nval = min(ctx - key0, kKH);
                 for (int i = lane; i < nval; i += 32) vmax = fmaxf(vmax, vsl[i]);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-                ebuf[st * 2 + kh] = vmax;       // every thread of the half: the same value
+                ebuf[st * kParts + kh] = vmax;  // every thread of the part: the same value
             }
-            if constexpr (kHalves == 2) {       // the row's max over both halves
-                pmax[(st * 2 + kh) * kRows + r] = mx_raw;
+            if constexpr (kParts > 1) {         // the row's max over every part
+                pmax[(st * kParts + kh) * kRows + r] = mx_raw;
                 if (!pair_sync()) {
                     ok = false;
                     break;
                 }
-                mx_raw = fmaxf(mx_raw, pmax[(st * 2 + (kh ^ 1)) * kRows + r]);
-                if constexpr (PT) vmax = fmaxf(vmax, ebuf[st * 2 + (kh ^ 1)]);
+#pragma unroll
+                for (int o = 1; o < kParts; ++o) {
+                    const int ko = (kh + o) % kParts;
+                    mx_raw = fmaxf(mx_raw, pmax[(st * kParts + ko) * kRows + r]);
+                    if constexpr (PT) vmax = fmaxf(vmax, ebuf[st * kParts + ko]);
+                }
             }
             const float mx = mx_raw * rf;
             float beta = 1.f;                   // PT: O's factor when the V bound grows
@@ -690,7 +723,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 }
             }
             float alpha = 1.f;
-            if (mx > m + S::kLazy) {            // lazy running max (the same in both halves)
+            if (mx > m + S::kLazy) {            // lazy running max (the same in every part)
                 alpha = ex2p(m - mx);
                 m = mx;
                 l *= alpha;
@@ -706,22 +739,22 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                     break;
                 }
                 tc_fence_after();
-                // this half's O columns, and l's columns (tensor-core l) in half 0
-                constexpr int kChunks = kDH / 32;
+                // this part's O columns, and l's columns (tensor-core l) in part 0
+                constexpr int kChunks = kDH / kCW;
 #pragma unroll 1
                 for (int cch = 0; cch < kChunks + ((kLMma) ? 1 : 0); ++cch) {
                     if (cch == kChunks && kh != 0) break;
-                    uint32_t rr[32];
+                    uint32_t rr[kCW];
                     const uint32_t ta = tmem + lane_addr +
-                                        (cch < kChunks ? kOCol + kh * kDH + cch * 32 : kLCol);
-                    tmem_ld32(ta, rr);
+                                        (cch < kChunks ? kOCol + kh * kDH + cch * kCW : kLCol);
+                    tmem_ld_n<kCW>(ta, rr);
                     tmem_wait_ld();
                     // O takes alpha and beta; the tensor-core l (not PT) only alpha
                     const float fo = cch < kChunks ? alpha * beta : alpha;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < kCW; ++i)
                         rr[i] = __float_as_uint(__uint_as_float(rr[i]) * fo);
-                    tmem_st32(ta, rr);
+                    tmem_st_n<kCW>(ta, rr);
                 }
                 tmem_wait_st();
             }
@@ -734,7 +767,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             }
             uint8_t* prow = smem + C::kOffP + st * C::kPBytes + r * 128;
             constexpr int kPerChunk = 16 / C::kElem;    // keys per 16-byte chunk
-            constexpr int kMyChunks = kKH / kPerChunk;  // this half's chunks of the row
+            constexpr int kMyChunks = kKH / kPerChunk;  // this part's chunks of the row
+            static_assert(kKH % kPerChunk == 0, "a part is whole 16-byte chunks of P");
             // PT: weight = p * s_v * lift / E, the unfolded p into l
             const float vinv = PT && e_run > 0.f ? lift / e_run : 0.f;
             if constexpr (PT) {
@@ -758,8 +792,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                         l += pa + pb;
                         // masked keys: p = 0 and a stale scale that must not enter
                         const bool va = full || key0 + ia <= pos_r, vb = full || key0 + ib <= pos_r;
-                        wa = va ? pa * ptf[64 + ia] : 0.f;
-                        wb = vb ? pb * ptf[64 + ib] : 0.f;
+                        const float2 f2 = *reinterpret_cast<const float2*>(ptf + 64 + ia);
+                        wa = va ? pa * f2.x : 0.f;
+                        wb = vb ? pb * f2.y : 0.f;
                     } else {
                         wa = ex2p(fmaf(s[ia], rf, -moff));
                         wb = ex2p(fmaf(s[ib], rf, -moff));
@@ -824,7 +859,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
 
             if constexpr (TWO_LEVEL) {
                 // O_acc (fp32, TMEM columns [kOCol, kOCol + D)) = alpha * O_acc + P V of
-                // this tile; this half's columns
+                // this tile; this part's columns
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(bar(kPvDone0 + st), (j >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
@@ -832,18 +867,18 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int cch = 0; cch < kDH / 32; ++cch) {
-                    const int col = kh * kDH + cch * 32;
-                    uint32_t pv[32], acc[32];
-                    tmem_ld32(tmem + lane_addr + col, pv);
-                    if (j > 0) tmem_ld32(tmem + lane_addr + kOCol + col, acc);
+                for (int cch = 0; cch < kDH / kCW; ++cch) {
+                    const int col = kh * kDH + cch * kCW;
+                    uint32_t pv[kCW], acc[kCW];
+                    tmem_ld_n<kCW>(tmem + lane_addr + col, pv);
+                    if (j > 0) tmem_ld_n<kCW>(tmem + lane_addr + kOCol + col, acc);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < kCW; ++i) {
                         const float prev = j > 0 ? __uint_as_float(acc[i]) * (alpha * beta) : 0.f;
                         acc[i] = __float_as_uint(prev + __uint_as_float(pv[i]));
                     }
-                    tmem_st32(tmem + lane_addr + kOCol + col, acc);
+                    tmem_st_n<kCW>(tmem + lane_addr + kOCol + col, acc);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -865,12 +900,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 tmem_ld32(tmem + lane_addr + kLCol, rr);
                 tmem_wait_ld();
                 l = __uint_as_float(rr[0]);
-            } else if constexpr (kHalves == 2) {     // the two halves' sums
-                // through the buffer of tile n-2, which both warps have finished with
+            } else if constexpr (kParts > 1) {       // the parts' sums
+                // through the buffer of tile n-2, which every warp has finished with
                 const int lb = ((n_tiles - 1) & 1) ^ 1;
-                pmax[(lb * 2 + kh) * kRows + r] = l;
+                pmax[(lb * kParts + kh) * kRows + r] = l;
                 if (pair_sync()) {
-                    l += pmax[(lb * 2 + (kh ^ 1)) * kRows + r];
+#pragma unroll
+                    for (int o = 1; o < kParts; ++o)
+                        l += pmax[(lb * kParts + (kh + o) % kParts) * kRows + r];
                 } else {
                     ok = false;
                 }
@@ -881,23 +918,23 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             // of the value codes; PT: l sums p itself and O carries lift / E
             const float f = l > 0.f ? (PT ? e_run / lift : vconst) / l : 0.f;
             const int head = r % G;
-            for (int cch = 0; cch < kDH / 32; ++cch) {
-                const int col = kh * kDH + cch * 32;
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + kOCol + col, rr);
+            for (int cch = 0; cch < kDH / kCW; ++cch) {
+                const int col = kh * kDH + cch * kCW;
+                uint32_t rr[kCW];
+                tmem_ld_n<kCW>(tmem + lane_addr + kOCol + col, rr);
                 tmem_wait_ld();
                 if (row_ok) {
                     const size_t o = (static_cast<size_t>(q0 + tk) * p.Hq + h * G + head) * D + col;
                     if (p.out_bf16) {
                         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2)
+                        for (int i = 0; i < kCW; i += 2)
                             *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(
                                 __uint_as_float(rr[i]) * f, __uint_as_float(rr[i + 1]) * f);
                     } else {
                         float* dst = reinterpret_cast<float*>(p.out) + o;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
+                        for (int i = 0; i < kCW; i += 4)
                             *reinterpret_cast<float4*>(dst + i) = make_float4(
                                 __uint_as_float(rr[i]) * f, __uint_as_float(rr[i + 1]) * f,
                                 __uint_as_float(rr[i + 2]) * f, __uint_as_float(rr[i + 3]) * f);
@@ -916,7 +953,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
 }
 
 template <int D, bool TWO_LEVEL, bool BF16, bool PT>
-__global__ void __launch_bounds__(PCfg<D, BF16, false>::kThreads, 1)
+__global__ void __launch_bounds__(PCfg<D, BF16, false, PT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -948,17 +985,17 @@ __global__ void __launch_bounds__(PCfg<D, BF16, false>::kThreads, 1)
         return;
     }
     if constexpr (BF16) {
-        cg.n_tiles = pos_max / PCfg<D, true, false>::kKeys + 1;
+        cg.n_tiles = pos_max / PCfg<D, true, false, false>::kKeys + 1;   // bf16: no PT
         prefill_body<D, TWO_LEVEL, true, PT, false>(kmap, vmap, p, smem, cg);
     } else {
         // split operands where a row of the CTA sees fewer than kSplitKeys keys
         const bool split = p.split == FP8KV_PREFILL_SPLIT_ALWAYS ||
                            (p.split == 0 && pos_min + 1 < kSplitKeys);
         if (split) {
-            cg.n_tiles = pos_max / PCfg<D, false, true>::kKeys + 1;
+            cg.n_tiles = pos_max / PCfg<D, false, true, PT>::kKeys + 1;
             prefill_body<D, TWO_LEVEL, false, PT, true>(kmap, vmap, p, smem, cg);
         } else {
-            cg.n_tiles = pos_max / PCfg<D, false, false>::kKeys + 1;
+            cg.n_tiles = pos_max / PCfg<D, false, false, PT>::kKeys + 1;
             prefill_body<D, TWO_LEVEL, false, PT, false>(kmap, vmap, p, smem, cg);
         }
     }
@@ -968,12 +1005,12 @@ template <int D, bool TWO, bool BF16, bool PT>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
     auto kern = prefill_kernel<D, TWO, BF16, PT>;
-    constexpr int kSmem = prefill_smem<D, BF16>();
+    constexpr int kSmem = prefill_smem<D, BF16, PT>();
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmem, attr_done);
     if (e != cudaSuccess) return e;
     dim3 grid(grid_x, p.Hkv, p.B);
-    kern<<<grid, PCfg<D, BF16, false>::kThreads, kSmem, stream>>>(kmap, vmap, p);
+    kern<<<grid, PCfg<D, BF16, false, PT>::kThreads, kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 

@@ -32,7 +32,8 @@ STATUS = {0: "FP8KV_OK", -1: "FP8KV_ERR_INVALID", -2: "FP8KV_ERR_UNSUPPORTED",
           -6: "FP8KV_ERR_BAD_INDEX"}
 
 EXPORTS = ("fp8kv_kv_cache_write", "fp8kv_decode_plan", "fp8kv_paged_decode_attn",
-           "fp8kv_decode_step", "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn", "fp8kv_quantize_e4m3",
+           "fp8kv_decode_step", "fp8kv_paged_decode_attn_noalloc", "fp8kv_prefill_attn",
+           "fp8kv_prefill_attn_ws", "fp8kv_prefill_workspace_bytes", "fp8kv_quantize_e4m3",
            "fp8kv_resolve_scales", "fp8kv_status_string", "fp8kv_last_warning")
 NOALLOC_DECODE_SCRATCH_BYTES = 8 << 20
 
@@ -83,6 +84,12 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_prefill_attn.argtypes = [P, P, i32, P, P, i32, i32, P, P, P, P, f32, f32, P, i32, P,
                                          i32, i32, i32, i32, i64, f32, i32, P, i32, P, P]
         L.fp8kv_prefill_attn.restype = i32
+        L.fp8kv_prefill_attn_ws.argtypes = [P, P, i32, P, P, i32, i32, P, P, P, P, f32, f32, P,
+                                            i32, P, i32, i32, i32, i32, i64, f32, i32, P, sz, P,
+                                            i32, P, P]
+        L.fp8kv_prefill_attn_ws.restype = i32
+        L.fp8kv_prefill_workspace_bytes.argtypes = [i32, ctypes.POINTER(sz)]
+        L.fp8kv_prefill_workspace_bytes.restype = i32
         L.fp8kv_quantize_e4m3.argtypes = [P, f32, P, i64, P]
         L.fp8kv_quantize_e4m3.restype = i32
         FP = ctypes.POINTER(f32)
@@ -294,14 +301,41 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, *,
     return out
 
 
+def prefill_workspace_bytes(D):
+    """Bytes of the workspace fp8kv_prefill_attn_ws takes at head_dim D."""
+    n = ctypes.c_size_t(0)
+    _raise(lib().fp8kv_prefill_workspace_bytes(int(D), ctypes.byref(n)), "prefill_workspace_bytes")
+    return n.value
+
+
+# zero-filled prefill workspaces, one per (device, stream, D): the kernel leaves
+# its counters zero after each call, and calls on one stream never overlap
+_prefill_ws = {}
+
+
+def prefill_workspace(device, stream, D):
+    """The cached zero-initialised workspace prefill_attn uses on `stream` (a
+    torch stream; None: the current one)."""
+    key = (torch.device(device).index, _stream(stream).value or 0, int(D))
+    ws = _prefill_ws.get(key)
+    if ws is None:
+        ws = torch.zeros(prefill_workspace_bytes(D), dtype=torch.uint8, device=device)
+        _prefill_ws[key] = ws
+    return ws
+
+
 def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, context_lens,
                  *, kv_dtype=KV_E4M3, scale_mode=SCALE_PER_TENSOR, k_scale=None, v_scale=None,
                  k_scale_cache=None, v_scale_cache=None, q_scale=1.0, prob_scale=1.0,
                  softmax_scale=None, two_level=False, split="auto", out=None, out_dtype=OUT_F32,
-                 err_flag=None, stream=None):
+                 err_flag=None, stream=None, workspace="auto"):
     """Chunked causal FP8 prefill of q [Tq][Hq][D] (bf16) over the paged cache;
     returns out [Tq][Hq][D].  split: "auto" (split e4m3 operands for blocks of
-    rows under 8192 keys), "always" or "never".  See fp8kv_prefill_attn."""
+    rows under 8192 keys), "always" or "never".  workspace: "auto" (a cached
+    zeroed workspace per device and stream, so that launches with more query
+    tiles than SMs run balanced over persistent CTAs), a zeroed uint8 tensor of
+    prefill_workspace_bytes(D), or None (one CTA per query tile).  See
+    fp8kv_prefill_attn and fp8kv_prefill_attn_ws."""
     if split not in ("auto", "always", "never"):
         raise ValueError("split: 'auto', 'always' or 'never'")
     flags = (PREFILL_TWO_LEVEL if two_level else 0) | {
@@ -323,12 +357,18 @@ def prefill_attn(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, block_table, c
         out = torch.empty(Tq, Hq, D, device=q.device,
                           dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
     _check(out, "out", torch.float32 if out_dtype == OUT_F32 else torch.bfloat16)
-    st = lib().fp8kv_prefill_attn(
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace: 'auto', a uint8 tensor or None")
+        workspace = prefill_workspace(q.device, stream, D)
+    _check(workspace, "workspace", torch.uint8)
+    st = lib().fp8kv_prefill_attn_ws(
         _ptr(q), _ptr(cu_seqlens_q), int(max_seqlen_q), _ptr(k_cache), _ptr(v_cache), kv_dtype,
         scale_mode, _ptr(k_scale), _ptr(v_scale), _ptr(k_scale_cache), _ptr(v_scale_cache),
         float(q_scale), float(prob_scale),
         _ptr(block_table), block_table.shape[1], _ptr(context_lens), cu_seqlens_q.numel() - 1,
-        Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), flags, _ptr(out),
+        Hq, Hkv, D, k_cache.shape[0], float(softmax_scale), flags, _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _ptr(out),
         out_dtype, _ptr(err_flag), _stream(stream))
     _raise(st, "prefill_attn")
     return out

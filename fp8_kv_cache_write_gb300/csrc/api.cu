@@ -509,6 +509,21 @@ int paged_decode_attn_fitting(const void* q, const void* k_cache, const void* v_
 
 }  // namespace fp8kv
 
+namespace {
+
+// Persistent prefill workspace: a counter per CTA (padded to 256 bytes), then
+// two partial slots per CTA of [128][D + 2] floats.
+size_t prefill_ws_count_bytes(int n_ctas) {
+    return (static_cast<size_t>(n_ctas) * 4 + 255) / 256 * 256;
+}
+
+size_t prefill_ws_bytes(int D, int n_ctas) {
+    return prefill_ws_count_bytes(n_ctas) +
+           static_cast<size_t>(2) * n_ctas * 128 * (static_cast<size_t>(D) + 2) * 4;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp8kv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -544,6 +559,15 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
                         cuda_stream);
 }
 
+int fp8kv_prefill_workspace_bytes(int D, size_t* bytes) {
+    if (!bytes) return FP8KV_ERR_INVALID;
+    if (!valid_d(D)) return FP8KV_ERR_UNSUPPORTED;
+    const int n = sm_count();
+    if (n <= 0) return FP8KV_ERR_CUDA;
+    *bytes = prefill_ws_bytes(D, n);
+    return FP8KV_OK;
+}
+
 int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
                        const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
                        const float* k_scale, const float* v_scale, const float* k_scale_cache,
@@ -552,6 +576,22 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
                        const int32_t* context_lens, int B, int Hq, int Hkv, int D,
                        int64_t num_blocks, float softmax_scale, int flags, void* out,
                        int out_dtype, int32_t* err_flag, void* cuda_stream) {
+    return fp8kv_prefill_attn_ws(q, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, kv_dtype,
+                                 scale_mode, k_scale, v_scale, k_scale_cache, v_scale_cache,
+                                 q_scale, prob_scale, block_table, max_blocks_per_seq,
+                                 context_lens, B, Hq, Hkv, D, num_blocks, softmax_scale, flags,
+                                 nullptr, 0, out, out_dtype, err_flag, cuda_stream);
+}
+
+int fp8kv_prefill_attn_ws(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
+                          const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
+                          const float* k_scale, const float* v_scale,
+                          const float* k_scale_cache, const float* v_scale_cache, float q_scale,
+                          float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                          int64_t num_blocks, float softmax_scale, int flags, void* workspace,
+                          size_t workspace_bytes, void* out, int out_dtype, int32_t* err_flag,
+                          void* cuda_stream) {
     g_warning.clear();
     constexpr int kKnown =
         FP8KV_PREFILL_TWO_LEVEL | FP8KV_PREFILL_SPLIT_ALWAYS | FP8KV_PREFILL_SPLIT_NEVER;
@@ -614,7 +654,19 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
     p.out_bf16 = out_dtype == FP8KV_OUT_BF16;
     p.err = err_flag;
     const int tpt = 128 / G;
-    const int grid_x = (max_seqlen_q + tpt - 1) / tpt;
+    int grid_x = (max_seqlen_q + tpt - 1) / tpt;
+    // more query tiles than SMs and a workspace: a persistent CTA per SM with
+    // the key tiles split evenly (no partly filled last wave)
+    const int n_sm = sm_count();
+    if (workspace != nullptr && n_sm > 0 &&
+        static_cast<int64_t>(grid_x) * Hkv * B > n_sm) {
+        if (workspace_bytes < prefill_ws_bytes(D, n_sm)) return FP8KV_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;
+        p.ws_count = static_cast<int32_t*>(workspace);
+        p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                             prefill_ws_count_bytes(n_sm));
+        grid_x = n_sm;
+    }
     cudaError_t e = launch_prefill(p, kmap, vmap, D, kv_dtype, two_level, grid_x,
                                    static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return FP8KV_ERR_CUDA;

@@ -97,6 +97,11 @@ struct PrefillParams {
     void* out;                     // [Tq][Hq][D]
     int out_bf16;
     int32_t* err;
+    // balanced split over a persistent grid (null: one CTA per query tile): the
+    // partial of each cut piece, [2 * CTAs][128][D + 2] floats, and a counter
+    // per CTA (zero between calls)
+    float* ws_part;
+    int32_t* ws_count;
 };
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap,

@@ -127,11 +127,10 @@ struct PCfg {
     // tile (128 floats each), then the parts' V-scale maxima [2][kParts]
     static constexpr int kOffScl = kOffBar + kNumBars * 8;
     static constexpr int kSclBytes = BF16 ? 0 : 4 * 1024 + 16 * 4;
-    static constexpr int kOffMisc = kOffScl + kSclBytes;    // tmem slot, abort flag
     // per-token-head scales: each softmax warp's column factors of the current
     // tile, [64] for the logits (k scale x logit scale), [64] for the weights
     // (v scale / bound)
-    static constexpr int kOffPtf = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr int kOffPtf = (kOffScl + kSclBytes + 15) / 16 * 16;
     static constexpr int kPtfBytes = BF16 ? 0 : kSoftWarps * 128 * 4;
     static constexpr int kSmem = 1024 + kOffPtf + kPtfBytes;
     static_assert(kKeys / kParts % 16 == 0, "a part is a whole number of 16-key loads");
@@ -142,14 +141,15 @@ struct PCfg {
 
 // Dynamic shared memory of the kernel: the larger of its two operand layouts.
 template <int D, bool BF16, bool PT>
-constexpr int prefill_smem() {
+__host__ __device__ constexpr int prefill_smem() {
     using C1 = PCfg<D, BF16, false, PT>;
     static_assert(C1::kPanelB == 128 || C1::kPanelB == 64, "panel rows of 64 or 128 bytes");
     if constexpr (BF16) {
         return C1::kSmem;
     } else {
         using C2 = PCfg<D, false, true, PT>;
-        static_assert(C1::kThreads == C2::kThreads, "single and split bodies run in one launch");
+        static_assert(C1::kThreads == C2::kThreads && C1::kTmemCols == C2::kTmemCols,
+                      "single and split bodies run in one launch, on one allocation");
         return C1::kSmem > C2::kSmem ? C1::kSmem : C2::kSmem;
     }
 }
@@ -228,19 +228,26 @@ __device__ __forceinline__ void e4m3x2_split(float a, float b, uint32_t& hi, uin
     }
 }
 
-// Where a CTA sits: sequence b, KV head h, its query tokens and key range.
+// One piece of work: query tile (sequence b, KV head h, query tokens from tok0)
+// against key tiles t0 .. t0 + n_tiles - 1.
 struct CtaGeo {
     int b, h;
     int q0, nq;          // the sequence's first q row and chunk length
-    int tok0;            // this CTA's first query token (in the chunk)
+    int tok0;            // the tile's first query token (in the chunk)
     int ctx, pos_base;   // keys of the sequence; position of the chunk's first query
-    int n_tiles;         // key tiles the CTA's last row reaches
+    int t0, n_tiles;     // the key tiles taken (all of them: t0 = 0, n_tiles = the
+                         // tiles the tile's last row reaches)
+    float* part;         // null: write the output; else this piece's partial
+                         // (O times its output factor [128][D], then m, l [128])
 };
 
+// tmem_slot holds the CTA's tensor memory (allocated once by the kernel);
+// abort_flag is raised by a wait that gave up.
 template <int D, bool TWO_LEVEL, bool BF16, bool PT, bool SPLIT>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                              const PrefillParams& p, uint8_t* smem,
-                                             const CtaGeo& cg) {
+                                             const CtaGeo& cg, const uint32_t* tmem_slot,
+                                             volatile int* abort_flag) {
     using C = PCfg<D, BF16, SPLIT, PT>;
     using S = Soft<SPLIT, PT>;
     constexpr int kKeys = C::kKeys;
@@ -263,11 +270,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
     const int b = cg.b, h = cg.h, q0 = cg.q0, nq = cg.nq, tok0 = cg.tok0;
     const int ctx = cg.ctx, pos_base = cg.pos_base, n_tiles = cg.n_tiles;
     const int ctx_pages = (ctx + kPage - 1) / kPage;
+    auto tile_of = [&](int j) { return cg.t0 + j; };   // key tile of the j-th step
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
     if (tid == 0) {
         for (int i = kKFull0; i <= kVEmpty1; ++i) mbar_init(bar(i), 1);
@@ -283,7 +289,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
     // ---- Q tile(s) (K-major, 128-byte swizzle)
     //   single: e4m3(q / q_scale); bf16: q itself;
@@ -394,17 +399,18 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             const int pg = base + lane;
             return pg < ctx_pages ? bt_row[pg] : 0;
         };
-        int bt_base = 0;
-        int bt_cur = bt_load(0), bt_nxt = bt_load(32);
+        int bt_base = -64;                             // no batch loaded yet
+        int bt_cur = 0, bt_nxt = 0;
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
-            const int page0 = j * kPPT;
+            const int page0 = tile_of(j) * kPPT;
             int n_pages = ctx_pages - page0;
             n_pages = n_pages > kPPT ? kPPT : n_pages;
-            if (page0 >= bt_base + 32) {
-                bt_base += 32;
-                bt_cur = bt_nxt;
-                bt_nxt = bt_load(bt_base + 32);
+            if ((page0 & ~31) != bt_base) {
+                const int base = page0 & ~31;
+                bt_cur = base == bt_base + 32 ? bt_nxt : bt_load(base);
+                bt_base = base;
+                bt_nxt = bt_load(base + 32);
             }
             int blk = __shfl_sync(0xffffffffu, bt_cur, (page0 - bt_base + lane) & 31);
             int z = 0;
@@ -628,7 +634,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
 
             // causal mask on the raw logits (keys past ctx always masked), the row
             // max of raw S, then base-2 logits s * rf - m inside one FFMA below
-            const int key0 = j * kKeys + kh * kKH;
+            const int key0 = tile_of(j) * kKeys + kh * kKH;
             float s[kKH];
             float mxp[8];                       // 8 independent partial maxima
 #pragma unroll
@@ -837,7 +843,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
             }
             // value rows past ctx in the last tile hold unwritten cache slots (any
             // bytes, NaN codes included): zero them so 0 * v stays 0
-            if (j * kKeys + kKeys > ctx) {
+            if (tile_of(j) * kKeys + kKeys > ctx) {
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(bar(kVFull0 + st), (j >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
@@ -847,7 +853,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 for (int idx = tid; idx < kKeys * C::kPanels * C::kCPR; idx += kSoft) {
                     const int chunk = idx % C::kCPR, row = (idx / C::kCPR) % kKeys,
                               pn = (idx / C::kCPR) / kKeys;
-                    if (j * kKeys + row >= ctx)
+                    if (tile_of(j) * kKeys + row >= ctx)
                         *reinterpret_cast<uint4*>(vt + pn * (kKeys * C::kPanelB) +
                                                   row * C::kPanelB + chunk * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -913,7 +919,27 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                 }
             }
         }
-        if (ok) {
+        if (ok && cg.part != nullptr) {
+            // a piece of a split tile: O times its output factor, then m and l
+            // (the row's logits are base-2 numbers relative to m)
+            const float g = PT ? e_run / lift : vconst;
+            float* prow = cg.part + static_cast<size_t>(r) * D;
+            for (int cch = 0; cch < kDH / kCW; ++cch) {
+                const int col = kh * kDH + cch * kCW;
+                uint32_t rr[kCW];
+                tmem_ld_n<kCW>(tmem + lane_addr + kOCol + col, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < kCW; i += 4)
+                    *reinterpret_cast<float4*>(prow + col + i) = make_float4(
+                        __uint_as_float(rr[i]) * g, __uint_as_float(rr[i + 1]) * g,
+                        __uint_as_float(rr[i + 2]) * g, __uint_as_float(rr[i + 3]) * g);
+            }
+            if (kh == 0) {
+                cg.part[kRows * D + r] = m;
+                cg.part[kRows * D + kRows + r] = l;
+            }
+        } else if (ok) {
             // not PT: l sums the weights the MMA used, so O / l is the weighted mean
             // of the value codes; PT: l sums p itself and O carries lift / E
             const float f = l > 0.f ? (PT ? e_run / lift : vconst) / l : 0.f;
@@ -946,9 +972,294 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
     }
 
     __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
+    // every copy and MMA has completed: the barriers' memory may take other
+    // data in the next piece (whose layout may differ)
+    if (tid == 0)
+        for (int i = 0; i < C::kNumBars; ++i) mbar_inval(bar(i));
+}
+
+// Geometry of query tile x of a sequence with chunk length nq and context
+// ctx_raw (its query rows from q0), KV head h, with all of its key tiles; false
+// when the tile holds no query (or its chunk is longer than the context,
+// reported when `report_errors`).  split: the tile takes split e4m3 operands
+// (some row sees fewer than kSplitKeys keys, or forced).
+template <int D, bool BF16, bool PT>
+__device__ __forceinline__ bool geo_of(const PrefillParams& p, int q0, int nq, int ctx_raw, int x,
+                                       bool report_errors, CtaGeo& cg, bool& split) {
+    cg.q0 = q0;
+    cg.nq = nq;
+    const int TPT = kRows / p.G;                        // query tokens per tile
+    cg.tok0 = x * TPT;
+    cg.t0 = 0;
+    cg.n_tiles = 0;
+    cg.part = nullptr;
+    split = false;
+    if (cg.tok0 >= nq) return false;
+    int ctx = ctx_raw;
+    if (ctx > p.max_blocks_per_seq * kPage) {
+        if (report_errors) report(p.err, FP8KV_ERR_BAD_INDEX);
+        ctx = p.max_blocks_per_seq * kPage;
+    }
+    cg.ctx = ctx;
+    cg.pos_base = ctx - nq;                             // position of the chunk's first query
+    const int n_tok = min(TPT, nq - cg.tok0);
+    const int pos_max = cg.pos_base + cg.tok0 + n_tok - 1;
+    const int pos_min = cg.pos_base + cg.tok0;
+    if (pos_min < 0) {                                  // chunk longer than the context
+        if (report_errors) report(p.err, FP8KV_ERR_BAD_INDEX);
+        return false;
+    }
+    int keys;
+    if constexpr (BF16) {
+        keys = PCfg<D, true, false, false>::kKeys;      // bf16: no PT
+    } else {
+        split = p.split == FP8KV_PREFILL_SPLIT_ALWAYS ||
+                (p.split == 0 && pos_min + 1 < kSplitKeys);
+        keys = split ? PCfg<D, false, true, PT>::kKeys : PCfg<D, false, false, PT>::kKeys;
+    }
+    cg.n_tiles = pos_max / keys + 1;
+    return true;
+}
+
+// geo_of for query tile x of sequence b, KV head h.
+template <int D, bool BF16, bool PT>
+__device__ bool tile_geo(const PrefillParams& p, int b, int h, int x, bool report_errors,
+                         CtaGeo& cg, bool& split) {
+    cg.b = b;
+    cg.h = h;
+    const int q0 = p.cu_seqlens_q[b];
+    return geo_of<D, BF16, PT>(p, q0, p.cu_seqlens_q[b + 1] - q0, p.context_lens[b], x,
+                               report_errors, cg, split);
+}
+
+// Key tiles of query tile x of a sequence (nq, ctx) (0 for an empty tile): the
+// unit of the balanced split.
+template <int D, bool BF16, bool PT>
+__device__ __forceinline__ int tile_cost(const PrefillParams& p, int nq, int ctx, int x,
+                                         bool report_errors = false) {
+    CtaGeo cg;
+    bool split;
+    return geo_of<D, BF16, PT>(p, 0, nq, ctx, x, report_errors, cg, split) ? cg.n_tiles : 0;
+}
+
+// Balanced split (persistent launch): the key tiles of every query tile, in the
+// order (sequence, KV head, query tile), form one list of W units; CTA c of n
+// takes units [c W / n, (c + 1) W / n).  A query tile cut between CTAs leaves a
+// partial per piece; the last of its CTAs to finish merges them.
+struct Piece {
+    int b, h, x;        // the query tile
+    int t0, n;          // its key tiles taken
+    int cf, cl;         // first and last CTA holding a piece of the tile
+};
+constexpr int kMaxPieces = 16;     // pieces planned at a time
+struct Plan {
+    long long W, w0, w1;           // all units; this CTA's range
+    long long S;                   // first unit of the next query tile to look at
+    int b, h, x;                   // that query tile
+    int n_pieces;
+    int last;                      // the merge of the current piece falls to this CTA
+    Piece pieces[kMaxPieces];
+};
+
+// CTA owning unit u under the split of W units over n CTAs.
+__device__ __forceinline__ int cta_of(long long u, long long W, int n) {
+    return static_cast<int>(((u + 1) * n + W - 1) / W) - 1;
+}
+
+// Warp 0 of the CTA: the next pieces of this CTA's range into pl (n_pieces 0
+// when the range is done).  First call (pl.S < 0): W, the range and its first
+// query tile.
+template <int D, bool BF16, bool PT>
+__device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int lane) {
+    const int TPT = kRows / p.G;
+    const int n = gridDim.x, c = blockIdx.x;
+    if (pl.S < 0) {
+        long long W = 0;                               // every sequence's units
+        for (int b = 0; b < p.B; ++b) {
+            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b], ctx = p.context_lens[b];
+            const int nqt = (nq + TPT - 1) / TPT;
+            int cost = 0;
+            for (int x0 = 0; x0 < nqt; x0 += 32)       // CTA 0 reports bad geometry
+                cost += x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane, c == 0)
+                                        : 0;
+            for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
+            W += static_cast<long long>(cost) * p.Hkv;
+        }
+        const long long w0 = W * c / n, w1 = W * (c + 1) / n;
+        // the query tile holding unit w0
+        long long S = 0;
+        int b = 0, h = 0, x = 0;
+        bool found = w0 >= w1;
+        for (; b < p.B && !found; ++b) {
+            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b], ctx = p.context_lens[b];
+            const int nqt = (nq + TPT - 1) / TPT;
+            int cost = 0;
+            for (int x0 = 0; x0 < nqt; x0 += 32)
+                cost += x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane) : 0;
+            for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
+            if (S + static_cast<long long>(cost) * p.Hkv <= w0) {
+                S += static_cast<long long>(cost) * p.Hkv;
+                continue;
+            }
+            h = static_cast<int>((w0 - S) / cost);
+            S += static_cast<long long>(h) * cost;
+            // query tiles of (b, h) 32 at a time: the first whose units pass w0
+            for (int x0 = 0; x0 < nqt; x0 += 32) {
+                const int ci = x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane) : 0;
+                int inc = ci;                          // inclusive prefix over the lanes
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += v;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, S + inc > w0);
+                if (hit) {
+                    const int l0 = __ffs(hit) - 1;
+                    x = x0 + l0;
+                    S += __shfl_sync(0xffffffffu, inc - ci, l0);
+                    break;
+                }
+                S += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            found = true;
+            break;
+        }
+        if (lane == 0) {
+            pl.W = W;
+            pl.w0 = w0;
+            pl.w1 = w1;
+            pl.S = found && w0 < w1 ? S : w1;          // nothing to do: S = w1
+            pl.b = b;
+            pl.h = h;
+            pl.x = x;
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        int np = 0;
+        long long S = pl.S;
+        int b = pl.b, h = pl.h, x = pl.x;
+        int nq = 0, ctx = 0, seq = -1;                 // the sequence b's chunk and context
+        while (np < kMaxPieces && S < pl.w1 && b < p.B) {
+            if (seq != b) {
+                nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
+                ctx = p.context_lens[b];
+                seq = b;
+            }
+            if (x >= (nq + TPT - 1) / TPT) {           // next KV head, next sequence
+                x = 0;
+                if (++h >= p.Hkv) {
+                    h = 0;
+                    ++b;
+                }
+                continue;
+            }
+            const int cost = tile_cost<D, BF16, PT>(p, nq, ctx, x);
+            if (cost > 0) {
+                const long long a = S > pl.w0 ? S : pl.w0;
+                const long long e = S + cost < pl.w1 ? S + cost : pl.w1;
+                Piece& pc = pl.pieces[np++];
+                pc.b = b;
+                pc.h = h;
+                pc.x = x;
+                pc.t0 = static_cast<int>(a - S);
+                pc.n = static_cast<int>(e - a);
+                pc.cf = cta_of(S, pl.W, gridDim.x);
+                pc.cl = cta_of(S + cost - 1, pl.W, gridDim.x);
+            }
+            S += cost;
+            ++x;
+        }
+        // the range's last piece, when cut, goes first: its partner pieces were
+        // taken early by the next CTA, so the merge happens early too instead of
+        // at the end of the launch
+        if (S >= pl.w1 && np > 1 && pl.pieces[np - 1].cf != pl.pieces[np - 1].cl) {
+            const Piece last = pl.pieces[np - 1];
+            for (int i = np - 1; i > 0; --i) pl.pieces[i] = pl.pieces[i - 1];
+            pl.pieces[0] = last;
+        }
+        pl.S = S;
+        pl.b = b;
+        pl.h = h;
+        pl.x = x;
+        pl.n_pieces = np;
+    }
+    __syncwarp();
+}
+
+// Partial slot of CTA c's piece of a query tile whose pieces run from CTA cf:
+// the tile is the last piece of cf (slot 2 cf + 1) and the first of the others.
+__device__ __forceinline__ float* part_slot(const PrefillParams& p, int c, int cf, int D) {
+    const int slot = c == cf ? 2 * c + 1 : 2 * c;
+    return p.ws_part + static_cast<size_t>(slot) * kRows * (D + 2);
+}
+
+// The output rows of a cut query tile from its pieces' partials (CTAs cf..cl):
+// out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M the largest m_i.  Every
+// thread of the CTA takes part (the body has finished, so its shared memory
+// holds the pieces' weights [cl - cf + 1][128]); each thread keeps 8 float4 loads
+// per piece in flight, as the partials come from L2.
+template <int D>
+__device__ __noinline__ void merge_pieces(const PrefillParams& p, const CtaGeo& cg, int cf,
+                                          int cl, float* wts) {
+    const int tid = threadIdx.x, nthreads = blockDim.x;
+    const int G = p.G;
+    if (tid < kRows) {
+        const int r = tid;
+        float M = kMaxInitP, L = 0.f;
+        for (int c = cf; c <= cl; ++c)
+            M = fmaxf(M, __ldcg(part_slot(p, c, cf, D) + kRows * D + r));
+        for (int c = cf; c <= cl; ++c) {
+            const float* ps = part_slot(p, c, cf, D);
+            const float e = ex2p(__ldcg(ps + kRows * D + r) - M);
+            wts[(c - cf) * kRows + r] = e;
+            L += __ldcg(ps + kRows * D + kRows + r) * e;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int c = cf; c <= cl; ++c) wts[(c - cf) * kRows + r] *= inv;
+    }
+    __syncthreads();
+    constexpr int kRow4 = D / 4;                        // float4 of a row
+    constexpr int kN = kRows * kRow4;
+    constexpr int kU = 8;
+    for (int base = tid; base < kN; base += kU * nthreads) {
+        float4 acc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = cf; c <= cl; ++c) {
+            const float4* ps = reinterpret_cast<const float4*>(part_slot(p, c, cf, D));
+            float4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = base + u * nthreads;
+                v[u] = i < kN ? __ldcg(ps + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = base + u * nthreads;
+                const float wgt = i < kN ? wts[(c - cf) * kRows + i / kRow4] : 0.f;
+                acc[u].x += v[u].x * wgt;
+                acc[u].y += v[u].y * wgt;
+                acc[u].z += v[u].z * wgt;
+                acc[u].w += v[u].w * wgt;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = base + u * nthreads;
+            if (i >= kN) continue;
+            const int r = i / kRow4, col = (i % kRow4) * 4;
+            const int tk = cg.tok0 + r / G;
+            if (tk >= cg.nq) continue;
+            const size_t o = (static_cast<size_t>(cg.q0 + tk) * p.Hq + cg.h * G + r % G) * D + col;
+            if (p.out_bf16) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+                *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+                *reinterpret_cast<__nv_bfloat162*>(dst + 2) =
+                    __floats2bfloat162_rn(acc[u].z, acc[u].w);
+            } else {
+                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = acc[u];
+            }
+        }
     }
 }
 
@@ -956,48 +1267,96 @@ template <int D, bool TWO_LEVEL, bool BF16, bool PT>
 __global__ void __launch_bounds__(PCfg<D, BF16, false, PT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using C1 = PCfg<D, BF16, false, PT>;               // thread roles are those of both bodies
     extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ Plan s_plan;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x;
-    CtaGeo cg;
-    cg.b = blockIdx.z;
-    cg.h = blockIdx.y;
-    cg.q0 = p.cu_seqlens_q[cg.b];
-    cg.nq = p.cu_seqlens_q[cg.b + 1] - cg.q0;
-    const int TPT = kRows / p.G;                        // query tokens per tile
-    // tiles go out last-first: later query tiles see more keys (causal), so the
-    // heaviest CTAs take the first wave and the lightest fill the partial last one
-    cg.tok0 = (gridDim.x - 1 - blockIdx.x) * TPT;
-    if (cg.tok0 >= cg.nq) return;
-    int ctx = p.context_lens[cg.b];
-    if (ctx > p.max_blocks_per_seq * kPage) {
-        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-        ctx = p.max_blocks_per_seq * kPage;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kMmaWarp = C1::kSoftWarps + 1;
+    if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), C1::kTmemCols);
+    const bool persistent = p.ws_part != nullptr;
+    if (tid == 0) {
+        s_plan.S = -1;
+        s_plan.n_pieces = 0;
     }
-    cg.ctx = ctx;
-    cg.pos_base = ctx - cg.nq;                          // position of the chunk's first query
-    const int n_tok = min(TPT, cg.nq - cg.tok0);
-    const int pos_max = cg.pos_base + cg.tok0 + n_tok - 1;
-    const int pos_min = cg.pos_base + cg.tok0;
-    if (pos_min < 0) {                                  // chunk longer than the context
-        if (tid == 0) report(p.err, FP8KV_ERR_BAD_INDEX);
-        return;
-    }
-    if constexpr (BF16) {
-        cg.n_tiles = pos_max / PCfg<D, true, false, false>::kKeys + 1;   // bf16: no PT
-        prefill_body<D, TWO_LEVEL, true, PT, false>(kmap, vmap, p, smem, cg);
-    } else {
-        // split operands where a row of the CTA sees fewer than kSplitKeys keys
-        const bool split = p.split == FP8KV_PREFILL_SPLIT_ALWAYS ||
-                           (p.split == 0 && pos_min + 1 < kSplitKeys);
-        if (split) {
-            cg.n_tiles = pos_max / PCfg<D, false, true, PT>::kKeys + 1;
-            prefill_body<D, TWO_LEVEL, false, PT, true>(kmap, vmap, p, smem, cg);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    int next = 0;                                       // next planned piece
+    bool grid_done = false;
+    for (;;) {
+        CtaGeo cg;
+        bool split = false, valid = false;
+        if (!persistent) {
+            if (grid_done) break;
+            grid_done = true;
+            // tiles go out last-first: later query tiles see more keys (causal), so
+            // the heaviest CTAs take the first wave and the lightest the last one
+            valid = tile_geo<D, BF16, PT>(p, blockIdx.z, blockIdx.y,
+                                          gridDim.x - 1 - blockIdx.x, tid == 0, cg, split);
+            if (!valid) break;
         } else {
-            cg.n_tiles = pos_max / PCfg<D, false, false, PT>::kKeys + 1;
-            prefill_body<D, TWO_LEVEL, false, PT, false>(kmap, vmap, p, smem, cg);
+            if (next == s_plan.n_pieces) {
+                __syncthreads();                        // every thread has read the pieces
+                if (warp == 0) plan_pieces<D, BF16, PT>(p, s_plan, lane);
+                __syncthreads();
+                next = 0;
+                if (s_plan.n_pieces == 0) break;
+            }
+            const Piece pc = s_plan.pieces[next++];
+            valid = tile_geo<D, BF16, PT>(p, pc.b, pc.h, pc.x, tid == 0 && pc.cf == blockIdx.x,
+                                          cg, split);
+            if (!valid) continue;                       // (planned tiles always hold queries)
+            cg.t0 = pc.t0;
+            cg.n_tiles = pc.n;
+            if (pc.cf != pc.cl) cg.part = part_slot(p, blockIdx.x, pc.cf, D);
         }
+        if constexpr (BF16) {
+            prefill_body<D, TWO_LEVEL, true, PT, false>(kmap, vmap, p, smem, cg, &s_tmem, &s_abort);
+        } else if (split) {
+            prefill_body<D, TWO_LEVEL, false, PT, true>(kmap, vmap, p, smem, cg, &s_tmem, &s_abort);
+        } else {
+            prefill_body<D, TWO_LEVEL, false, PT, false>(kmap, vmap, p, smem, cg, &s_tmem,
+                                                         &s_abort);
+        }
+        if (!persistent) continue;
+        // ---- a piece of a cut query tile: the last CTA of its pieces to get here
+        // merges their partials into the output (the piece and its geometry are
+        // read again rather than kept in registers across the body)
+        const Piece pc = s_plan.pieces[next - 1];
+        const int cf = pc.cf, cl = pc.cl;
+        if (cf == cl) continue;
+        tile_geo<D, BF16, PT>(p, pc.b, pc.h, pc.x, false, cg, split);
+        __threadfence();                                // this CTA's partial, device-wide
+        __syncthreads();
+        if (tid == 0) {
+            const int old = atomicAdd(p.ws_count + cf, 1);
+            s_plan.last = old == cl - cf;
+            if (s_plan.last) atomicExch(p.ws_count + cf, 0);   // ready for the next call
+        }
+        __syncthreads();
+        if (s_plan.last) {                              // (uniform over the CTA)
+            // the pieces' weights fit the shared memory for any GPU of up to
+            // (dynamic shared memory) / 512 SMs
+            constexpr int kSmemBytes = prefill_smem<D, BF16, PT>();
+            if ((cl - cf + 1) * kRows * 4 > kSmemBytes - 1024) {
+                if (tid == 0) report(p.err, FP8KV_ERR_UNSUPPORTED);
+                continue;
+            }
+            __threadfence();
+            merge_pieces<D>(p, cg, cf, cl, reinterpret_cast<float*>(smem));
+            __syncthreads();                            // the weights are read
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(s_tmem, C1::kTmemCols);
     }
 }
 
@@ -1009,7 +1368,8 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmem, attr_done);
     if (e != cudaSuccess) return e;
-    dim3 grid(grid_x, p.Hkv, p.B);
+    // persistent (balanced split): grid_x CTAs, one per SM
+    const dim3 grid = p.ws_part != nullptr ? dim3(grid_x, 1, 1) : dim3(grid_x, p.Hkv, p.B);
     kern<<<grid, PCfg<D, BF16, false, PT>::kThreads, kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }

@@ -264,6 +264,44 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
                        int out_dtype, int32_t* err_flag, void* cuda_stream);
 
 /*
+ * fp8kv_prefill_attn_ws -- fp8kv_prefill_attn with a device workspace, which
+ * lets a launch with more query tiles than the GPU has SMs (B * Hkv *
+ * ceil(max_seqlen_q * G / 128) > SMs) run as one persistent CTA per SM that
+ * takes an equal share of all (query tile, key tile) work instead of one CTA per
+ * query tile (whose last wave leaves SMs idle).  A query tile cut between CTAs
+ * leaves an fp32 partial per piece (O, its running max and sum, as in the
+ * split decode's merge); the last CTA of the tile to finish merges them.  The
+ * result is the same computation up to fp32 summation order.  Smaller launches
+ * ignore the workspace.
+ *
+ *   workspace        device memory, 16-byte aligned, workspace_bytes >=
+ *                    fp8kv_prefill_workspace_bytes(D) (else FP8KV_ERR_WORKSPACE):
+ *                    a counter per CTA, then the partials.  It must be zero
+ *                    before its first use; every call that ends without error
+ *                    leaves its counters zero again.  Calls that may run at the
+ *                    same time (other streams) need separate workspaces.  NULL:
+ *                    exactly fp8kv_prefill_attn.
+ * Other arguments, supported shapes and errors: fp8kv_prefill_attn.
+ */
+int fp8kv_prefill_attn_ws(const void* q, const int32_t* cu_seqlens_q, int max_seqlen_q,
+                          const void* k_cache, const void* v_cache, int kv_dtype, int scale_mode,
+                          const float* k_scale, const float* v_scale,
+                          const float* k_scale_cache, const float* v_scale_cache, float q_scale,
+                          float prob_scale, const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                          int64_t num_blocks, float softmax_scale, int flags, void* workspace,
+                          size_t workspace_bytes, void* out, int out_dtype, int32_t* err_flag,
+                          void* cuda_stream);
+
+/*
+ * fp8kv_prefill_workspace_bytes -- *bytes = the workspace fp8kv_prefill_attn_ws
+ * needs at head_dim D on the current device (2 x SMs x 128 x (D + 2) floats of
+ * partials plus the counters: 40 MB at D 256 on 152 SMs).  D outside {64, 128,
+ * 256}: FP8KV_ERR_UNSUPPORTED.
+ */
+int fp8kv_prefill_workspace_bytes(int D, size_t* bytes);
+
+/*
  * fp8kv_quantize_e4m3 -- the cache writer's encoder on its own: out[i] =
  * e4m3_rn_satfinite(fp32(x[i] / scale)) for n fp32 values (device arrays).
  * [PR] "코드 분석" (torch.float8_e4m3fn storage).  A zero scale writes code 0.

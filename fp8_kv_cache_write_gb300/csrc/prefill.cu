@@ -78,7 +78,8 @@ struct Soft {
     static constexpr float kLift = SPLIT ? 256.f : (PT ? 32.f : 1.f);
 };
 
-template <int D, bool BF16, bool SPLIT, bool PT>
+// WIDE: four softmax parts per row (per-token-head scales, two-level off)
+template <int D, bool BF16, bool SPLIT, bool WIDE>
 struct PCfg {
     // e4m3 tiles hold 128 keys (8 pages), bf16 and split tiles 64 keys (4 pages):
     // every P row is 128 bytes (bf16: 64 weights; split: 64 hi + 64 lo weights)
@@ -112,9 +113,10 @@ struct PCfg {
     // memory).  Two, except: per-token-head scales, whose column factors make
     // the softmax the longest stage, take four (32 keys of a single tile, 16 of
     // a split one) so that four warps per scheduler hide each other's
-    // latencies; bf16 at D 256 takes one (its tiles leave no shared memory for
-    // the exchange).
-    static constexpr int kParts = (BF16 && D == 256) ? 1 : (PT ? 4 : 2);
+    // latencies (not with two-level accumulation, whose extra registers spill
+    // at the 96 a thread of 19 warps gets); bf16 at D 256 takes one (its tiles
+    // leave no shared memory for the exchange).
+    static constexpr int kParts = (BF16 && D == 256) ? 1 : (WIDE ? 4 : 2);
     static constexpr int kSoftWarps = 4 * kParts;
     static constexpr int kThreads = 32 * (kSoftWarps + 3);   // + K loader, MMA, V loader
     static constexpr int kOffPMax = kOffOnes2;               // [2][kParts][128] partial maxima
@@ -140,14 +142,14 @@ struct PCfg {
 };
 
 // Dynamic shared memory of the kernel: the larger of its two operand layouts.
-template <int D, bool BF16, bool PT>
+template <int D, bool BF16, bool WIDE>
 __host__ __device__ constexpr int prefill_smem() {
-    using C1 = PCfg<D, BF16, false, PT>;
+    using C1 = PCfg<D, BF16, false, WIDE>;
     static_assert(C1::kPanelB == 128 || C1::kPanelB == 64, "panel rows of 64 or 128 bytes");
     if constexpr (BF16) {
         return C1::kSmem;
     } else {
-        using C2 = PCfg<D, false, true, PT>;
+        using C2 = PCfg<D, false, true, WIDE>;
         static_assert(C1::kThreads == C2::kThreads && C1::kTmemCols == C2::kTmemCols,
                       "single and split bodies run in one launch, on one allocation");
         return C1::kSmem > C2::kSmem ? C1::kSmem : C2::kSmem;
@@ -248,7 +250,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& kmap, const CUte
                                              const PrefillParams& p, uint8_t* smem,
                                              const CtaGeo& cg, const uint32_t* tmem_slot,
                                              volatile int* abort_flag) {
-    using C = PCfg<D, BF16, SPLIT, PT>;
+    using C = PCfg<D, BF16, SPLIT, PT && !TWO_LEVEL>;
     using S = Soft<SPLIT, PT>;
     constexpr int kKeys = C::kKeys;
     constexpr int kParts = C::kParts;
@@ -1015,7 +1017,7 @@ __device__ __forceinline__ bool geo_of(const PrefillParams& p, int q0, int nq, i
     } else {
         split = p.split == FP8KV_PREFILL_SPLIT_ALWAYS ||
                 (p.split == 0 && pos_min + 1 < kSplitKeys);
-        keys = split ? PCfg<D, false, true, PT>::kKeys : PCfg<D, false, false, PT>::kKeys;
+        keys = split ? PCfg<D, false, true, false>::kKeys : PCfg<D, false, false, false>::kKeys;
     }
     cg.n_tiles = pos_max / keys + 1;
     return true;
@@ -1264,10 +1266,10 @@ __device__ __noinline__ void merge_pieces(const PrefillParams& p, const CtaGeo& 
 }
 
 template <int D, bool TWO_LEVEL, bool BF16, bool PT>
-__global__ void __launch_bounds__(PCfg<D, BF16, false, PT>::kThreads, 1)
+__global__ void __launch_bounds__(PCfg<D, BF16, false, PT && !TWO_LEVEL>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-    using C1 = PCfg<D, BF16, false, PT>;               // thread roles are those of both bodies
+    using C1 = PCfg<D, BF16, false, PT && !TWO_LEVEL>;   // thread roles of both bodies
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -1342,7 +1344,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16, false, PT>::kThreads, 1)
         if (s_plan.last) {                              // (uniform over the CTA)
             // the pieces' weights fit the shared memory for any GPU of up to
             // (dynamic shared memory) / 512 SMs
-            constexpr int kSmemBytes = prefill_smem<D, BF16, PT>();
+            constexpr int kSmemBytes = prefill_smem<D, BF16, PT && !TWO_LEVEL>();
             if ((cl - cf + 1) * kRows * 4 > kSmemBytes - 1024) {
                 if (tid == 0) report(p.err, FP8KV_ERR_UNSUPPORTED);
                 continue;
@@ -1364,13 +1366,13 @@ template <int D, bool TWO, bool BF16, bool PT>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, int grid_x, cudaStream_t stream) {
     auto kern = prefill_kernel<D, TWO, BF16, PT>;
-    constexpr int kSmem = prefill_smem<D, BF16, PT>();
+    constexpr int kSmem = prefill_smem<D, BF16, PT && !TWO>();
     static unsigned long long attr_done[64] = {};
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmem, attr_done);
     if (e != cudaSuccess) return e;
     // persistent (balanced split): grid_x CTAs, one per SM
     const dim3 grid = p.ws_part != nullptr ? dim3(grid_x, 1, 1) : dim3(grid_x, p.Hkv, p.B);
-    kern<<<grid, PCfg<D, BF16, false, PT>::kThreads, kSmem, stream>>>(kmap, vmap, p);
+    kern<<<grid, PCfg<D, BF16, false, PT && !TWO>::kThreads, kSmem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 

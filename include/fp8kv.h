@@ -245,6 +245,12 @@ int fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, void*
  *                  prob_scale), which meets max-abs 1e-2 on N(0,1) data at any
  *                  length.  FP8KV_PREFILL_SPLIT_ALWAYS / _NEVER force one of
  *                  them; setting both is FP8KV_ERR_INVALID, as is any other bit.
+ *                  The 8192-key threshold holds for N(0,1)-like data; with
+ *                  per-token-head scales on data with x20 outlier channels
+ *                  single operands lost up to ~0.3 of a channel's value rms on
+ *                  9000-key rows (many small weights underflow e4m3 once the V
+ *                  scales are folded in), split operands ~1.5e-2: force
+ *                  SPLIT_ALWAYS for such data.
  *   out            [Tq][Hq][D] fp32 or bf16.
  * Supported: e4m3 cache (every scale mode) and its bf16 twin (bf16 Q, P and
  * cache, kind::f16; scales ignored), D in {64, 128, 256}, Hq / Hkv dividing 128.

@@ -212,6 +212,12 @@ __device__ __forceinline__ int swz_off(int r, int cc) {
         return r * 64 + ((cc ^ ((r >> 1) & 3)) << 4);
 }
 
+// Orders this thread's generic-proxy view of memory (all state spaces) before its
+// later async-proxy accesses (bulk copies of data other threads stored).
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
 // Named barrier of the softmax warps only (the loader and MMA warps run on).
 __device__ __forceinline__ void soft_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -1034,14 +1040,20 @@ __device__ bool tile_geo(const PrefillParams& p, int b, int h, int x, bool repor
                                report_errors, cg, split);
 }
 
-// Key tiles of query tile x of a sequence (nq, ctx) (0 for an empty tile): the
-// unit of the balanced split.
-template <int D, bool BF16, bool PT>
-__device__ __forceinline__ int tile_cost(const PrefillParams& p, int nq, int ctx, int x,
-                                         bool report_errors = false) {
-    CtaGeo cg;
-    bool split;
-    return geo_of<D, BF16, PT>(p, 0, nq, ctx, x, report_errors, cg, split) ? cg.n_tiles : 0;
+// Key tiles of query tile x (TPT tokens) of a sequence whose chunk of nq queries
+// ends its context of ctx keys (already clamped to the page table): the unit of
+// the balanced split, 0 for an empty tile.  The same count as geo_of's, in
+// shifts (a tile is 128 keys, 64 for bf16 and split operands).
+template <bool BF16>
+__device__ __forceinline__ int tile_units(int nq, int ctx, int x, int TPT, int split_mode) {
+    const int tok0 = x * TPT;
+    if (tok0 >= nq) return 0;
+    const int pos_min = ctx - nq + tok0;
+    if (pos_min < 0) return 0;
+    const int pos_max = ctx - nq + min(tok0 + TPT, nq) - 1;
+    const bool split = !BF16 && (split_mode == FP8KV_PREFILL_SPLIT_ALWAYS ||
+                                 (split_mode == 0 && pos_min + 1 < kSplitKeys));
+    return (pos_max >> ((BF16 || split) ? 6 : 7)) + 1;
 }
 
 // Balanced split (persistent launch): the key tiles of every query tile, in the
@@ -1073,17 +1085,24 @@ __device__ __forceinline__ int cta_of(long long u, long long W, int n) {
 // query tile.
 template <int D, bool BF16, bool PT>
 __device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int lane) {
+    static_assert(PCfg<D, false, false, false>::kKeys == 128 &&
+                      PCfg<D, false, true, false>::kKeys == 64 &&
+                      PCfg<D, true, false, false>::kKeys == 64, "tile_units' shifts");
     const int TPT = kRows / p.G;
     const int n = gridDim.x, c = blockIdx.x;
+    const int max_ctx = p.max_blocks_per_seq * kPage;
     if (pl.S < 0) {
         long long W = 0;                               // every sequence's units
         for (int b = 0; b < p.B; ++b) {
-            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b], ctx = p.context_lens[b];
+            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
+            const int ctx = min(p.context_lens[b], max_ctx);
+            if (c == 0 && lane == 0 && nq > 0 &&       // CTA 0 reports bad geometry
+                (p.context_lens[b] > max_ctx || ctx < nq))
+                report(p.err, FP8KV_ERR_BAD_INDEX);
             const int nqt = (nq + TPT - 1) / TPT;
             int cost = 0;
-            for (int x0 = 0; x0 < nqt; x0 += 32)       // CTA 0 reports bad geometry
-                cost += x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane, c == 0)
-                                        : 0;
+            for (int x0 = 0; x0 < nqt; x0 += 32)
+                cost += x0 + lane < nqt ? tile_units<BF16>(nq, ctx, x0 + lane, TPT, p.split) : 0;
             for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
             W += static_cast<long long>(cost) * p.Hkv;
         }
@@ -1093,11 +1112,12 @@ __device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int l
         int b = 0, h = 0, x = 0;
         bool found = w0 >= w1;
         for (; b < p.B && !found; ++b) {
-            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b], ctx = p.context_lens[b];
+            const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
+            const int ctx = min(p.context_lens[b], max_ctx);
             const int nqt = (nq + TPT - 1) / TPT;
             int cost = 0;
             for (int x0 = 0; x0 < nqt; x0 += 32)
-                cost += x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane) : 0;
+                cost += x0 + lane < nqt ? tile_units<BF16>(nq, ctx, x0 + lane, TPT, p.split) : 0;
             for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
             if (S + static_cast<long long>(cost) * p.Hkv <= w0) {
                 S += static_cast<long long>(cost) * p.Hkv;
@@ -1107,7 +1127,7 @@ __device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int l
             S += static_cast<long long>(h) * cost;
             // query tiles of (b, h) 32 at a time: the first whose units pass w0
             for (int x0 = 0; x0 < nqt; x0 += 32) {
-                const int ci = x0 + lane < nqt ? tile_cost<D, BF16, PT>(p, nq, ctx, x0 + lane) : 0;
+                const int ci = x0 + lane < nqt ? tile_units<BF16>(nq, ctx, x0 + lane, TPT, p.split) : 0;
                 int inc = ci;                          // inclusive prefix over the lanes
                 for (int o = 1; o < 32; o <<= 1) {
                     const int v = __shfl_up_sync(0xffffffffu, inc, o);
@@ -1144,7 +1164,7 @@ __device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int l
         while (np < kMaxPieces && S < pl.w1 && b < p.B) {
             if (seq != b) {
                 nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
-                ctx = p.context_lens[b];
+                ctx = min(p.context_lens[b], max_ctx);
                 seq = b;
             }
             if (x >= (nq + TPT - 1) / TPT) {           // next KV head, next sequence
@@ -1155,7 +1175,7 @@ __device__ __noinline__ void plan_pieces(const PrefillParams& p, Plan& pl, int l
                 }
                 continue;
             }
-            const int cost = tile_cost<D, BF16, PT>(p, nq, ctx, x);
+            const int cost = tile_units<BF16>(nq, ctx, x, TPT, p.split);
             if (cost > 0) {
                 const long long a = S > pl.w0 ? S : pl.w0;
                 const long long e = S + cost < pl.w1 ? S + cost : pl.w1;
@@ -1202,7 +1222,7 @@ __device__ __forceinline__ float* part_slot(const PrefillParams& p, int c, int c
 // per piece in flight, as the partials come from L2.
 template <int D>
 __device__ __noinline__ void merge_pieces(const PrefillParams& p, const CtaGeo& cg, int cf,
-                                          int cl, float* wts) {
+                                          int cl, float* wts, uint32_t bar, int& bar_phase) {
     const int tid = threadIdx.x, nthreads = blockDim.x;
     const int G = p.G;
     if (tid < kRows) {
@@ -1221,6 +1241,54 @@ __device__ __noinline__ void merge_pieces(const PrefillParams& p, const CtaGeo& 
     }
     __syncthreads();
     constexpr int kRow4 = D / 4;                        // float4 of a row
+    if (cl == cf + 1) {
+        // two pieces (the usual cut): half a tile's rows of both partials at a time
+        // come into shared memory by bulk copies, which keep far more bytes in
+        // flight than loads; out = w0 * O0 + w1 * O1 from there
+        constexpr int kHalfRows = kRows / 2;
+        constexpr uint32_t kBytes = kHalfRows * D * 4;
+        const float4* st0 = reinterpret_cast<const float4*>(wts + 2 * kRows);
+        const float4* st1 = st0 + kHalfRows * kRow4;
+        const uint32_t dst0 = smem_addr(wts + 2 * kRows);
+        for (int hh = 0; hh < 2; ++hh) {
+            if (tid == 0) {
+                fence_proxy_async_all();                // the partials: other CTAs' stores
+                mbar_arrive_expect_tx(bar, 2 * kBytes);
+                bulk_load(dst0, part_slot(p, cf, cf, D) + hh * kHalfRows * D, kBytes, bar);
+                bulk_load(dst0 + kBytes, part_slot(p, cl, cf, D) + hh * kHalfRows * D, kBytes,
+                          bar);
+            }
+            // (the same answer in every thread: a bounded wait that ran out in one
+            // thread ends the merge in all of them)
+            const bool landed = __syncthreads_and(mbar_wait_bounded(bar, bar_phase & 1));
+            ++bar_phase;
+            if (!landed) {
+                if (tid == 0) report(p.err, FP8KV_ERR_TIMEOUT);
+                return;
+            }
+            for (int i = tid; i < kHalfRows * kRow4; i += nthreads) {
+                const int r = hh * kHalfRows + i / kRow4, col = (i % kRow4) * 4;
+                const int tk = cg.tok0 + r / G;
+                if (tk >= cg.nq) continue;
+                const float w0 = wts[r], w1 = wts[kRows + r];
+                const float4 a = st0[i], b = st1[i];
+                const float4 acc = make_float4(a.x * w0 + b.x * w1, a.y * w0 + b.y * w1,
+                                               a.z * w0 + b.z * w1, a.w * w0 + b.w * w1);
+                const size_t o =
+                    (static_cast<size_t>(cg.q0 + tk) * p.Hq + cg.h * G + r % G) * D + col;
+                if (p.out_bf16) {
+                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+                    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x, acc.y);
+                    *reinterpret_cast<__nv_bfloat162*>(dst + 2) =
+                        __floats2bfloat162_rn(acc.z, acc.w);
+                } else {
+                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = acc;
+                }
+            }
+            __syncthreads();                            // the staging is read
+        }
+        return;
+    }
     constexpr int kN = kRows * kRow4;
     constexpr int kU = 8;
     for (int base = tid; base < kN; base += kU * nthreads) {
@@ -1274,6 +1342,7 @@ __global__ void __launch_bounds__(PCfg<D, BF16, false, PT && !TWO_LEVEL>::kThrea
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ Plan s_plan;
+    __shared__ uint64_t s_merge_bar;                    // the merge's bulk copies
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1283,7 +1352,12 @@ __global__ void __launch_bounds__(PCfg<D, BF16, false, PT && !TWO_LEVEL>::kThrea
     if (tid == 0) {
         s_plan.S = -1;
         s_plan.n_pieces = 0;
+        if (persistent) {
+            mbar_init(smem_addr(&s_merge_bar), 1);
+            mbar_init_fence();
+        }
     }
+    int merge_phase = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1345,17 +1419,21 @@ __global__ void __launch_bounds__(PCfg<D, BF16, false, PT && !TWO_LEVEL>::kThrea
             // the pieces' weights fit the shared memory for any GPU of up to
             // (dynamic shared memory) / 512 SMs
             constexpr int kSmemBytes = prefill_smem<D, BF16, PT && !TWO_LEVEL>();
+            static_assert(2 * kRows * 4 + kRows * D * 4 <= kSmemBytes - 1024,
+                          "two pieces' weights and half rows fit the shared memory");
             if ((cl - cf + 1) * kRows * 4 > kSmemBytes - 1024) {
                 if (tid == 0) report(p.err, FP8KV_ERR_UNSUPPORTED);
                 continue;
             }
             __threadfence();
-            merge_pieces<D>(p, cg, cf, cl, reinterpret_cast<float*>(smem));
+            merge_pieces<D>(p, cg, cf, cl, reinterpret_cast<float*>(smem),
+                            smem_addr(&s_merge_bar), merge_phase);
             __syncthreads();                            // the weights are read
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (persistent && tid == 0) mbar_inval(smem_addr(&s_merge_bar));
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(s_tmem, C1::kTmemCols);

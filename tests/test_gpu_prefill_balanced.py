@@ -165,3 +165,23 @@ def test_balanced_prefill_workspace_checks():
     assert _q_tiles(w2) <= _sm_count()
     dev_c2, _ = _caches(w2)
     assert torch.equal(_run(w2, dev_c2, small), _run(w2, dev_c2, None))
+
+
+def test_balanced_prefill_tile_cut_into_many_pieces():
+    # one 60 000-key query tile among 160 one-tile sequences: the long tile's
+    # key tiles spread over ~110 CTAs, whose partials the last of them merges
+    ctx = (60000,) + (64,) * 160
+    chunk = (16,) + (16,) * 160
+    w = synth.prefill(seed=560, ctx=ctx, chunk=chunk, Hq=8, Hkv=1, D=128)
+    assert _q_tiles(w) > _sm_count()
+    dev_c, host_c = _caches(w)
+    ws = _workspace(128)
+    out = _run(w, dev_c, ws)
+    assert _counters_zero(ws)
+    units = [(t, h) for t in range(16) for h in range(8)] + \
+            [(t, h) for t in range(16, w.q.shape[0], 37) for h in (0, 5)]
+    ref = _oracle(w, host_c, units)
+    err = _max_err(w, out.cpu().numpy(), ref, units)
+    assert err <= PREFILL_TOL, err
+    grid = _run(w, dev_c, None)
+    assert float((out - grid).abs().max()) <= PREFILL_TOL

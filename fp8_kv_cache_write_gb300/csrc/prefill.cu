@@ -51,6 +51,13 @@
 //     row sums use the unfolded weights.
 //   * every mbarrier wait is bounded and watches a shared abort flag, so a stuck
 //     stage ends the kernel with FP8KV_ERR_TIMEOUT instead of hanging.
+//   * launch: one CTA per query tile, or (with a workspace, more query tiles than
+//     SMs) one persistent CTA per SM on an equal share of all (query tile, key
+//     tile) units.  A query tile cut between CTAs is computed in pieces over key
+//     ranges; each piece leaves its unnormalised O, running max m and sum l (the
+//     state the online softmax carries from tile to tile), and the last CTA of
+//     the tile to finish combines them, O = sum_i O_i 2^(m_i - M) / sum_i l_i
+//     2^(m_i - M).
 #include <cuda_runtime.h>
 
 #include "common.cuh"

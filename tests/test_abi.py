@@ -157,3 +157,39 @@ def test_prefill_rejects_bad_arguments_without_a_gpu(lib):
     assert call(max_q=-1) == -1
     assert call(B=0) == 0               # nothing to do, nothing launched
     assert call(max_q=0) == 0
+
+
+def test_prefill_with_workspace_rejects_bad_arguments_without_a_gpu(lib):
+    # fp8kv_prefill_attn_ws checks its arguments as fp8kv_prefill_attn does, before
+    # any workspace or device question
+    N = _null()
+
+    def call(B=1, Hq=8, Hkv=1, D=256, dtype=0, flags=0, max_q=128, ws_bytes=0):
+        return lib.fp8kv_prefill_attn_ws(N, N, max_q, N, N, dtype, 0, N, N, N, N, 1.0, 1.0, N, 4,
+                                         N, B, Hq, Hkv, D, 10, 0.0625, flags, N, ws_bytes, N, 0,
+                                         N, N)
+
+    assert call() == -1                 # null pointers
+    assert call(Hq=9) == -2
+    assert call(D=80) == -2
+    assert call(dtype=2) == -1
+    assert call(flags=8) == -1
+    assert call(flags=6) == -1
+    assert call(max_q=-1) == -1
+    assert call(B=0) == 0
+    assert call(max_q=0, ws_bytes=1 << 20) == 0
+
+
+def test_prefill_workspace_bytes_without_a_gpu(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.fp8kv_prefill_workspace_bytes(80, ctypes.byref(n)) == -2
+    assert lib.fp8kv_prefill_workspace_bytes(256, None) == -1
+    st = lib.fp8kv_prefill_workspace_bytes(256, ctypes.byref(n))
+    # no device here: FP8KV_ERR_CUDA; with one, two partial slots of
+    # 128 x (D + 2) floats per SM after the 256-byte-padded counters
+    assert st in (0, -4), st
+    if st == 0:
+        slot = 128 * (256 + 2) * 4
+        sms = [k for k in range(1, 1025)
+               if n.value == (k * 4 + 255) // 256 * 256 + 2 * k * slot]
+        assert sms, n.value

@@ -656,9 +656,12 @@ int fp8kv_prefill_attn_ws(const void* q, const int32_t* cu_seqlens_q, int max_se
     const int tpt = 128 / G;
     int grid_x = (max_seqlen_q + tpt - 1) / tpt;
     // more query tiles than SMs and a workspace: a persistent CTA per SM with
-    // the key tiles split evenly (no partly filled last wave)
+    // the key tiles split evenly (no partly filled last wave).  Each CTA plans
+    // its share by walking the sequences one after another (~1 us each), so
+    // batches of more than kBalancedMaxSeqs sequences keep one CTA per tile.
+    constexpr int kBalancedMaxSeqs = 8;
     const int n_sm = sm_count();
-    if (workspace != nullptr && n_sm > 0 &&
+    if (workspace != nullptr && n_sm > 0 && B <= kBalancedMaxSeqs &&
         static_cast<int64_t>(grid_x) * Hkv * B > n_sm) {
         if (workspace_bytes < prefill_ws_bytes(D, n_sm)) return FP8KV_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return FP8KV_ERR_INVALID;

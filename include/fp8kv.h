@@ -271,14 +271,17 @@ int fp8kv_prefill_attn(const void* q, const int32_t* cu_seqlens_q, int max_seqle
 
 /*
  * fp8kv_prefill_attn_ws -- fp8kv_prefill_attn with a device workspace, which
- * lets a launch with more query tiles than the GPU has SMs (B * Hkv *
- * ceil(max_seqlen_q * G / 128) > SMs) run as one persistent CTA per SM that
- * takes an equal share of all (query tile, key tile) work instead of one CTA per
- * query tile (whose last wave leaves SMs idle).  A query tile cut between CTAs
- * leaves an fp32 partial per piece (O, its running max and sum, as in the
- * split decode's merge); the last CTA of the tile to finish merges them.  The
- * result is the same computation up to fp32 summation order.  Smaller launches
- * ignore the workspace.
+ * lets a launch of at most 8 sequences with more query tiles than the GPU has
+ * SMs (B * Hkv * ceil(max_seqlen_q * G / 128) > SMs) run as one persistent CTA
+ * per SM that takes an equal share of all (query tile, key tile) work instead
+ * of one CTA per query tile (whose last wave leaves SMs idle).  A query tile
+ * cut between CTAs leaves an fp32 partial per piece (O, its running max and
+ * sum, as in the split decode's merge); the last CTA of the tile to finish
+ * merges them.  Each piece rounds its e4m3 weights against its own running
+ * maximum, so results differ from one CTA per tile within the rounding of FP8
+ * attention.  Other launches (no more query tiles than SMs, or more than 8
+ * sequences: every CTA plans its share by walking the sequences one after
+ * another) ignore the workspace.
  *
  *   workspace        device memory, 16-byte aligned, workspace_bytes >=
  *                    fp8kv_prefill_workspace_bytes(D) (else FP8KV_ERR_WORKSPACE):

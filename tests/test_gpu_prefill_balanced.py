@@ -168,10 +168,11 @@ def test_balanced_prefill_workspace_checks():
 
 
 def test_balanced_prefill_tile_cut_into_many_pieces():
-    # one 60 000-key query tile among 160 one-tile sequences: the long tile's
-    # key tiles spread over ~110 CTAs, whose partials the last of them merges
-    ctx = (60000,) + (64,) * 160
-    chunk = (16,) + (16,) * 160
+    # one 60 000-key query tile beside 7 sequences of 25 short query tiles each
+    # (the balanced launch takes at most 8 sequences): the long tile's key
+    # tiles spread over ~60 CTAs, whose partials the last of them merges
+    ctx = (60000,) + (400,) * 7
+    chunk = (16,) + (400,) * 7
     w = synth.prefill(seed=560, ctx=ctx, chunk=chunk, Hq=8, Hkv=1, D=128)
     assert _q_tiles(w) > _sm_count()
     dev_c, host_c = _caches(w)

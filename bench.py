@@ -865,6 +865,16 @@ def _extra_prefill(fk, synth, dev, stream, emit):
             if kv == E4 and not two and split == "auto" and _CPU_BASELINE:
                 line["cpu_baseline"] = _oracle_prefill_baseline(w)
             emit(line)
+            if kv == E4 and split == "auto":
+                # the same call with one CTA per query tile (no workspace): what the
+                # balanced persistent launch gains
+                fn = lambda i, kc=kc, vc=vc, two=two: fk.prefill_attn(
+                    q, cu, w.max_seqlen_q, kc, vc, bt, cl, kv_dtype=E4, k_scale=one,
+                    v_scale=one, two_level=two, out=out, workspace=None)
+                ms1 = _time_graph(fn, 10, stream)
+                emit({"extra": "prefill_chunk4096_ctx32768_d256", "kv": name, "two_level": two,
+                      "split": split, "launch": "one CTA per query tile", "ms": ms1,
+                      "tflops": flops / ms1 / 1e9})
         del kc, vc
         torch.cuda.empty_cache()
     # the same chunk over a per-token-head e4m3 cache (scales computed at write time)
